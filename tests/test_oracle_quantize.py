@@ -1,0 +1,242 @@
+"""Pins of the oracle's quantizer (CPU only): closed forms, invariants, statistics."""
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import formats as F
+from oracle import quantize as Q
+from oracle.amax import AmaxState
+
+
+def bf16(a):
+    """Round float values to bf16 and return them as float32 (input preparation only)."""
+    return torch.from_numpy(np.asarray(a, dtype=np.float32)).to(torch.bfloat16).float().numpy()
+
+
+def test_global_encode_scale_closed_forms():
+    assert Q.global_encode_scale(2688.0, "E4M3") == 1.0
+    assert Q.global_encode_scale(1.0, "E4M3") == 2688.0
+    assert Q.global_encode_scale(1.0, "UE5M3") == 2688.0
+    assert Q.global_encode_scale(1.0, "E1M6") == np.float32(23.8125)
+    assert Q.global_encode_scale(0.0, "E4M3") == 1.0
+    assert Q.global_encode_scale(1e-45, "E4M3") == np.finfo(np.float32).max
+    assert Q.global_encode_scale(123.0, "E8M0") == 1.0
+    assert Q.global_encode_scale(3.0, "E4M3") == np.float32(896.0)
+    with pytest.raises(Q.NonFiniteAmax):
+        Q.global_encode_scale(float("inf"), "E4M3")
+    with pytest.raises(Q.NonFiniteAmax):
+        Q.global_encode_scale(float("nan"), "UE5M3")
+
+
+def test_all_ones_block_closed_form():
+    # x = 1 everywhere, fresh amax 1: s_enc = 2688, s_real = 448 -> code 0x7E, y = 6 -> code 7
+    x = np.ones((4, 64), dtype=np.float32)
+    q = Q.quantize(x, "E4M3")
+    assert np.all(q["scales"] == 0x7E)
+    assert np.all(q["codes"] == 0x77)
+    assert np.array_equal(Q.dequantize(q["codes"], q["scales"], "E4M3", 1.0), x)
+    # negative ones: sign bit set in both nibbles
+    q = Q.quantize(-x, "E4M3")
+    assert np.all(q["codes"] == 0xFF)
+
+
+def test_mxfp4_closed_form():
+    # block max 4.0 -> floor(log2 4) - 2 = 0 -> code 127, s_b = 1, y = x
+    x = np.zeros((1, 32), dtype=np.float32)
+    x[0, 0] = 4.0
+    x[0, 1:9] = [0.5, 1, 1.5, 2, 3, -4, -6, 0.25]
+    q = Q.quantize(x, "E8M0")
+    assert q["scales"][0, 0] == 127
+    codes = Q.unpack(q["codes"])[0]
+    assert list(codes[:9]) == [6, 1, 2, 3, 4, 5, 0xE, 0xF, 0]
+    # block max 100 -> floor(log2 100) = 6 -> code 131, s_b = 16, y = 6.25 -> 6
+    x[0, 0] = 100.0
+    q = Q.quantize(x, "E8M0")
+    assert q["scales"][0, 0] == 131
+    assert Q.unpack(q["codes"])[0][0] == 7
+
+
+def test_nibble_order_and_signed_zero():
+    x = np.zeros((1, 16), dtype=np.float32)
+    x[0, 0] = 6.0
+    x[0, 1] = -0.0
+    x[0, 2] = -1e-3   # rounds to zero, keeps its sign
+    x[0, 3] = 3.0
+    q = Q.quantize(x, "E4M3", global_amax=6.0)
+    assert q["codes"][0, 0] == (0x7 | (0x8 << 4))
+    assert q["codes"][0, 1] == (0x8 | (0x5 << 4))
+
+
+def test_zero_and_flushed_blocks():
+    x = np.zeros((2, 32), dtype=np.float32)
+    x[1, :16] = -1e-6          # block amax far below the global amax: scale flushes to 0
+    x[1, 16] = 1.0
+    q = Q.quantize(x, "E4M3")
+    assert np.all(q["scales"][0] == 0)
+    assert q["scales"][1, 0] == 0
+    assert np.all(Q.unpack(q["codes"])[1, :16] == 0x8)
+    assert np.all(Q.unpack(q["codes"])[0] == 0)
+
+
+def _data(seed, shape, outliers=0.01):
+    rng = np.random.default_rng(seed)
+    x = rng.standard_normal(shape).astype(np.float32)
+    m = rng.random(shape) < outliers
+    x[m] *= 50
+    return bf16(x)
+
+
+@pytest.mark.parametrize("fmt", ["E4M3", "UE5M3", "E8M0"])
+def test_block_max_code_invariant(fmt):
+    # Every block whose scale is non-zero and not subnormal contains |code| = 6
+    # (E4M3/UE5M3: scale rounding error <= 1/16 puts y_max above 5) or
+    # |code| in {4, 6} (E8M0: y_max in [4, 8)).
+    x = _data(0, (256, 512))
+    q = Q.quantize(x, fmt)
+    G = Q.group_size(fmt)
+    mag = (Q.unpack(q["codes"]) & 7).reshape(256, 512 // G, G).max(axis=2)
+    s = Q.scale_values(q["scales"], fmt)
+    if fmt == "E8M0":
+        assert np.all(np.isin(mag, [6, 7]))
+    else:
+        normal = s >= {"E4M3": 2.0 ** -6, "UE5M3": 2.0 ** -14}[fmt]
+        assert normal.mean() > 0.99
+        assert np.all(mag[normal] == 7)
+
+
+@pytest.mark.parametrize("fmt", ["E4M3", "UE5M3", "E8M0"])
+def test_requantize_fixed_point(fmt):
+    # quantize(bf16(dequantize(q))) == q under the same global amax, on blocks with
+    # a normal scale
+    x = _data(1, (128, 512))
+    q = Q.quantize(x, fmt)
+    xd = bf16(Q.dequantize(q["codes"], q["scales"], fmt, q["amax"]))
+    q2 = Q.quantize(xd, fmt, global_amax=q["amax"])
+    G = Q.group_size(fmt)
+    s = Q.scale_values(q["scales"], fmt)
+    normal = s >= {"E4M3": 2.0 ** -6, "UE5M3": 2.0 ** -14, "E8M0": 0}[fmt]
+    assert np.array_equal(q2["scales"][normal], q["scales"][normal])
+    c1 = Q.unpack(q["codes"]).reshape(128, -1, G)[normal]
+    c2 = Q.unpack(q2["codes"]).reshape(128, -1, G)[normal]
+    assert np.array_equal(c1, c2)
+
+
+def test_ue5m3_equals_e4m3_where_e4m3_normal():
+    x = _data(2, (256, 256))
+    a = Q.quantize(x, "E4M3")
+    b = Q.quantize(x, "UE5M3")
+    sa = Q.scale_values(a["scales"], "E4M3")
+    sb = Q.scale_values(b["scales"], "UE5M3")
+    normal = (sa >= 2.0 ** -6) & (sa < 448)
+    assert normal.mean() > 0.99
+    assert np.array_equal(sa[normal], sb[normal])
+    ca = Q.unpack(a["codes"]).reshape(256, -1, 16)[normal]
+    cb = Q.unpack(b["codes"]).reshape(256, -1, 16)[normal]
+    assert np.array_equal(ca, cb)
+
+
+def test_stale_amax_e4m3_saturates_ue5m3_absorbs():
+    # stored amax 4x below the true one ("UE5M3 ..." blog, "Что сделали": the tensor
+    # maximum is refreshed once every 50 steps; large values must not be clipped)
+    x = _data(3, (64, 256))
+    g = float(np.max(np.abs(x))) / 4
+    a = Q.quantize(x, "E4M3", global_amax=g)
+    b = Q.quantize(x, "UE5M3", global_amax=g)
+    assert np.any(Q.scale_values(a["scales"], "E4M3") == 448.0)
+    assert np.all(Q.scale_values(b["scales"], "UE5M3") < 114688.0)
+    ea = np.abs(Q.dequantize(a["codes"], a["scales"], "E4M3", g) - x).max()
+    eb = np.abs(Q.dequantize(b["codes"], b["scales"], "UE5M3", g) - x).max()
+    assert eb < ea / 4
+
+
+def test_e1m6_narrow_range_direction():
+    # gonzo_ML #3986, "Форматы FP4": of the scale-format sweep only E1M6, the one
+    # with the narrowest range, fails.  Under the global scale a block flushes to
+    # zero when its scale rounds below half the smallest positive scale:
+    #   E1M6: 3.96875 * a_b / g < 1/64   (a_b/g < 1/254)
+    #   E4M3: 448 * a_b / g < 2^-10      (a_b/g < 2.2e-6)
+    #   UE5M3: 448 * a_b / g < 2^-18     (a_b/g < 8.5e-9)
+    # Rows whose scale spans four decades cross only E1M6's threshold.
+    rng = np.random.default_rng(2)
+    row_sig = 10.0 ** rng.uniform(-4, 0, 512)
+    x = bf16(rng.standard_normal((512, 1024)) * row_sig[:, None])
+    flushed = {}
+    for fmt in ("E4M3", "UE5M3", "E1M6"):
+        q = Q.quantize(x, fmt)
+        blk_nonzero = np.abs(x).reshape(512, -1, 16).max(axis=2) > 0
+        flushed[fmt] = float(np.mean((q["scales"] == 0) & blk_nonzero))
+    assert flushed["E4M3"] == 0 and flushed["UE5M3"] == 0
+    a_b = np.abs(x).reshape(512, -1, 16).max(axis=2)
+    expect = float(np.mean(a_b / np.abs(x).max() < 1 / 254.5))
+    assert flushed["E1M6"] > 0.1
+    assert abs(flushed["E1M6"] - expect) < 0.01
+
+
+def test_sr_rule_exact_thresholds():
+    # y = 0.25 lies half-way between 0 and 0.5: up iff r < 32768
+    ay = np.array([0.25, 0.25, 0.5, 0.5, 2.5, 2.5, 6.5], dtype=np.float32)
+    r = np.array([32767, 32768, 0, 65535, 32767, 32768, 0], dtype=np.uint32)
+    assert list(Q._round_sr(ay, r)) == [1, 0, 1, 1, 5, 4, 7]
+    # on-grid values never move
+    grid = np.repeat(F.E2M1_MAGNITUDES.astype(np.float32), 5)
+    rr = np.tile(np.array([0, 1, 30000, 65534, 65535], dtype=np.uint32), 8)
+    assert np.array_equal(Q._round_sr(grid, rr), np.repeat(np.arange(8), 5))
+
+
+@pytest.mark.parametrize("y", [0.30078125, 0.8125, 1.1015625, 2.75, 4.5, 5.96875])
+def test_sr_unbiased_4sigma(y):
+    # MXFP4 block with max 4.0 has s_b = 1 and r_b = 1, so the element reaching the
+    # rounder is x itself; 10^6 draws of SR(y) must average to y within 4 sigma
+    # (gonzo_ML #3986, "Стохастическая квантизация": stochastic rounding reduces bias).
+    n_blocks = 32258  # 31 draws per block -> ~10^6
+    x = np.full((n_blocks, 32), y, dtype=np.float32)
+    x[:, 0] = 4.0 if y <= 4 else 6.0
+    q = Q.quantize(x, "E8M0", rounding="sr", seed=1234)
+    s = Q.scale_values(q["scales"], "E8M0")
+    assert np.all(s == 1.0)
+    vals = F.e2m1_decode(Q.unpack(q["codes"]))[:, 1:].reshape(-1)
+    lo = F.E2M1_MAGNITUDES[F.e2m1_floor_magnitude(np.array([y]))[0]]
+    hi = F.E2M1_MAGNITUDES[F.e2m1_floor_magnitude(np.array([y]))[0] + 1]
+    assert set(np.unique(vals)) <= {lo, hi}
+    f = (y - lo) / (hi - lo)
+    sigma = np.sqrt(f * (1 - f)) * (hi - lo) / np.sqrt(vals.size)
+    assert abs(vals.mean() - y) < 4 * sigma
+    assert abs(np.mean(vals == hi) - f) < 4 * np.sqrt(f * (1 - f) / vals.size)
+
+
+def test_sr_depends_only_on_seed_and_index():
+    x = _data(4, (64, 128))
+    a = Q.quantize(x, "E4M3", rounding="sr", seed=77)
+    b = Q.quantize(x, "E4M3", rounding="sr", seed=77, chunk_rows=7)
+    c = Q.quantize(x, "E4M3", rounding="sr", seed=78)
+    assert np.array_equal(a["codes"], b["codes"])
+    assert not np.array_equal(a["codes"], c["codes"])
+    r1 = Q.quantize(x, "E4M3", rounding="rne", seed=1)
+    r2 = Q.quantize(x, "E4M3", rounding="rne", seed=2)
+    assert np.array_equal(r1["codes"], r2["codes"])
+
+
+def test_amax_refresh_every_50_steps():
+    st = AmaxState(period=50)
+    rng = np.random.default_rng(0)
+    seen = []
+    for t in range(101):
+        x = (rng.standard_normal((8, 32)) * 1.02 ** t).astype(np.float32)
+        g = st.amax_for_step(t, x)
+        seen.append(g)
+        if t in (0, 50, 100):
+            assert g == np.max(np.abs(x))
+        else:
+            assert g == seen[t - 1]
+
+
+def test_ue5m3_reencode_exact_for_fresh_amax():
+    x = _data(5, (128, 256))
+    q = Q.quantize(x, "UE5M3")
+    t = Q.ue5m3_shift(q["scales"])
+    assert t == 1  # fresh amax puts the largest scale at 448 (exponent 8)
+    codes, exact = Q.ue5m3_reencode_e4m3(q["scales"], t)
+    assert exact
+    assert np.array_equal(F.CODECS["E4M3"].decode(codes) * 2.0 ** t,
+                          Q.scale_values(q["scales"], "UE5M3"))
