@@ -1,0 +1,282 @@
+// C ABI of libfp4.so (declared in include/fp4.h): host-side argument checks,
+// then launches on the caller's stream.  No allocation, no synchronization.
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/fp4.h"
+#include "launch.h"
+
+namespace {
+
+thread_local int g_last_cuda_error = 0;
+
+fp4_status cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return FP4_OK;
+  g_last_cuda_error = (int)e;
+  return FP4_ERR_CUDA;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool valid_fmt(int f) { return f == FP4_SF_E4M3 || f == FP4_SF_UE5M3 || f == FP4_SF_E8M0 || f == FP4_SF_E1M6; }
+
+int group_of(int f) {
+  switch (f) {
+    case FP4_SF_E4M3:
+    case FP4_SF_UE5M3:
+    case FP4_SF_E1M6: return 16;
+    case FP4_SF_E8M0: return 32;
+    default: return 0;
+  }
+}
+
+// Checks shared by the quantizer entry points.  rows/cols are the OUTPUT
+// layout's (blocks run along cols).
+fp4_status check_quant_common(const void* x, int64_t M, int64_t K, int64_t ldx, int f, int sfl, int64_t out_rows,
+                              int64_t out_cols) {
+  if (!valid_fmt(f) || (sfl != FP4_SFLAYOUT_PLAIN && sfl != FP4_SFLAYOUT_MMA)) return FP4_ERR_INVALID_ARG;
+  if (M < 0 || K < 0 || ldx < K) return FP4_ERR_SHAPE;
+  const int G = group_of(f);
+  if (out_cols % G != 0) return FP4_ERR_SHAPE;
+  if (x == nullptr && M * K > 0) return FP4_ERR_INVALID_ARG;
+  if (!aligned16(x) || (ldx * 2) % 16 != 0) return FP4_ERR_ALIGNMENT;
+  if (sfl == FP4_SFLAYOUT_MMA && (out_rows % 128 != 0 || (out_cols / G) % 4 != 0)) return FP4_ERR_SHAPE;
+  return FP4_OK;
+}
+
+fp4_status check_out(const void* codes, const void* scales) {
+  if (codes == nullptr || scales == nullptr) return FP4_ERR_INVALID_ARG;
+  if (!aligned16(codes) || !aligned16(scales)) return FP4_ERR_ALIGNMENT;
+  return FP4_OK;
+}
+
+// Fresh or stored global amax; sets a.gptr / a.amax_by_product / a.amax_out.
+fp4_status prepare_amax(fp4lib::QuantArgs& a, const float* global_amax, float* amax_out, cudaStream_t st) {
+  a.amax_out = amax_out;
+  if (global_amax == nullptr) {
+    if (amax_out == nullptr) return FP4_ERR_INVALID_ARG;
+    fp4_status s = cuda_status(fp4lib::launch_amax(a.x, a.M, a.K, a.ldx, amax_out, st));
+    if (s != FP4_OK) return s;
+    a.gptr = amax_out;
+    a.amax_by_product = false;
+  } else {
+    a.gptr = global_amax;
+    a.amax_by_product = amax_out != nullptr;
+    if (a.amax_by_product) {
+      fp4_status s = cuda_status(cudaMemsetAsync(amax_out, 0, sizeof(float), st));
+      if (s != FP4_OK) return s;
+    }
+  }
+  return FP4_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int fp4_group_size(fp4_scale_fmt f) { return group_of((int)f); }
+
+fp4_status fp4_storage_bytes(int64_t rows, int64_t cols, fp4_scale_fmt f, size_t* code_bytes,
+                             size_t* scale_bytes) {
+  if (!valid_fmt((int)f) || code_bytes == nullptr || scale_bytes == nullptr) return FP4_ERR_INVALID_ARG;
+  const int G = group_of((int)f);
+  if (rows < 0 || cols < 0 || cols % G != 0) return FP4_ERR_SHAPE;
+  *code_bytes = (size_t)(rows * (cols / 2));
+  *scale_bytes = (size_t)(rows * (cols / G));
+  return FP4_OK;
+}
+
+fp4_status fp4_amax(const void* x_bf16, int64_t M, int64_t K, int64_t ldx, float* amax_out,
+                    fp4_stream_t stream) {
+  if (amax_out == nullptr) return FP4_ERR_INVALID_ARG;
+  if (M < 0 || K < 0 || ldx < K || K % 8 != 0) return FP4_ERR_SHAPE;
+  if (x_bf16 == nullptr && M * K > 0) return FP4_ERR_INVALID_ARG;
+  if (!aligned16(x_bf16) || (ldx * 2) % 16 != 0) return FP4_ERR_ALIGNMENT;
+  return cuda_status(fp4lib::launch_amax(x_bf16, M, K, ldx, amax_out, (cudaStream_t)stream));
+}
+
+fp4_status fp4_quantize(const void* x_bf16, int64_t M, int64_t K, int64_t ldx, fp4_scale_fmt f, fp4_rounding r,
+                        uint64_t seed, const float* global_amax, int transpose, fp4_sf_layout sfl, uint8_t* codes,
+                        uint8_t* scales, float* amax_out, int32_t* dev_status, fp4_stream_t stream) {
+  if (r != FP4_ROUND_RNE && r != FP4_ROUND_STOCHASTIC) return FP4_ERR_INVALID_ARG;
+  if (transpose != 0 && transpose != 1) return FP4_ERR_INVALID_ARG;
+  const int64_t out_rows = transpose ? K : M, out_cols = transpose ? M : K;
+  fp4_status s = check_quant_common(x_bf16, M, K, ldx, (int)f, (int)sfl, out_rows, out_cols);
+  if (s != FP4_OK) return s;
+  if (transpose && (M % 32 != 0 || K % 32 != 0)) return FP4_ERR_SHAPE;
+  if (M * K > 0 && (s = check_out(codes, scales)) != FP4_OK) return s;
+  cudaStream_t st = (cudaStream_t)stream;
+  fp4lib::QuantArgs a{};
+  a.mode = transpose ? fp4lib::QuantArgs::COLS : fp4lib::QuantArgs::ROWS;
+  a.fmt = (int)f;
+  a.x = x_bf16;
+  a.M = M;
+  a.K = K;
+  a.ldx = ldx;
+  a.mma = sfl == FP4_SFLAYOUT_MMA;
+  a.status = dev_status;
+  const bool sr = r == FP4_ROUND_STOCHASTIC;
+  if (transpose) {
+    a.col_sr = sr;
+    a.seed_col = seed;
+    a.codes_col = codes;
+    a.scales_col = scales;
+  } else {
+    a.row_sr = sr;
+    a.seed_row = seed;
+    a.codes_row = codes;
+    a.scales_row = scales;
+  }
+  if ((s = prepare_amax(a, global_amax, amax_out, st)) != FP4_OK) return s;
+  return cuda_status(fp4lib::launch_quantize(a, st));
+}
+
+fp4_status fp4_quantize_dual(const void* x_bf16, int64_t M, int64_t K, int64_t ldx, fp4_scale_fmt f,
+                             fp4_rounding r_row, uint64_t seed_row, fp4_rounding r_col, uint64_t seed_col,
+                             const float* global_amax, fp4_sf_layout sfl, uint8_t* codes_row, uint8_t* scales_row,
+                             uint8_t* codes_col, uint8_t* scales_col, float* amax_out, int32_t* dev_status,
+                             fp4_stream_t stream) {
+  if ((r_row != FP4_ROUND_RNE && r_row != FP4_ROUND_STOCHASTIC) ||
+      (r_col != FP4_ROUND_RNE && r_col != FP4_ROUND_STOCHASTIC))
+    return FP4_ERR_INVALID_ARG;
+  fp4_status s = check_quant_common(x_bf16, M, K, ldx, (int)f, (int)sfl, M, K);
+  if (s != FP4_OK) return s;
+  if ((s = check_quant_common(x_bf16, M, K, ldx, (int)f, (int)sfl, K, M)) != FP4_OK) return s;
+  if (M % 32 != 0 || K % 32 != 0) return FP4_ERR_SHAPE;
+  if (M * K > 0) {
+    if ((s = check_out(codes_row, scales_row)) != FP4_OK) return s;
+    if ((s = check_out(codes_col, scales_col)) != FP4_OK) return s;
+  }
+  cudaStream_t st = (cudaStream_t)stream;
+  fp4lib::QuantArgs a{};
+  a.mode = fp4lib::QuantArgs::DUAL;
+  a.fmt = (int)f;
+  a.x = x_bf16;
+  a.M = M;
+  a.K = K;
+  a.ldx = ldx;
+  a.mma = sfl == FP4_SFLAYOUT_MMA;
+  a.status = dev_status;
+  a.row_sr = r_row == FP4_ROUND_STOCHASTIC;
+  a.col_sr = r_col == FP4_ROUND_STOCHASTIC;
+  a.seed_row = seed_row;
+  a.seed_col = seed_col;
+  a.codes_row = codes_row;
+  a.scales_row = scales_row;
+  a.codes_col = codes_col;
+  a.scales_col = scales_col;
+  if ((s = prepare_amax(a, global_amax, amax_out, st)) != FP4_OK) return s;
+  return cuda_status(fp4lib::launch_quantize(a, st));
+}
+
+fp4_status fp4_dequantize(const uint8_t* codes, const uint8_t* scales, fp4_sf_layout sfl, int64_t M, int64_t K,
+                          fp4_scale_fmt f, const float* global_amax, fp4_out_dtype od, void* out,
+                          fp4_stream_t stream) {
+  if (!valid_fmt((int)f) || (sfl != FP4_SFLAYOUT_PLAIN && sfl != FP4_SFLAYOUT_MMA) ||
+      (od != FP4_OUT_F32 && od != FP4_OUT_BF16))
+    return FP4_ERR_INVALID_ARG;
+  const int G = group_of((int)f);
+  if (M < 0 || K < 0 || K % G != 0) return FP4_ERR_SHAPE;
+  if (sfl == FP4_SFLAYOUT_MMA && (M % 128 != 0 || (K / G) % 4 != 0)) return FP4_ERR_SHAPE;
+  if (M * K == 0) return FP4_OK;
+  if (codes == nullptr || scales == nullptr || out == nullptr || global_amax == nullptr) return FP4_ERR_INVALID_ARG;
+  if (!aligned16(codes) || !aligned16(out)) return FP4_ERR_ALIGNMENT;
+  return cuda_status(fp4lib::launch_dequantize(codes, scales, sfl == FP4_SFLAYOUT_MMA, M, K, (int)f, global_amax,
+                                               od == FP4_OUT_BF16, out, (cudaStream_t)stream));
+}
+
+fp4_status fp4_ue5m3_to_e4m3(const uint8_t* ue5m3_scales, int64_t n, int32_t* t_out, uint8_t* e4m3_out,
+                             int32_t* dev_status, fp4_stream_t stream) {
+  if (t_out == nullptr || n < 0) return n < 0 ? FP4_ERR_SHAPE : FP4_ERR_INVALID_ARG;
+  if (n > 0 && (ue5m3_scales == nullptr || e4m3_out == nullptr)) return FP4_ERR_INVALID_ARG;
+  return cuda_status(fp4lib::launch_ue5m3_to_e4m3(ue5m3_scales, n, t_out, e4m3_out, dev_status,
+                                                  (cudaStream_t)stream));
+}
+
+fp4_status fp4_gemm(const uint8_t* Aq, const uint8_t* As, const uint8_t* Bq, const uint8_t* Bs, const float* ga,
+                    const float* gb, const int32_t* tA, const int32_t* tB, int64_t M, int64_t N, int64_t K,
+                    fp4_scale_fmt f, fp4_gemm_layout layout, fp4_out_dtype od, void* C, int64_t ldc,
+                    int32_t* dev_status, fp4_stream_t stream) {
+  if (layout != FP4_LAYOUT_TN || (od != FP4_OUT_F32 && od != FP4_OUT_BF16) || !valid_fmt((int)f))
+    return FP4_ERR_INVALID_ARG;
+  if (f == FP4_SF_E1M6) return FP4_ERR_UNSUPPORTED;
+  if (Aq == nullptr || As == nullptr || Bq == nullptr || Bs == nullptr || C == nullptr) return FP4_ERR_INVALID_ARG;
+  if (f != FP4_SF_E8M0 && (ga == nullptr || gb == nullptr)) return FP4_ERR_INVALID_ARG;
+  if (f == FP4_SF_UE5M3 && (tA == nullptr || tB == nullptr)) return FP4_ERR_INVALID_ARG;
+  if (M <= 0 || N <= 0 || K <= 0 || M % 128 != 0 || N % 256 != 0 || K % 256 != 0 || ldc < N) return FP4_ERR_SHAPE;
+  const int64_t esz = od == FP4_OUT_BF16 ? 2 : 4;
+  if (!aligned16(Aq) || !aligned16(As) || !aligned16(Bq) || !aligned16(Bs) || !aligned16(C) ||
+      (ldc * esz) % 16 != 0)
+    return FP4_ERR_ALIGNMENT;
+  fp4lib::GemmArgs a{};
+  a.Aq = Aq;
+  a.As = As;
+  a.Bq = Bq;
+  a.Bs = Bs;
+  a.ga = ga;
+  a.gb = gb;
+  a.tA = f == FP4_SF_UE5M3 ? tA : nullptr;
+  a.tB = f == FP4_SF_UE5M3 ? tB : nullptr;
+  a.M = M;
+  a.N = N;
+  a.K = K;
+  a.ldc = ldc;
+  a.fmt = (int)f;
+  a.bf16_out = od == FP4_OUT_BF16;
+  a.C = C;
+  a.status = dev_status;
+  return cuda_status(fp4lib::launch_gemm(a, (cudaStream_t)stream));
+}
+
+fp4_status fp4_gemv_w4a16(const uint8_t* Wq, const uint8_t* Ws, const float* gw, const void* x_bf16,
+                          int64_t batch, int64_t N, int64_t K, fp4_out_dtype od, void* y, fp4_stream_t stream) {
+  if (od != FP4_OUT_F32 && od != FP4_OUT_BF16) return FP4_ERR_INVALID_ARG;
+  if (Wq == nullptr || Ws == nullptr || gw == nullptr || x_bf16 == nullptr || y == nullptr)
+    return FP4_ERR_INVALID_ARG;
+  if (batch < 1 || batch > 64 || N <= 0 || K <= 0 || K % 32 != 0) return FP4_ERR_SHAPE;
+  if (!aligned16(Wq) || !aligned16(Ws) || !aligned16(x_bf16) || !aligned16(y)) return FP4_ERR_ALIGNMENT;
+  fp4lib::GemvArgs a{};
+  a.Wq = Wq;
+  a.Ws = Ws;
+  a.gw = gw;
+  a.x = x_bf16;
+  a.batch = batch;
+  a.N = N;
+  a.K = K;
+  a.bf16_out = od == FP4_OUT_BF16;
+  a.y = y;
+  return cuda_status(fp4lib::launch_gemv(a, (cudaStream_t)stream));
+}
+
+fp4_status fp4_encode_scales(const float* s, int64_t n, fp4_scale_fmt f, uint8_t* codes, float* decoded,
+                             fp4_stream_t stream) {
+  if (!valid_fmt((int)f)) return FP4_ERR_INVALID_ARG;
+  if (n < 0) return FP4_ERR_SHAPE;
+  if (n > 0 && (s == nullptr || codes == nullptr || decoded == nullptr)) return FP4_ERR_INVALID_ARG;
+  return cuda_status(fp4lib::launch_encode_scales(s, n, (int)f, codes, decoded, (cudaStream_t)stream));
+}
+
+fp4_status fp4_philox_bits16(uint64_t seed, uint64_t start, int64_t n, uint16_t* out, fp4_stream_t stream) {
+  if (n < 0) return FP4_ERR_SHAPE;
+  if (n > 0 && out == nullptr) return FP4_ERR_INVALID_ARG;
+  return cuda_status(fp4lib::launch_philox_bits16(seed, start, n, out, (cudaStream_t)stream));
+}
+
+const char* fp4_status_string(fp4_status s) {
+  switch (s) {
+    case FP4_OK: return "ok";
+    case FP4_ERR_INVALID_ARG: return "invalid argument (NULL pointer or bad enum)";
+    case FP4_ERR_SHAPE: return "unsupported shape";
+    case FP4_ERR_ALIGNMENT: return "pointer or leading dimension not 16-byte aligned";
+    case FP4_ERR_UNSUPPORTED: return "combination not supported";
+    case FP4_ERR_NONFINITE: return "stored global amax is not finite";
+    case FP4_ERR_UE5M3_RANGE: return "UE5M3 scale not exact on the shifted E4M3 path";
+    case FP4_ERR_TIMEOUT: return "bounded device wait expired";
+    case FP4_ERR_CUDA: return "CUDA runtime error (see fp4_last_cuda_error)";
+    default: return "unknown status";
+  }
+}
+
+int fp4_last_cuda_error(void) { return g_last_cuda_error; }
+
+}  // extern "C"

@@ -1,0 +1,287 @@
+// Device building blocks of the FP4 block-scaled quantizer (sm_103a).
+//
+// Method sources (web pages, cited by title and section):
+//   "NVFP4 vs MXFP" post (quant_prune_distill #486), "Метод": E2M1 elements,
+//     group 16 with an E4M3 scale (NVFP4), group 32 with an E8M0 power-of-two
+//     scale (MXFP4).
+//   "UE5M3 FP4 Block Scaling for Stable Language Model Pretraining" (rit.work
+//     blog), "Что сделали": unsigned 5-exponent/3-fraction block scale.
+//   Review of Intel's FP4 training paper (gonzo_ML #3986), "Форматы FP4"
+//     (E1M6 .. E8M0 scale sweep) and "Стохастическая квантизация" (nearest
+//     rounding forward, stochastic rounding backward).
+//
+// Every float32 step of the method is a single correctly rounded operation
+// (__fmul_rn / __fdiv_rn / __fadd_rn), so no fused multiply-add or reciprocal
+// approximation changes a result; the integer steps work on IEEE bit fields.
+#pragma once
+
+#include <cstdint>
+#include <cuda_bf16.h>
+
+#include "../../include/fp4.h"
+
+namespace fp4dev {
+
+// ---------------------------------------------------------------------------
+// Status word (first error wins)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void set_status(int32_t* st, int32_t code) {
+  if (st != nullptr) atomicCAS(st, 0, code);
+}
+
+// ---------------------------------------------------------------------------
+// bf16 helpers: a 32-bit word holds element 2j in its low half, 2j+1 high.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// max |x| over the two bf16 halves of each word, kept as packed non-negative
+// bf16 (sign bit cleared, so the packed max is the magnitude max).
+__device__ __forceinline__ uint32_t absmax2(uint32_t a, uint32_t b) {
+  __nv_bfloat162 x = *reinterpret_cast<__nv_bfloat162*>(&a);
+  __nv_bfloat162 y = *reinterpret_cast<__nv_bfloat162*>(&b);
+  __nv_bfloat162 m = __hmax2(x, y);
+  return *reinterpret_cast<uint32_t*>(&m);
+}
+__device__ __forceinline__ float absmax_words(const uint32_t* w, int n) {
+  uint32_t m = w[0] & 0x7FFF7FFFu;
+#pragma unroll
+  for (int i = 1; i < n; ++i) m = absmax2(m, w[i] & 0x7FFF7FFFu);
+  return fmaxf(bf16_lo(m), bf16_hi(m));
+}
+
+// ---------------------------------------------------------------------------
+// Scale formats.  Generic small float with EB exponent bits, MB mantissa bits,
+// bias BIAS, IEEE-style subnormals; MAXCODE is the largest finite
+// non-negative code.  Encoding: nearest value, ties to the even code,
+// saturating at MAXCODE.
+// ---------------------------------------------------------------------------
+template <int MB, int BIAS>
+__device__ __forceinline__ float exmy_decode(uint32_t code) {
+  const uint32_t e = code >> MB, m = code & ((1u << MB) - 1u);
+  if (e == 0) {
+    // m * 2^(1-BIAS-MB): an exact product of a small integer and a power of two
+    return __fmul_rn((float)m, __uint_as_float((uint32_t)(127 + 1 - BIAS - MB) << 23));
+  }
+  return __uint_as_float(((e + 127u - (uint32_t)BIAS) << 23) | (m << (23 - MB)));
+}
+
+template <int MB, int BIAS, uint32_t MAXCODE>
+__device__ __forceinline__ uint32_t exmy_encode_rne_sat(float s) {
+  const float maxv = exmy_decode<MB, BIAS>(MAXCODE);
+  if (!(s < maxv)) return MAXCODE;  // also +Inf
+  const uint32_t b = __float_as_uint(s);
+  const int e = (int)(b >> 23) - 127;
+  if (e >= 1 - BIAS) {
+    // normal in the target: round the 23-bit fraction to MB bits, ties to even;
+    // a carry out of the fraction moves into the exponent field by itself
+    constexpr int SH = 23 - MB;
+    const uint32_t lsb = (b >> SH) & 1u;
+    const uint32_t r = (b + ((1u << (SH - 1)) - 1u) + lsb) >> SH;
+    return r - ((uint32_t)(127 - BIAS) << MB);
+  }
+  // subnormal in the target: count of 2^(1-BIAS-MB) steps, nearest even integer
+  const float t = __fmul_rn(s, __uint_as_float((uint32_t)(127 + BIAS + MB - 1) << 23));
+  return (uint32_t)__float2int_rn(t);
+}
+
+// Format tags, matching fp4_scale_fmt.
+enum : int { SF_E4M3 = FP4_SF_E4M3, SF_UE5M3 = FP4_SF_UE5M3, SF_E8M0 = FP4_SF_E8M0, SF_E1M6 = FP4_SF_E1M6 };
+
+template <int FMT> struct ScaleFmt;
+template <> struct ScaleFmt<SF_E4M3> {
+  static constexpr int G = 16;
+  static constexpr float SIX_ST = 2688.0f;  // 6 * 448
+  __device__ static uint32_t encode(float s) { return exmy_encode_rne_sat<3, 7, 0x7Eu>(s); }
+  __device__ static float decode(uint32_t c) { return exmy_decode<3, 7>(c); }
+};
+template <> struct ScaleFmt<SF_UE5M3> {
+  static constexpr int G = 16;
+  static constexpr float SIX_ST = 2688.0f;  // 6 * 448
+  __device__ static uint32_t encode(float s) { return exmy_encode_rne_sat<3, 15, 0xFEu>(s); }
+  __device__ static float decode(uint32_t c) { return exmy_decode<3, 15>(c); }
+};
+template <> struct ScaleFmt<SF_E1M6> {
+  static constexpr int G = 16;
+  static constexpr float SIX_ST = 23.8125f;  // 6 * 3.96875
+  __device__ static uint32_t encode(float s) { return exmy_encode_rne_sat<6, 0, 0x7Fu>(s); }
+  __device__ static float decode(uint32_t c) { return exmy_decode<6, 0>(c); }
+};
+template <> struct ScaleFmt<SF_E8M0> {
+  static constexpr int G = 32;
+  static constexpr float SIX_ST = 0.0f;  // unused: no global scale
+  // code = clamp(floor(log2 a) - 2 + 127, 0, 254), the exponent read from the bits
+  __device__ static uint32_t encode_from_amax(float a) {
+    const int e = (int)(__float_as_uint(a) >> 23);
+    int c = e > 0 ? e - 2 : 0;
+    c = c < 0 ? 0 : (c > 254 ? 254 : c);
+    return (uint32_t)c;
+  }
+  __device__ static float decode(uint32_t c) {
+    return c > 0 ? __uint_as_float(c << 23) : __uint_as_float(0x00400000u);  // 2^-127
+  }
+};
+
+// Per-tensor encode scale from the stored amax g.
+template <int FMT>
+__device__ __forceinline__ float global_encode_scale(float g, int32_t* status) {
+  if (FMT == SF_E8M0) return 1.0f;
+  if (!(fabsf(g) <= 3.402823466e38f)) {  // Inf or NaN
+    set_status(status, FP4_ERR_NONFINITE);
+    return 1.0f;
+  }
+  if (g == 0.0f) return 1.0f;
+  const float s = __fdiv_rn(ScaleFmt<FMT>::SIX_ST, g);
+  return (s > 3.402823466e38f) ? 3.402823466e38f : s;
+}
+
+struct BlockScale {
+  uint32_t code;
+  float r;  // element multiplier s_enc / s_b (0 when s_b == 0)
+};
+
+template <int FMT>
+__device__ __forceinline__ BlockScale block_scale(float a_b, float s_enc) {
+  BlockScale out;
+  float s_b;
+  if constexpr (FMT == SF_E8M0) {
+    out.code = ScaleFmt<SF_E8M0>::encode_from_amax(a_b);
+    s_b = ScaleFmt<SF_E8M0>::decode(out.code);
+  } else {
+    const float s_real = __fmul_rn(__fdiv_rn(a_b, 6.0f), s_enc);
+    out.code = ScaleFmt<FMT>::encode(s_real);
+    s_b = ScaleFmt<FMT>::decode(out.code);
+  }
+  out.r = (s_b == 0.0f) ? 0.0f : __fdiv_rn(s_enc, s_b);
+  return out;
+}
+
+// ---------------------------------------------------------------------------
+// E2M1 element rounding
+// ---------------------------------------------------------------------------
+// Round-to-nearest-even with saturation, two values into one byte: `lo` in the
+// low nibble, `hi` in the high nibble (cvt.rn.satfinite.e2m1x2.f32 puts its
+// first source in the upper nibble).
+__device__ __forceinline__ uint32_t e2m1x2_rne(float lo, float hi) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 t;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\t"
+      "cvt.u32.u8 %0, t;\n\t}"
+      : "=r"(r)
+      : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Software RNE of one value (|y| thresholds at the grid midpoints; a tie goes
+// to the even code): magnitude code with the sign of y in bit 3.
+__device__ __forceinline__ uint32_t e2m1_rne_soft(float y) {
+  const float a = fabsf(y);
+  uint32_t m = (uint32_t)(a > 0.25f) + (uint32_t)(a >= 0.75f) + (uint32_t)(a > 1.25f) +
+               (uint32_t)(a >= 1.75f) + (uint32_t)(a > 2.5f) + (uint32_t)(a >= 3.5f) +
+               (uint32_t)(a > 5.0f);
+  return m | ((__float_as_uint(y) >> 28) & 8u);
+}
+
+// Stochastic rounding of one value with a 16-bit draw r: lo <= |y| < hi the
+// neighbouring grid values, round up iff r < 65536 * (|y| - lo) / (hi - lo);
+// |y| >= 6 gives 6.  Both sides of the comparison are exact in float32.
+__device__ __forceinline__ uint32_t e2m1_sr(float y, uint32_t r16) {
+  const float a = fabsf(y);
+  uint32_t lc;
+  float lo, sc;
+  if (a < 2.0f) {
+    lc = (uint32_t)__float2uint_rz(__fmul_rn(a, 2.0f));  // 0..3
+    lo = __fmul_rn((float)lc, 0.5f);
+    sc = 131072.0f;  // 65536 / 0.5
+  } else if (a < 4.0f) {
+    const float f = floorf(a);
+    lc = (uint32_t)f + 2u;  // 4, 5
+    lo = f;
+    sc = 65536.0f;
+  } else {
+    lc = 6u;
+    lo = 4.0f;
+    sc = 32768.0f;  // 65536 / 2
+  }
+  const float t = __fmul_rn(__fsub_rn(a, lo), sc);
+  uint32_t m = lc + (uint32_t)((float)r16 < t);
+  m = (a >= 6.0f) ? 7u : m;
+  return m | ((__float_as_uint(y) >> 28) & 8u);
+}
+
+// ---------------------------------------------------------------------------
+// Philox4x32-10 (Salmon, Moraes, Dror, Shaw, SC'11): 10 rounds of
+// (c0,c1,c2,c3) -> (hi(M1*c2)^c1^k0, lo(M1*c2), hi(M0*c0)^c3^k1, lo(M0*c0)),
+// the key advanced by the Weyl constants between rounds.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint4 philox4x32_10(uint32_t c0, uint32_t c1, uint32_t c2, uint32_t c3,
+                                               uint32_t k0, uint32_t k1) {
+#pragma unroll
+  for (int i = 0; i < 10; ++i) {
+    if (i > 0) {
+      k0 += 0x9E3779B9u;
+      k1 += 0xBB67AE85u;
+    }
+    const uint32_t hi0 = __umulhi(0xD2511F53u, c0), lo0 = 0xD2511F53u * c0;
+    const uint32_t hi1 = __umulhi(0xCD9E8D57u, c2), lo1 = 0xCD9E8D57u * c2;
+    c0 = hi1 ^ c1 ^ k0;
+    c1 = lo1;
+    c2 = hi0 ^ c3 ^ k1;
+    c3 = lo0;
+  }
+  return make_uint4(c0, c1, c2, c3);
+}
+
+// The 8 draws of output indices 8*blk .. 8*blk+7: element j takes word j/2,
+// low half for even j, high half for odd j.
+__device__ __forceinline__ uint4 sr_draws8(uint64_t seed, uint64_t blk) {
+  return philox4x32_10((uint32_t)blk, (uint32_t)(blk >> 32), 0u, 0u, (uint32_t)seed,
+                       (uint32_t)(seed >> 32));
+}
+__device__ __forceinline__ uint32_t draw16(const uint4& w, int j) {
+  const uint32_t v = (j >> 1) == 0 ? w.x : (j >> 1) == 1 ? w.y : (j >> 1) == 2 ? w.z : w.w;
+  return (j & 1) ? (v >> 16) : (v & 0xFFFFu);
+}
+
+// ---------------------------------------------------------------------------
+// Quantize 16 bf16 values (8 words, element order = word order, low half
+// first) with block multiplier r into 8 bytes of packed codes.
+// Philox indices of the 16 elements start at idx0 (a multiple of 8).
+// ---------------------------------------------------------------------------
+template <bool SR>
+__device__ __forceinline__ uint2 quant16(const uint32_t* w, float r, uint64_t seed, uint64_t idx0) {
+  uint32_t bytes[8];
+  if constexpr (!SR) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float y0 = __fmul_rn(bf16_lo(w[i]), r);
+      const float y1 = __fmul_rn(bf16_hi(w[i]), r);
+      bytes[i] = e2m1x2_rne(y0, y1);
+    }
+  } else {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const uint4 d = sr_draws8(seed, (idx0 >> 3) + h);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint32_t wi = w[4 * h + i];
+        const float y0 = __fmul_rn(bf16_lo(wi), r);
+        const float y1 = __fmul_rn(bf16_hi(wi), r);
+        bytes[4 * h + i] = e2m1_sr(y0, draw16(d, 2 * i)) | (e2m1_sr(y1, draw16(d, 2 * i + 1)) << 4);
+      }
+    }
+  }
+  uint2 out;
+  out.x = bytes[0] | (bytes[1] << 8) | (bytes[2] << 16) | (bytes[3] << 24);
+  out.y = bytes[4] | (bytes[5] << 8) | (bytes[6] << 16) | (bytes[7] << 24);
+  return out;
+}
+
+// Byte offset of scale (row r, block b) in the tiled MMA scale layout with nb
+// blocks per row: 128-row x 4-block atoms of 512 bytes, row-major over atoms;
+// inside an atom row r sits at (r%32)*16 + ((r/32)%4)*4, block b at b%4.
+__device__ __forceinline__ int64_t mma_sf_offset(int64_t r, int64_t b, int64_t nb) {
+  return ((r >> 7) * (nb >> 2) + (b >> 2)) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4 + (b & 3);
+}
+
+}  // namespace fp4dev

@@ -1,0 +1,509 @@
+// Block-scaled FP4 GEMM on the sm_103a tcgen05 tensor cores.
+//
+// Computes, for packed E2M1 operands A [M, K], B [N, K] (blocks along K) and
+// their block scales ("NVFP4 vs MXFP" post, quant_prune_distill #486, section
+// "Метод"; every eligible linear in FP4 for forward and backward: "UE5M3 FP4
+// Block Scaling ..." blog, section "Что сделали"):
+//
+//   C[m, n] = alpha * sum_k (qa * sa)(qb * sb),   float32 accumulation,
+//   alpha   = f32(1 / f32(s_encA * s_encB)) * 2^(tA + tB).
+//
+// NVFP4 (E4M3 scales, 16-element blocks) runs as kind::mxf4nvf4 with
+// scale_vec::4X and ue4m3 scales; MXFP4 (E8M0, 32-element blocks) as
+// scale_vec::2X with ue8m0 scales.  UE5M3 has no tensor-core scale type; its
+// scales arrive re-encoded as E4M3 of s * 2^-t (exact) and 2^(tA + tB) folds
+// into alpha (the software emulation of the "UE5M3 ..." blog, "Ограничения").
+//
+// Kernel structure (one CTA per SM, persistent over 128 x 256 output tiles):
+//   warp 0      TMA producer: A/B code tiles (128-byte swizzle) by
+//               cp.async.bulk.tensor, scale atoms by cp.async.bulk, into a
+//               4-stage shared-memory ring guarded by mbarriers;
+//   warp 1      allocates tensor memory; one lane moves each stage's scales
+//               into tensor memory (tcgen05.cp 32x128b.warpx4) and issues the
+//               4 tcgen05.mma of the 256-wide K step; tcgen05.commit frees the
+//               stage and, after the last K step, hands the accumulator over;
+//   warps 2-9   epilogue: tcgen05.ld the 128 x 256 float32 accumulator into
+//               registers (each warp 32 rows x 128 columns), release the
+//               tensor memory at once so the next tile's MMAs overlap the
+//               conversion and the global stores.
+// Every mbarrier wait is bounded: on expiry the CTA records FP4_ERR_TIMEOUT in
+// the status word and winds down instead of spinning.
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include "fp4_device.cuh"
+#include "launch.h"
+
+namespace {
+
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int BK = 256;  // FP4 elements per K step = 128 bytes per row
+constexpr int STAGES = 4;
+constexpr int A_BYTES = BM * BK / 2;     // 16 KB
+constexpr int B_BYTES = BN * BK / 2;     // 32 KB
+constexpr int SFA_MAX = BM * BK / 16;    // 2 KB (NVFP4); MXFP4 uses half
+constexpr int SFB_MAX = BN * BK / 16;    // 4 KB
+constexpr int SMEM_A = 0;
+constexpr int SMEM_B = SMEM_A + STAGES * A_BYTES;
+constexpr int SMEM_SFA = SMEM_B + STAGES * B_BYTES;
+constexpr int SMEM_SFB = SMEM_SFA + STAGES * SFA_MAX;
+constexpr int SMEM_BAR = SMEM_SFB + STAGES * SFB_MAX;
+constexpr int SMEM_TOTAL = SMEM_BAR + 256;
+constexpr int SMEM_LAUNCH = SMEM_TOTAL + 1024;  // room to align the base to 1024
+
+constexpr int NUM_EPI_WARPS = 8;
+constexpr int NUM_THREADS = 32 * (2 + NUM_EPI_WARPS);
+
+// tensor memory columns: accumulator 0..255, scales for 4 stages after it
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t TMEM_SFA = 256;             // 16 columns per stage
+constexpr uint32_t TMEM_SFB = 256 + 16 * STAGES;  // 32 columns per stage
+
+constexpr long long WAIT_LIMIT_CYCLES = 4000000000LL;  // ~2 s at 2 GHz
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// ---- mbarrier -------------------------------------------------------------
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait.  Returns false (and raises the CTA's abort flag and the status
+// word) if the phase does not complete within the limit or another role has
+// already aborted.
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                             int32_t* status) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (clock64() - t0 > WAIT_LIMIT_CYCLES) {
+      *abort_flag = 1;
+      fp4dev::set_status(status, FP4_ERR_TIMEOUT);
+      return false;
+    }
+  }
+}
+
+// ---- TMA / bulk copies ----------------------------------------------------
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], "
+      "[%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
+
+// ---- tcgen05 --------------------------------------------------------------
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+               : "memory");
+}
+
+// Shared-memory matrix descriptor: start address, leading/stride byte offsets
+// (16-byte units), fixed version field 1 at bit 46, layout type at bits 61-63
+// (0 = no swizzle, 2 = 128-byte swizzle).
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo, uint32_t layout) {
+  uint64_t d = 0;
+  d |= (uint64_t)((addr >> 4) & 0x3FFFu);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)(layout & 7u) << 61;
+  return d;
+}
+
+// Instruction descriptor of kind::mxf4nvf4: A and B E2M1 (format 1) at bits
+// 7-9 and 10-12, K-major both, N>>3 at bits 17-22, scale type at bit 23
+// (0 = ue4m3, 1 = ue8m0), M>>4 at bits 24-28, scale-factor ids 0.
+__host__ __device__ constexpr uint32_t make_idesc(int m, int n, bool ue8m0) {
+  return (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((ue8m0 ? 1u : 0u) << 23) |
+         ((uint32_t)(m >> 4) << 24);
+}
+
+template <bool MX>
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                       uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  if constexpr (MX) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+            d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+  } else {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+            d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+  }
+}
+
+// 512 bytes of scales (32 rows x 16 bytes) -> 4 tensor-memory columns,
+// replicated into each 32-lane quarter.
+__device__ __forceinline__ void tc_cp_sf(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
+#define TC_LD32(taddr, r)                                                                                          \
+  asm volatile(                                                                                                    \
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18," \
+      "%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"                                               \
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),            \
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),      \
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),    \
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])     \
+      : "r"(taddr))
+
+struct Params {
+  const uint8_t* As;
+  const uint8_t* Bs;
+  const float* ga;
+  const float* gb;
+  const int32_t* tA;
+  const int32_t* tB;
+  void* C;
+  int64_t ldc;
+  int M, N, K;
+  int32_t* status;
+};
+
+template <int FMT, bool BF16>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    k_gemm_fp4(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b, Params p) {
+  constexpr bool MX = FMT == fp4dev::SF_E8M0;
+  constexpr int SFA_BYTES = MX ? SFA_MAX / 2 : SFA_MAX;  // scales of one K step for 128 rows
+  constexpr int SFB_HALF = SFA_BYTES;                    // per 128 rows of B
+  constexpr uint32_t IDESC = make_idesc(BM, BN, MX);
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SMEM_BAR);
+  // bars[0..S-1] full, bars[S..2S-1] empty, bars[2S] acc_full, bars[2S+1] acc_empty
+  const uint32_t bar_full = smem_u32(bars);
+  const uint32_t bar_empty = bar_full + 8 * STAGES;
+  const uint32_t bar_acc_full = bar_full + 16 * STAGES;
+  const uint32_t bar_acc_empty = bar_acc_full + 8;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + SMEM_BAR + 8 * (2 * STAGES + 2));
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + SMEM_BAR + 8 * (2 * STAGES + 2) + 8);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int m_tiles = p.M / BM, n_tiles = p.N / BN;
+  const int num_tiles = m_tiles * n_tiles;
+  const int k_steps = p.K / BK;
+  const int64_t sf_row_stride = (int64_t)(p.K / (MX ? 32 : 16)) / 4 * 512;  // bytes per 128-row slab
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(bar_full + 8 * s, 1);
+      mbar_init(bar_empty + 8 * s, 1);
+    }
+    mbar_init(bar_acc_full, 1);
+    mbar_init(bar_acc_empty, NUM_EPI_WARPS);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                 "r"(TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------ producer ------------------------------
+    if (lane == 0) {
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_a)) : "memory");
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_b)) : "memory");
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+        const int mt = tile % m_tiles, nt = tile / m_tiles;
+        for (int ks = 0; ks < k_steps; ++ks) {
+          if (!wait_bounded(bar_empty + 8 * stage, phase ^ 1u, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = bar_full + 8 * stage;
+          mbar_expect_tx(fb, A_BYTES + B_BYTES + SFA_BYTES + 2 * SFB_HALF);
+          tma_load_2d(sbase + SMEM_A + stage * A_BYTES, &tmap_a, fb, ks * (BK / 2), mt * BM);
+          tma_load_2d(sbase + SMEM_B + stage * B_BYTES, &tmap_b, fb, ks * (BK / 2), nt * BN);
+          // scales of this K step: SFA_BYTES contiguous bytes per 128-row slab
+          bulk_load(sbase + SMEM_SFA + stage * SFA_MAX, p.As + mt * sf_row_stride + (int64_t)ks * SFA_BYTES,
+                    SFA_BYTES, fb);
+          bulk_load(sbase + SMEM_SFB + stage * SFB_MAX, p.Bs + (2 * nt) * sf_row_stride + (int64_t)ks * SFB_HALF,
+                    SFB_HALF, fb);
+          bulk_load(sbase + SMEM_SFB + stage * SFB_MAX + SFB_HALF,
+                    p.Bs + (2 * nt + 1) * sf_row_stride + (int64_t)ks * SFB_HALF, SFB_HALF, fb);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------ MMA issuer ----------------------------
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      int iter = 0;
+      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x, ++iter) {
+        if (iter > 0) {
+          if (!wait_bounded(bar_acc_empty, acc_phase ^ 1u, abort_flag, p.status)) break;
+          tc_fence_after();
+        }
+        for (int ks = 0; ks < k_steps; ++ks) {
+          if (!wait_bounded(bar_full + 8 * stage, phase, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sfa_smem = sbase + SMEM_SFA + stage * SFA_MAX;
+          const uint32_t sfb_smem = sbase + SMEM_SFB + stage * SFB_MAX;
+          const uint32_t sfa_t = tmem_base + TMEM_SFA + 16 * stage;
+          const uint32_t sfb_t = tmem_base + TMEM_SFB + 32 * stage;
+          // each 512-byte scale atom covers 128 rows x 4 blocks: one MMA K step
+          // for NVFP4, two for MXFP4
+          constexpr int ATOMS = MX ? 2 : 4;
+#pragma unroll
+          for (int j = 0; j < ATOMS; ++j) {
+            tc_cp_sf(sfa_t + 4 * j, smem_desc(sfa_smem + 512 * j, 0, 128, 0));
+            tc_cp_sf(sfb_t + 8 * j, smem_desc(sfb_smem + 512 * j, 0, 128, 0));
+            tc_cp_sf(sfb_t + 8 * j + 4, smem_desc(sfb_smem + SFB_HALF + 512 * j, 0, 128, 0));
+          }
+          const uint32_t a_smem = sbase + SMEM_A + stage * A_BYTES;
+          const uint32_t b_smem = sbase + SMEM_B + stage * B_BYTES;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            // K step j: 64 elements = 32 bytes into each 128-byte swizzled row
+            const uint64_t ad = smem_desc(a_smem + 32 * j, 0, 1024, 2);
+            const uint64_t bd = smem_desc(b_smem + 32 * j, 0, 1024, 2);
+            uint32_t idesc = IDESC;
+            uint32_t sfa_col = sfa_t + 4 * j, sfb_col = sfb_t + 8 * j;
+            if constexpr (MX) {
+              // two K steps share an atom; the second reads bytes 2-3 of each cell
+              sfa_col = sfa_t + 4 * (j >> 1);
+              sfb_col = sfb_t + 8 * (j >> 1);
+              const uint32_t id = (j & 1) ? 2u : 0u;
+              idesc |= (id << 29) | (id << 4);
+            }
+            tc_mma<MX>(tmem_base, ad, bd, idesc, sfa_col, sfb_col, (ks > 0 || j > 0) ? 1u : 0u);
+          }
+          tc_commit(bar_empty + 8 * stage);  // stage free once these MMAs finish
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        tc_commit(bar_acc_full);
+        acc_phase ^= 1u;
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------ epilogue ------------------------------
+    const int ew = warp - 2;          // 0..7
+    const int quarter = warp & 3;     // tensor-memory lanes this warp may access
+    const int half = ew >> 2;         // columns 0..127 or 128..255
+    float alpha = 1.0f;
+    if constexpr (!MX) {
+      const float sa = fp4dev::global_encode_scale<FMT == fp4dev::SF_UE5M3 ? fp4dev::SF_E4M3 : FMT>(__ldg(p.ga), nullptr);
+      const float sb = fp4dev::global_encode_scale<FMT == fp4dev::SF_UE5M3 ? fp4dev::SF_E4M3 : FMT>(__ldg(p.gb), nullptr);
+      alpha = __fdiv_rn(1.0f, __fmul_rn(sa, sb));
+      if (FMT == fp4dev::SF_UE5M3) alpha = ldexpf(alpha, __ldg(p.tA) + __ldg(p.tB));
+    }
+    uint32_t acc_phase = 0;
+    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+      const int mt = tile % m_tiles, nt = tile / m_tiles;
+      if (!wait_bounded(bar_acc_full, acc_phase, abort_flag, p.status)) break;
+      acc_phase ^= 1u;
+      tc_fence_after();
+      uint32_t r[4][32];
+      const uint32_t t0 = tmem_base + ((uint32_t)(32 * quarter) << 16) + 128 * half;
+      TC_LD32(t0 + 0, r[0]);
+      TC_LD32(t0 + 32, r[1]);
+      TC_LD32(t0 + 64, r[2]);
+      TC_LD32(t0 + 96, r[3]);
+      asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_acc_empty);
+      const int64_t row = (int64_t)mt * BM + 32 * quarter + lane;
+      const int64_t col0 = (int64_t)nt * BN + 128 * half;
+      if constexpr (BF16) {
+        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.C) + row * p.ldc + col0;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            uint32_t w[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const float x0 = __fmul_rn(__uint_as_float(r[c][8 * v + 2 * i]), alpha);
+              const float x1 = __fmul_rn(__uint_as_float(r[c][8 * v + 2 * i + 1]), alpha);
+              const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
+              w[i] = *reinterpret_cast<const uint32_t*>(&h);
+            }
+            *reinterpret_cast<uint4*>(out + 32 * c + 8 * v) = make_uint4(w[0], w[1], w[2], w[3]);
+          }
+        }
+      } else {
+        float* out = static_cast<float*>(p.C) + row * p.ldc + col0;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+#pragma unroll
+          for (int v = 0; v < 8; ++v) {
+            float4 f;
+            f.x = __fmul_rn(__uint_as_float(r[c][4 * v + 0]), alpha);
+            f.y = __fmul_rn(__uint_as_float(r[c][4 * v + 1]), alpha);
+            f.z = __fmul_rn(__uint_as_float(r[c][4 * v + 2]), alpha);
+            f.w = __fmul_rn(__uint_as_float(r[c][4 * v + 3]), alpha);
+            *reinterpret_cast<float4*>(out + 32 * c + 4 * v) = f;
+          }
+        }
+      }
+    }
+  }
+
+  // ------------------------------ teardown --------------------------------
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS)
+                 : "memory");
+  }
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (fn == nullptr) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
+// 2-D uint8 map over packed codes [rows, K/2 bytes] with a 128-byte x box_rows
+// box and the 128-byte swizzle the MMA descriptors assume.
+bool make_code_map(CUtensorMap* map, const void* base, int64_t rows, int64_t row_bytes, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)row_bytes, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
+  cuuint32_t box[2] = {128u, box_rows};
+  cuuint32_t estr[2] = {1u, 1u};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int sm_count() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 148;
+  }
+  return n;
+}
+
+template <int FMT, bool BF16>
+cudaError_t launch_t(const fp4lib::GemmArgs& a, cudaStream_t st) {
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(k_gemm_fp4<FMT, BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         SMEM_LAUNCH);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  CUtensorMap ma, mb;
+  if (!make_code_map(&ma, a.Aq, a.M, a.K / 2, BM) || !make_code_map(&mb, a.Bq, a.N, a.K / 2, BN))
+    return cudaErrorInvalidValue;
+  Params p;
+  p.As = a.As;
+  p.Bs = a.Bs;
+  p.ga = a.ga;
+  p.gb = a.gb;
+  p.tA = a.tA;
+  p.tB = a.tB;
+  p.C = a.C;
+  p.ldc = a.ldc;
+  p.M = (int)a.M;
+  p.N = (int)a.N;
+  p.K = (int)a.K;
+  p.status = a.status;
+  const int tiles = (int)((a.M / BM) * (a.N / BN));
+  const int grid = tiles < sm_count() ? tiles : sm_count();
+  k_gemm_fp4<FMT, BF16><<<grid, NUM_THREADS, SMEM_LAUNCH, st>>>(ma, mb, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+namespace fp4lib {
+
+cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t st) {
+  if (a.N % BN != 0) return cudaErrorNotSupported;  // 128-wide N tail not built yet
+  switch (a.fmt) {
+    case FP4_SF_E4M3: return a.bf16_out ? launch_t<fp4dev::SF_E4M3, true>(a, st) : launch_t<fp4dev::SF_E4M3, false>(a, st);
+    case FP4_SF_UE5M3: return a.bf16_out ? launch_t<fp4dev::SF_UE5M3, true>(a, st) : launch_t<fp4dev::SF_UE5M3, false>(a, st);
+    case FP4_SF_E8M0: return a.bf16_out ? launch_t<fp4dev::SF_E8M0, true>(a, st) : launch_t<fp4dev::SF_E8M0, false>(a, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace fp4lib

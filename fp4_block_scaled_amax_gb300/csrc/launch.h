@@ -1,0 +1,54 @@
+// Internal launcher interface between the C ABI (abi.cu) and the kernel files.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace fp4lib {
+
+struct QuantArgs {
+  enum Mode { ROWS, COLS, DUAL } mode;
+  int fmt;
+  const void* x;
+  int64_t M, K, ldx;
+  const float* gptr;  // device: stored global amax
+  bool row_sr, col_sr, mma, amax_by_product;
+  uint64_t seed_row, seed_col;
+  uint8_t *codes_row, *scales_row, *codes_col, *scales_col;
+  float* amax_out;
+  int32_t* status;
+};
+
+cudaError_t launch_amax(const void* x, int64_t M, int64_t K, int64_t ldx, float* out, cudaStream_t st);
+cudaError_t launch_quantize(const QuantArgs& a, cudaStream_t st);
+cudaError_t launch_dequantize(const uint8_t* codes, const uint8_t* scales, bool mma, int64_t M, int64_t K,
+                              int fmt, const float* gptr, bool bf16, void* out, cudaStream_t st);
+cudaError_t launch_ue5m3_to_e4m3(const uint8_t* in, int64_t n, int32_t* t_out, uint8_t* out, int32_t* status,
+                                 cudaStream_t st);
+cudaError_t launch_encode_scales(const float* s, int64_t n, int fmt, uint8_t* codes, float* decoded,
+                                 cudaStream_t st);
+cudaError_t launch_philox_bits16(uint64_t seed, uint64_t start, int64_t n, uint16_t* out, cudaStream_t st);
+
+struct GemmArgs {
+  const uint8_t *Aq, *As, *Bq, *Bs;
+  const float *ga, *gb;
+  const int32_t *tA, *tB;
+  int64_t M, N, K, ldc;
+  int fmt;
+  bool bf16_out;
+  void* C;
+  int32_t* status;
+};
+cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t st);
+
+struct GemvArgs {
+  const uint8_t *Wq, *Ws;
+  const float* gw;
+  const void* x;
+  int64_t batch, N, K;
+  bool bf16_out;
+  void* y;
+};
+cudaError_t launch_gemv(const GemvArgs& a, cudaStream_t st);
+
+}  // namespace fp4lib

@@ -1,0 +1,474 @@
+// FP4 block-scaled quantizer kernels for sm_103a (HBM-bound).
+//
+// What they compute (web pages, cited by title and section):
+//   "NVFP4 vs MXFP" post (quant_prune_distill #486), "Метод": per-block scale
+//     stored in low precision (E4M3 / group 16, E8M0 / group 32), elements in
+//     FP4 E2M1, scale handling fused into the kernel.
+//   "UE5M3 FP4 Block Scaling ..." (rit.work blog), "Что сделали": UE5M3 block
+//     scale per 16 elements; the tensor maximum may be a stored (stale) value.
+//   gonzo_ML #3986, "Стохастическая квантизация": nearest rounding for forward
+//     weights/activations, stochastic rounding for backward tensors.
+//
+// Kernels:
+//   k_amax            max|x| of a bf16 matrix (fresh global amax), 2 B/elem read.
+//   k_quant_rows      blocks along K; one thread per 16 elements straight from
+//                     two 128-bit loads; 2 + 0.5 + 1/G B per element.
+//   k_quant_tile      32 x 256 tile staged in shared memory; writes the
+//                     transposed quantization (blocks along M) and, in the dual
+//                     form, the row quantization from the same read:
+//                     2 + 2 * (0.5 + 1/G) B per element.
+//   k_dequant         codes + scales -> float32 / bf16.
+//   k_ue5m3_*         UE5M3 -> shifted E4M3 re-encode for the tensor-core path.
+//   k_encode_scales, k_philox_bits16   conformance helpers (same device code).
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "fp4_device.cuh"
+#include "launch.h"
+
+using namespace fp4dev;
+
+namespace {
+
+__device__ __forceinline__ uint4 ld_stream(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ void atomic_max_nonneg(float* dst, float v) {
+  // non-negative IEEE floats order like their bit patterns
+  atomicMax(reinterpret_cast<unsigned int*>(dst), __float_as_uint(v));
+}
+
+// ---------------------------------------------------------------------------
+// K0: global amax
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) k_amax(const uint16_t* __restrict__ x, int64_t M, int64_t K,
+                                              int64_t ldx, float* __restrict__ out) {
+  const int64_t per_row = K / 8;  // 16-byte chunks per row
+  const int64_t total = M * per_row;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  uint32_t m = 0;
+  int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  for (; i + 3 * stride < total; i += 4 * stride) {
+    uint4 v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int64_t c = i + u * stride;
+      const int64_t r = c / per_row;
+      v[u] = ld_stream(x + r * ldx + (c - r * per_row) * 8);
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      m = absmax2(m, v[u].x & 0x7FFF7FFFu);
+      m = absmax2(m, v[u].y & 0x7FFF7FFFu);
+      m = absmax2(m, v[u].z & 0x7FFF7FFFu);
+      m = absmax2(m, v[u].w & 0x7FFF7FFFu);
+    }
+  }
+  for (; i < total; i += stride) {
+    const int64_t r = i / per_row;
+    const uint4 v = ld_stream(x + r * ldx + (i - r * per_row) * 8);
+    m = absmax2(m, v.x & 0x7FFF7FFFu);
+    m = absmax2(m, v.y & 0x7FFF7FFFu);
+    m = absmax2(m, v.z & 0x7FFF7FFFu);
+    m = absmax2(m, v.w & 0x7FFF7FFFu);
+  }
+  float a = fmaxf(bf16_lo(m), bf16_hi(m));
+  unsigned int ab = __reduce_max_sync(0xFFFFFFFFu, __float_as_uint(a));
+  __shared__ unsigned int warp_max[8];
+  if ((threadIdx.x & 31) == 0) warp_max[threadIdx.x >> 5] = ab;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    unsigned int v = threadIdx.x < (blockDim.x >> 5) ? warp_max[threadIdx.x] : 0u;
+    v = __reduce_max_sync(0xFFFFFFFFu, v);
+    if (threadIdx.x == 0) atomicMax(reinterpret_cast<unsigned int*>(out), v);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// K1: row quantizer (blocks along K)
+// ---------------------------------------------------------------------------
+template <int FMT, bool SR, bool MMA, bool AMAX>
+__global__ void __launch_bounds__(256) k_quant_rows(const uint16_t* __restrict__ x, int64_t M, int64_t K,
+                                                    int64_t ldx, const float* __restrict__ gptr,
+                                                    uint64_t seed, uint8_t* __restrict__ codes,
+                                                    uint8_t* __restrict__ scales,
+                                                    float* __restrict__ amax_out, int32_t* status) {
+  constexpr int G = ScaleFmt<FMT>::G;
+  const int64_t per_row = K / 16;
+  const int64_t chunk = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const bool valid = chunk < M * per_row;
+  const unsigned mask = __ballot_sync(0xFFFFFFFFu, valid);
+  if (!valid) return;
+  const float s_enc = global_encode_scale<FMT>(
+      __ldg(gptr), (blockIdx.x == 0 && threadIdx.x == 0) ? status : nullptr);
+  const int64_t row = chunk / per_row;
+  const int64_t c16 = chunk - row * per_row;
+  const uint16_t* src = x + row * ldx + c16 * 16;
+  const uint4 v0 = ld_stream(src), v1 = ld_stream(src + 8);
+  const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+  float a = absmax_words(w, 8);
+  if constexpr (AMAX) {
+    const unsigned int am = __reduce_max_sync(mask, __float_as_uint(a));
+    if ((threadIdx.x & 31) == (unsigned)(__ffs(mask) - 1)) atomicMax(reinterpret_cast<unsigned int*>(amax_out), am);
+  }
+  if constexpr (G == 32) a = fmaxf(a, __shfl_xor_sync(mask, a, 1));
+  const BlockScale bs = block_scale<FMT>(a, s_enc);
+  const uint2 q = quant16<SR>(w, bs.r, seed, (uint64_t)(row * K + c16 * 16));
+  *reinterpret_cast<uint2*>(codes + row * (K / 2) + c16 * 8) = q;
+  if (G == 16 || (c16 & 1) == 0) {
+    const int64_t b = c16 * 16 / G;
+    const int64_t nb = K / G;
+    const int64_t off = MMA ? mma_sf_offset(row, b, nb) : row * nb + b;
+    scales[off] = (uint8_t)bs.code;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// K2/K3: tile quantizer (transposed output, plus the row output when DUAL)
+// ---------------------------------------------------------------------------
+constexpr int TILE_M = 32;
+constexpr int TILE_K = 256;
+
+template <int FMT, bool DUAL, bool ROW_SR, bool COL_SR, bool MMA, bool AMAX>
+__global__ void __launch_bounds__(256) k_quant_tile(
+    const uint16_t* __restrict__ x, int64_t M, int64_t K, int64_t ldx, const float* __restrict__ gptr,
+    uint64_t seed_row, uint64_t seed_col, uint8_t* __restrict__ codes_row, uint8_t* __restrict__ scales_row,
+    uint8_t* __restrict__ codes_col, uint8_t* __restrict__ scales_col, float* __restrict__ amax_out,
+    int32_t* status) {
+  constexpr int G = ScaleFmt<FMT>::G;
+  __shared__ __align__(16) uint16_t tile[TILE_M][TILE_K];
+  // blockIdx.x walks M fastest so neighbouring CTAs fill the two halves of each
+  // 32-byte sector of the transposed output
+  const int64_t m0 = (int64_t)blockIdx.x * TILE_M;
+  const int64_t k0 = (int64_t)blockIdx.y * TILE_K;
+  const float s_enc = global_encode_scale<FMT>(
+      __ldg(gptr), (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) ? status : nullptr);
+
+  // ---- load 32 x 256 (two 16-element chunks per thread), row pass ----
+  float amax_local = 0.0f;
+#pragma unroll
+  for (int it = 0; it < 2; ++it) {
+    const int j = threadIdx.x + 256 * it;  // chunk id in the tile
+    const int r = j >> 4;                  // 16 chunks per tile row
+    const int cc = j & 15;
+    const int64_t col = k0 + cc * 16;
+    const bool valid = col < K;  // K % 32 == 0: a G=32 pair is valid together
+    uint32_t w[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    if (valid) {
+      const uint16_t* src = x + (m0 + r) * ldx + col;
+      const uint4 v0 = ld_stream(src), v1 = ld_stream(src + 8);
+      w[0] = v0.x; w[1] = v0.y; w[2] = v0.z; w[3] = v0.w;
+      w[4] = v1.x; w[5] = v1.y; w[6] = v1.z; w[7] = v1.w;
+    }
+    uint4* dst = reinterpret_cast<uint4*>(&tile[r][cc * 16]);
+    dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+    dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+    float a = absmax_words(w, 8);
+    amax_local = fmaxf(amax_local, a);
+    if constexpr (DUAL) {
+      if constexpr (G == 32) a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 1));
+      if (valid) {
+        const int64_t row = m0 + r;
+        const BlockScale bs = block_scale<FMT>(a, s_enc);
+        const uint2 q = quant16<ROW_SR>(w, bs.r, seed_row, (uint64_t)(row * K + col));
+        *reinterpret_cast<uint2*>(codes_row + row * (K / 2) + col / 2) = q;
+        if (G == 16 || (cc & 1) == 0) {
+          const int64_t b = col / G;
+          const int64_t nb = K / G;
+          scales_row[MMA ? mma_sf_offset(row, b, nb) : row * nb + b] = (uint8_t)bs.code;
+        }
+      }
+    }
+  }
+  if constexpr (AMAX) {
+    const unsigned int am = __reduce_max_sync(0xFFFFFFFFu, __float_as_uint(amax_local));
+    if ((threadIdx.x & 31) == 0) atomicMax(reinterpret_cast<unsigned int*>(amax_out), am);
+  }
+  __syncthreads();
+
+  // ---- column pass: thread t owns column k0 + t, rows m0 .. m0+31 ----
+  const int t = threadIdx.x;
+  const int64_t c = k0 + t;
+  if (c >= K) return;
+  uint32_t w[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i)
+    w[i] = (uint32_t)tile[2 * i][t] | ((uint32_t)tile[2 * i + 1][t] << 16);
+  const uint64_t idx0 = (uint64_t)(c * M + m0);
+  uint2 q0, q1;
+  uint32_t sc0, sc1 = 0;
+  if constexpr (G == 16) {
+    const BlockScale b0 = block_scale<FMT>(absmax_words(w, 8), s_enc);
+    const BlockScale b1 = block_scale<FMT>(absmax_words(w + 8, 8), s_enc);
+    q0 = quant16<COL_SR>(w, b0.r, seed_col, idx0);
+    q1 = quant16<COL_SR>(w + 8, b1.r, seed_col, idx0 + 16);
+    sc0 = b0.code;
+    sc1 = b1.code;
+  } else {
+    const BlockScale b0 = block_scale<FMT>(absmax_words(w, 16), s_enc);
+    q0 = quant16<COL_SR>(w, b0.r, seed_col, idx0);
+    q1 = quant16<COL_SR>(w + 8, b0.r, seed_col, idx0 + 16);
+    sc0 = b0.code;
+  }
+  *reinterpret_cast<uint4*>(codes_col + c * (M / 2) + m0 / 2) = make_uint4(q0.x, q0.y, q1.x, q1.y);
+  const int64_t nb = M / G;
+  const int64_t b = m0 / G;
+  if constexpr (G == 16) {
+    // blocks b, b+1 (b even) are adjacent bytes in both layouts
+    const int64_t off = MMA ? mma_sf_offset(c, b, nb) : c * nb + b;
+    *reinterpret_cast<uint16_t*>(scales_col + off) = (uint16_t)(sc0 | (sc1 << 8));
+  } else {
+    scales_col[MMA ? mma_sf_offset(c, b, nb) : c * nb + b] = (uint8_t)sc0;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// K4: dequantize
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float e2m1_value(uint32_t n) {
+  const uint32_t m = n & 7u;
+  float v = (m < 2u) ? (m == 1u ? 0.5f : 0.0f)
+                     : __uint_as_float(((126u + (m >> 1)) << 23) | ((m & 1u) << 22));
+  return (n & 8u) ? -v : v;
+}
+
+template <int FMT, bool MMA, bool BF16>
+__global__ void __launch_bounds__(256) k_dequant(const uint8_t* __restrict__ codes, const uint8_t* __restrict__ scales,
+                                                 int64_t M, int64_t K, const float* __restrict__ gptr,
+                                                 void* __restrict__ out) {
+  constexpr int G = ScaleFmt<FMT>::G;
+  const int64_t per_row = K / 16;
+  const int64_t chunk = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (chunk >= M * per_row) return;
+  const float s_enc = global_encode_scale<FMT>(__ldg(gptr), nullptr);
+  const int64_t row = chunk / per_row, c16 = chunk - row * per_row;
+  const int64_t b = c16 * 16 / G, nb = K / G;
+  const uint32_t code = scales[MMA ? mma_sf_offset(row, b, nb) : row * nb + b];
+  const float s_b = ScaleFmt<FMT>::decode(code);
+  const uint2 q = *reinterpret_cast<const uint2*>(codes + row * (K / 2) + c16 * 8);
+  float v[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const uint32_t word = i < 8 ? q.x : q.y;
+    const uint32_t n = (word >> (4 * (i & 7))) & 0xFu;
+    v[i] = __fdiv_rn(__fmul_rn(e2m1_value(n), s_b), s_enc);
+  }
+  if constexpr (BF16) {
+    uint32_t o[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+      o[i] = *reinterpret_cast<const uint32_t*>(&h);
+    }
+    uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(out) + row * K + c16 * 16);
+    dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+    dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+  } else {
+    float4* dst = reinterpret_cast<float4*>(static_cast<float*>(out) + row * K + c16 * 16);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// K8: UE5M3 -> E4M3 re-encode with a per-tensor power-of-two shift
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) k_ue5m3_maxcode(const uint8_t* __restrict__ s, int64_t n, int32_t* acc) {
+  unsigned int m = 0;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
+    m = max(m, (unsigned int)s[i]);
+  m = __reduce_max_sync(0xFFFFFFFFu, m);
+  if ((threadIdx.x & 31) == 0 && m > 0) atomicMax(reinterpret_cast<unsigned int*>(acc), m);
+}
+
+// t = e_max - 7 from the largest UE5M3 code (codes order like their values)
+__device__ __forceinline__ int ue5m3_shift_from_maxcode(uint32_t c) {
+  const uint32_t e = c >> 3, m = c & 7u;
+  if (e > 0) return (int)e - 15 - 7;
+  if (m == 0) return 0;
+  return (31 - __clz(m)) - 17 - 7;  // m * 2^-17, floor(log2 m) in 0..2
+}
+
+__global__ void __launch_bounds__(256) k_ue5m3_reencode(const uint8_t* __restrict__ s, int64_t n,
+                                                        const int32_t* maxcode, uint8_t* __restrict__ out,
+                                                        int32_t* status) {
+  const int t = ue5m3_shift_from_maxcode((uint32_t)__ldg(maxcode));
+  // 2^-t as a float (|t| <= 26)
+  const float scale = __uint_as_float((uint32_t)(127 - t) << 23);
+  bool bad = false;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+    const float v = __fmul_rn(ScaleFmt<SF_UE5M3>::decode(s[i]), scale);  // exact
+    const uint32_t c = ScaleFmt<SF_E4M3>::encode(v);
+    bad |= ScaleFmt<SF_E4M3>::decode(c) != v;
+    out[i] = (uint8_t)c;
+  }
+  if (__any_sync(0xFFFFFFFFu, bad) && (threadIdx.x & 31) == 0) set_status(status, FP4_ERR_UE5M3_RANGE);
+}
+
+__global__ void k_ue5m3_finalize(int32_t* t_inout) {
+  *t_inout = ue5m3_shift_from_maxcode((uint32_t)*t_inout);
+}
+
+// ---------------------------------------------------------------------------
+// Conformance helpers
+// ---------------------------------------------------------------------------
+template <int FMT>
+__global__ void __launch_bounds__(256) k_encode_scales(const float* __restrict__ s, int64_t n, uint8_t* codes,
+                                                       float* decoded) {
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  uint32_t c;
+  if constexpr (FMT == SF_E8M0) c = ScaleFmt<SF_E8M0>::encode_from_amax(s[i]);
+  else c = ScaleFmt<FMT>::encode(s[i]);
+  codes[i] = (uint8_t)c;
+  decoded[i] = ScaleFmt<FMT>::decode(c);
+}
+
+__global__ void __launch_bounds__(256) k_philox_bits16(uint64_t seed, uint64_t start, int64_t n, uint16_t* out) {
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  const uint64_t idx = start + (uint64_t)i;
+  const uint4 d = sr_draws8(seed, idx >> 3);
+  out[i] = (uint16_t)draw16(d, (int)(idx & 7));
+}
+
+inline unsigned grid_for(int64_t items, int per_block = 256) {
+  return (unsigned)((items + per_block - 1) / per_block);
+}
+
+}  // namespace
+
+// ===========================================================================
+// Launchers (called by the C ABI after argument checks)
+// ===========================================================================
+namespace fp4lib {
+
+cudaError_t launch_amax(const void* x, int64_t M, int64_t K, int64_t ldx, float* out, cudaStream_t st) {
+  cudaError_t e = cudaMemsetAsync(out, 0, sizeof(float), st);
+  if (e != cudaSuccess) return e;
+  if (M == 0 || K == 0) return cudaSuccess;
+  const int64_t chunks = M * (K / 8);
+  int64_t blocks = (chunks + 255) / 256;
+  const int64_t cap = 152 * 8;
+  if (blocks > cap) blocks = cap;
+  k_amax<<<(unsigned)blocks, 256, 0, st>>>(static_cast<const uint16_t*>(x), M, K, ldx, out);
+  return cudaGetLastError();
+}
+
+template <int FMT, bool SR, bool MMA, bool AMAX>
+static void rows_t(const QuantArgs& a, cudaStream_t st) {
+  const int64_t chunks = a.M * (a.K / 16);
+  if (chunks == 0) return;
+  k_quant_rows<FMT, SR, MMA, AMAX><<<grid_for(chunks), 256, 0, st>>>(
+      static_cast<const uint16_t*>(a.x), a.M, a.K, a.ldx, a.gptr, a.seed_row, a.codes_row, a.scales_row,
+      a.amax_out, a.status);
+}
+
+template <int FMT, bool DUAL, bool RSR, bool CSR, bool MMA, bool AMAX>
+static void tile_t(const QuantArgs& a, cudaStream_t st) {
+  if (a.M == 0 || a.K == 0) return;
+  dim3 grid((unsigned)(a.M / TILE_M), (unsigned)((a.K + TILE_K - 1) / TILE_K));
+  k_quant_tile<FMT, DUAL, RSR, CSR, MMA, AMAX><<<grid, 256, 0, st>>>(
+      static_cast<const uint16_t*>(a.x), a.M, a.K, a.ldx, a.gptr, a.seed_row, a.seed_col, a.codes_row,
+      a.scales_row, a.codes_col, a.scales_col, a.amax_out, a.status);
+}
+
+// runtime -> template dispatch
+template <int FMT>
+static void dispatch_fmt(const QuantArgs& a, cudaStream_t st) {
+  const bool amax = a.amax_by_product;
+  if (a.mode == QuantArgs::ROWS) {
+#define ROWS_CASE(SR, MMA, AM) \
+  if (a.row_sr == SR && a.mma == MMA && amax == AM) return rows_t<FMT, SR, MMA, AM>(a, st);
+    ROWS_CASE(false, false, false) ROWS_CASE(false, false, true) ROWS_CASE(false, true, false)
+    ROWS_CASE(false, true, true) ROWS_CASE(true, false, false) ROWS_CASE(true, false, true)
+    ROWS_CASE(true, true, false) ROWS_CASE(true, true, true)
+#undef ROWS_CASE
+  } else {
+    const bool dual = a.mode == QuantArgs::DUAL;
+#define TILE_CASE(D, RS, CS, MMA, AM)                                                           \
+  if (dual == D && (!D || a.row_sr == RS) && a.col_sr == CS && a.mma == MMA && amax == AM) \
+    return tile_t<FMT, D, RS, CS, MMA, AM>(a, st);
+#define TILE_CASES(D, RS) \
+  TILE_CASE(D, RS, false, false, false) TILE_CASE(D, RS, false, false, true) \
+  TILE_CASE(D, RS, false, true, false) TILE_CASE(D, RS, false, true, true)   \
+  TILE_CASE(D, RS, true, false, false) TILE_CASE(D, RS, true, false, true)   \
+  TILE_CASE(D, RS, true, true, false) TILE_CASE(D, RS, true, true, true)
+    TILE_CASES(false, false) TILE_CASES(true, false) TILE_CASES(true, true)
+#undef TILE_CASES
+#undef TILE_CASE
+  }
+}
+
+cudaError_t launch_quantize(const QuantArgs& a, cudaStream_t st) {
+  switch (a.fmt) {
+    case FP4_SF_E4M3: dispatch_fmt<SF_E4M3>(a, st); break;
+    case FP4_SF_UE5M3: dispatch_fmt<SF_UE5M3>(a, st); break;
+    case FP4_SF_E8M0: dispatch_fmt<SF_E8M0>(a, st); break;
+    case FP4_SF_E1M6: dispatch_fmt<SF_E1M6>(a, st); break;
+    default: return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dequantize(const uint8_t* codes, const uint8_t* scales, bool mma, int64_t M, int64_t K,
+                              int fmt, const float* gptr, bool bf16, void* out, cudaStream_t st) {
+  const int64_t chunks = M * (K / 16);
+  if (chunks == 0) return cudaSuccess;
+  const unsigned g = grid_for(chunks);
+#define DQ(F)                                                                                           \
+  if (mma && bf16) k_dequant<F, true, true><<<g, 256, 0, st>>>(codes, scales, M, K, gptr, out);         \
+  else if (mma) k_dequant<F, true, false><<<g, 256, 0, st>>>(codes, scales, M, K, gptr, out);           \
+  else if (bf16) k_dequant<F, false, true><<<g, 256, 0, st>>>(codes, scales, M, K, gptr, out);          \
+  else k_dequant<F, false, false><<<g, 256, 0, st>>>(codes, scales, M, K, gptr, out);
+  switch (fmt) {
+    case FP4_SF_E4M3: DQ(SF_E4M3) break;
+    case FP4_SF_UE5M3: DQ(SF_UE5M3) break;
+    case FP4_SF_E8M0: DQ(SF_E8M0) break;
+    case FP4_SF_E1M6: DQ(SF_E1M6) break;
+    default: return cudaErrorInvalidValue;
+  }
+#undef DQ
+  return cudaGetLastError();
+}
+
+cudaError_t launch_ue5m3_to_e4m3(const uint8_t* in, int64_t n, int32_t* t_out, uint8_t* out, int32_t* status,
+                                 cudaStream_t st) {
+  cudaError_t e = cudaMemsetAsync(t_out, 0, sizeof(int32_t), st);
+  if (e != cudaSuccess) return e;
+  if (n > 0) {
+    int64_t blocks = (n + 255) / 256;
+    if (blocks > 152 * 8) blocks = 152 * 8;
+    k_ue5m3_maxcode<<<(unsigned)blocks, 256, 0, st>>>(in, n, t_out);
+    k_ue5m3_reencode<<<(unsigned)blocks, 256, 0, st>>>(in, n, t_out, out, status);
+  }
+  k_ue5m3_finalize<<<1, 1, 0, st>>>(t_out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_encode_scales(const float* s, int64_t n, int fmt, uint8_t* codes, float* decoded,
+                                 cudaStream_t st) {
+  if (n == 0) return cudaSuccess;
+  const unsigned g = grid_for(n);
+  switch (fmt) {
+    case FP4_SF_E4M3: k_encode_scales<SF_E4M3><<<g, 256, 0, st>>>(s, n, codes, decoded); break;
+    case FP4_SF_UE5M3: k_encode_scales<SF_UE5M3><<<g, 256, 0, st>>>(s, n, codes, decoded); break;
+    case FP4_SF_E8M0: k_encode_scales<SF_E8M0><<<g, 256, 0, st>>>(s, n, codes, decoded); break;
+    case FP4_SF_E1M6: k_encode_scales<SF_E1M6><<<g, 256, 0, st>>>(s, n, codes, decoded); break;
+    default: return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_philox_bits16(uint64_t seed, uint64_t start, int64_t n, uint16_t* out, cudaStream_t st) {
+  if (n == 0) return cudaSuccess;
+  k_philox_bits16<<<grid_for(n), 256, 0, st>>>(seed, start, n, out);
+  return cudaGetLastError();
+}
+
+}  // namespace fp4lib

@@ -1,0 +1,41 @@
+"""GPU weight-only NVFP4 GEMV vs the oracle (through the C ABI)."""
+
+import numpy as np
+import pytest
+import torch
+
+from fp4_block_scaled_amax_gb300 import synth
+from oracle import gemm as Gm
+from oracle import quantize as Q
+from gpu_util import dev, f32, host, lib
+
+pytestmark = pytest.mark.gpu
+
+
+def run(W_bf16, x_bf16, out="f32"):
+    fp4 = lib()
+    qw = Q.quantize(f32(W_bf16), "E4M3")
+    N, K = W_bf16.shape
+    b = x_bf16.shape[0]
+    y = torch.empty((b, N), dtype=torch.float32 if out == "f32" else torch.bfloat16, device="cuda")
+    gw = torch.tensor([qw["amax"]], dtype=torch.float32, device="cuda")
+    fp4.fp4_gemv_w4a16(dev(qw["codes"]), dev(qw["scales"]), gw, dev(x_bf16), b, N, K,
+                       fp4.FP4_OUT_F32 if out == "f32" else fp4.FP4_OUT_BF16, y)
+    yr, S = Gm.gemv_ref(qw["codes"], qw["scales"], qw["amax"], f32(x_bf16))
+    yg = host(y.float())
+    bound = Gm.gemm_bound(S) + (np.abs(yr) * 2.0 ** -8 if out == "bf16" else 0)
+    err = np.abs(yg - yr)
+    assert (err <= bound).all(), f"worst ratio {np.max(err / bound):.3g}"
+
+
+@pytest.mark.parametrize("batch", [1, 3, 8, 13, 64])
+def test_gemv_scaled_shapes(batch):
+    d = synth.config5(batch, scale=4)  # W_up 4608 x 768, W_down 768 x 4608
+    run(d["W_up"], d["x_up"])
+    run(d["W_down"], d["x_down"], "bf16")
+
+
+def test_gemv_ragged_rows_and_k():
+    W = synth.normal((1000, 1056), 30, 0, std=0.02)  # N not a multiple of 16, K % 128 = 32
+    x = synth.normal((5, 1056), 30, 1)
+    run(W, x)

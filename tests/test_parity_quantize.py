@@ -1,0 +1,163 @@
+"""GPU quantizer vs the CPU oracle: codes and scales bit-exact (through the C ABI)."""
+
+import numpy as np
+import pytest
+import torch
+
+from fp4_block_scaled_amax_gb300 import synth
+from oracle import formats as F
+from oracle import philox as P
+from oracle import quantize as Q
+from gpu_util import dev, f32, from_mma, host, lib
+
+pytestmark = pytest.mark.gpu
+
+FMTS = ["E4M3", "UE5M3", "E8M0", "E1M6"]
+
+
+def gpu_quant(x_bf16, fmt, rounding, seed, g=None, transpose=False, mma=False):
+    fp4 = lib()
+    x = dev(x_bf16)
+    M, K = x.shape
+    rows, cols = (K, M) if transpose else (M, K)
+    G = Q.group_size(fmt)
+    codes = torch.empty((rows, cols // 2), dtype=torch.uint8, device="cuda")
+    scales = torch.empty((rows * cols // G,), dtype=torch.uint8, device="cuda")
+    amax_out = torch.zeros(1, dtype=torch.float32, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    gt = None if g is None else torch.tensor([g], dtype=torch.float32, device="cuda")
+    fp4.fp4_quantize(x, fmt, fp4.FP4_ROUND_STOCHASTIC if rounding == "sr" else fp4.FP4_ROUND_RNE, seed, gt,
+                     transpose, fp4.FP4_SFLAYOUT_MMA if mma else fp4.FP4_SFLAYOUT_PLAIN, codes, scales, amax_out, st)
+    sc = host(scales)
+    sc = from_mma(sc, rows, cols // G) if mma else sc.reshape(rows, cols // G)
+    return host(codes), sc, float(host(amax_out)[0]), int(host(st)[0])
+
+
+def check(x_bf16, fmt, rounding, seed, g=None, transpose=False, mma=False):
+    c, s, a, st = gpu_quant(x_bf16, fmt, rounding, seed, g, transpose, mma)
+    ref = Q.quantize(f32(x_bf16), fmt, rounding, seed, global_amax=g, transpose=transpose)
+    assert st == 0
+    assert np.array_equal(s, ref["scales"]), "scales differ"
+    if not np.array_equal(c, ref["codes"]):
+        bad = np.argwhere(c != ref["codes"])
+        r, k = bad[0]
+        raise AssertionError(f"{len(bad)} code bytes differ, first at {r},{k}: gpu {c[r, k]:#x} oracle "
+                             f"{ref['codes'][r, k]:#x}")
+    assert a == np.float32(ref["amax"])
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("rounding", ["rne", "sr"])
+def test_rows_config1_shapes(fmt, rounding):
+    d = synth.config1()
+    check(d["A"], fmt, rounding, 1234)
+    check(d["B"], fmt, rounding, 99)
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("rounding", ["rne", "sr"])
+def test_transposed_ragged(fmt, rounding):
+    # 96 x 800: three 32-row tiles, a ragged fourth 256-column tile
+    x = synth.normal((96, 800), 7, 0, outlier_p=0.01, outlier_mult=50.0)
+    check(x, fmt, rounding, 5, transpose=True)
+    check(x, fmt, rounding, 5, transpose=False)
+
+
+@pytest.mark.parametrize("fmt", ["E4M3", "UE5M3", "E8M0"])
+def test_mma_layout_and_stale_amax(fmt):
+    x = synth.normal((256, 512), 8, 0, outlier_p=0.01, outlier_mult=50.0)
+    g = float(x.float().abs().max()) / 3  # stale: true max 3x the stored one
+    check(x, fmt, "rne", 0, g=g, mma=True)
+    check(x, fmt, "sr", 3, g=g, transpose=True, mma=True)
+
+
+def test_dual_matches_two_single_calls():
+    fp4 = lib()
+    for fmt in FMTS:
+        G = Q.group_size(fmt)
+        x = synth.normal((160, 544), 9, 0, outlier_p=0.01, outlier_mult=50.0)
+        M, K = x.shape
+        xd = dev(x)
+        cr, sr = torch.empty((M, K // 2), dtype=torch.uint8, device="cuda"), torch.empty(M * K // G, dtype=torch.uint8, device="cuda")
+        cc, sc = torch.empty((K, M // 2), dtype=torch.uint8, device="cuda"), torch.empty(M * K // G, dtype=torch.uint8, device="cuda")
+        amax = torch.zeros(1, dtype=torch.float32, device="cuda")
+        fp4.fp4_quantize_dual(xd, fmt, fp4.FP4_ROUND_RNE, 11, fp4.FP4_ROUND_STOCHASTIC, 12, None,
+                              fp4.FP4_SFLAYOUT_PLAIN, cr, sr, cc, sc, amax)
+        ref_r = Q.quantize(f32(x), fmt, "rne", 11)
+        ref_c = Q.quantize(f32(x), fmt, "sr", 12, transpose=True)
+        assert np.array_equal(host(cr), ref_r["codes"]) and np.array_equal(host(sr).reshape(M, -1), ref_r["scales"])
+        assert np.array_equal(host(cc), ref_c["codes"]) and np.array_equal(host(sc).reshape(K, -1), ref_c["scales"])
+        assert float(host(amax)[0]) == ref_r["amax"]
+
+
+def test_edge_cases():
+    # zeros, a single outlier, exact E2M1 ties, bf16 subnormals, -0.0
+    M, K = 64, 256
+    x = np.zeros((M, K), dtype=np.float32)
+    x[1, 0] = 1e30
+    x[2, :16] = [6, 5, 3.5, 2.5, 1.75, 1.25, 0.75, 0.25, -6, -5, -3.5, -2.5, -1.75, -1.25, -0.75, -0.25]
+    x[3, :] = -0.0
+    x[4, :] = 9.2e-41  # bf16 subnormal
+    x[5, :32] = np.linspace(-1, 1, 32)
+    x[6, 5] = -3.0
+    xb = synth.to_bf16(x)
+    for fmt in FMTS:
+        for rnd in ("rne", "sr"):
+            check(xb, fmt, rnd, 77)
+            check(xb, fmt, rnd, 77, g=6.0)
+            check(xb, fmt, rnd, 77, transpose=True)
+
+
+def test_nonfinite_stored_amax_reports_status():
+    x = synth.normal((32, 64), 1, 0)
+    _, _, _, st = gpu_quant(x, "E4M3", "rne", 0, g=float("inf"))
+    assert st == lib().FP4_ERR_NONFINITE
+
+
+def test_empty_tensor_is_noop():
+    fp4 = lib()
+    x = torch.empty((0, 64), dtype=torch.bfloat16, device="cuda")
+    c = torch.empty((0, 32), dtype=torch.uint8, device="cuda")
+    s = torch.empty((0,), dtype=torch.uint8, device="cuda")
+    g = torch.ones(1, device="cuda")
+    fp4.fp4_quantize(x, "E4M3", 0, 0, g, False, 0, c, s)
+    torch.cuda.synchronize()
+
+
+def test_scale_encoder_conformance():
+    # every scale code boundary: midpoints, codes, and a dense sweep of float32 values
+    fp4 = lib()
+    for fmt in ["E4M3", "UE5M3", "E1M6"]:
+        codec = F.CODECS[fmt]
+        v = codec.vals
+        mids = (v[1:] + v[:-1]) / 2
+        rng = np.random.default_rng(0)
+        sweep = np.exp(rng.uniform(np.log(v[1] / 8), np.log(v[-1] * 4), 2_000_000))
+        s = np.concatenate([v, mids, np.nextafter(mids.astype(np.float32), 0), np.nextafter(mids.astype(np.float32), np.inf),
+                            sweep, [0.0, np.inf, 3.4e38]]).astype(np.float32)
+        codes = torch.empty(len(s), dtype=torch.uint8, device="cuda")
+        dec = torch.empty(len(s), dtype=torch.float32, device="cuda")
+        fp4.fp4_encode_scales(dev(s), fmt, codes, dec)
+        want = codec.encode(s.astype(np.float64))
+        assert np.array_equal(host(codes), want), fmt
+        assert np.array_equal(host(dec), codec.decode(want).astype(np.float32)), fmt
+    # E8M0 takes block amaxes
+    a = np.concatenate([np.exp(np.random.default_rng(1).uniform(-85, 85, 100000)), [0, 1e-45, 4.0, 8.0]]).astype(np.float32)
+    codes = torch.empty(len(a), dtype=torch.uint8, device="cuda")
+    dec = torch.empty(len(a), dtype=torch.float32, device="cuda")
+    fp4.fp4_encode_scales(dev(a), "E8M0", codes, dec)
+    want, wv = Q.block_scales(a, np.float32(1), "E8M0")
+    assert np.array_equal(host(codes), want)
+    assert np.array_equal(host(dec), wv)
+
+
+def test_philox_matches_oracle_10M():
+    fp4 = lib()
+    n = 10_000_000
+    for seed, start in [(1234, 0), (0xDEADBEEFCAFEF00D, (1 << 35) - 4096)]:
+        out = torch.empty(n, dtype=torch.int16, device="cuda")
+        fp4.fp4_philox_bits16(seed, start, n, out)
+        got = host(out).view(np.uint16)
+        idx = np.arange(start, start + n, dtype=np.uint64)
+        want = np.concatenate([P.sr_bits16(seed, idx[i:i + 1_000_000]) for i in range(0, n, 1_000_000)])
+        assert np.array_equal(got.astype(np.uint32), want)
