@@ -1,0 +1,475 @@
+#!/usr/bin/env python3
+"""Benchmark of the FP4 block-scaled linear layer at Llama-2-7B MLP shapes.
+
+One step is one pass of the whole hot path over the seeded synthetic workload
+"Llama-2 7B MLP linear, forward and backward" (tokens M = 16384, K = 4096,
+N = 11008; X N(0,1) with 0.5 % outliers x100, W N(0,0.02), dY Laplace(0,1e-4)):
+
+  fresh global amax of X, W, dY                      (3 x amax kernel)
+  dual quantization, E4M3 scales, 16-element blocks  (3 x tile quantizer)
+      X: rows RNE, X^T stochastic (seed 1236)
+      W: rows RNE, W^T RNE
+      dY: rows stochastic (seed 1234), dY^T stochastic (seed 1235)
+  forward  Y  = X W^T    16384 x 11008 x 4096  bf16 out (tcgen05 FP4 GEMM)
+  dgrad    dX = dY W     16384 x  4096 x 11008 bf16 out
+  wgrad    dW = dY^T X   11008 x  4096 x 16384 bf16 out
+  weight-only decode GEMV with the same layer's weight (quantized once,
+      batch 8): y = x W^T                                (GEMV kernel)
+
+metric: FP4 GEMM TFLOP/s of the whole step (3 * 2*M*N*K / step time);
+per-kernel rooflines from CUDA events on the launching stream.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+--impl reference times the CPU oracle (plain numpy, test infrastructure) on
+a bounded slice of the same step.  With N > 1 (torchrun) every rank runs its
+own independent batch (weak scaling, no collective on the data path).
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+M_TOK, K_HID, N_FFN = 16384, 4096, 11008
+GEMV_BATCH = 8
+STEP_FLOPS = 3 * 2 * M_TOK * N_FFN * K_HID
+WORKLOAD = "llama2-7b-mlp-linear-fwd-bwd"
+METRIC = "NVFP4 GEMM TFLOPS & quantize GB/s at 7B shapes, % of FP4-MMA/HBM peak"
+FP4_PER_BF16 = 6.0  # nominal dense FP4 / bf16 tensor ratio on GB300 (13.5 / 2.25 PFLOP/s)
+# DRAM traffic per launch from one ncu capture, valid only while the kernel
+# source hashes to the recorded value.
+NCU_TRAFFIC = {}
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=10)
+    p.add_argument("--warmup", type=int, default=3)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--tokens", type=int, default=16384,
+                   help="token count M (default: the workload's 16384; smaller only for ncu captures)")
+    return p.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (one process per GPU)
+# ---------------------------------------------------------------------------
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def dist_init(world, backend):
+    if world > 1 and not torch.distributed.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        torch.distributed.init_process_group(backend)
+
+
+def barrier(world):
+    if world > 1:
+        torch.distributed.barrier()
+
+
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """Largest value over all ranks (the slowest rank sets the time)."""
+    if world == 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# peaks, clocks, cpu baseline
+# ---------------------------------------------------------------------------
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons every 200 ms during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device):
+        # address the GPU by UUID: CUDA_VISIBLE_DEVICES may renumber devices
+        try:
+            u = str(torch.cuda.get_device_properties(device).uuid)
+            self.gpu = u if u.startswith("GPU-") else "GPU-" + u
+        except Exception:  # noqa: BLE001
+            self.gpu = str(device.index or 0)
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            out, _ = self.proc.communicate(timeout=10)
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in getattr(self, "lines", []):
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def oracle_slice_step(d, Ms=1024, Ns=1024):
+    """The oracle's version of one step restricted to Ms tokens x Ns output
+    features at full K (quantizations of the needed operands, then the three
+    float64 GEMMs).  Returns (flops, seconds)."""
+    from oracle import gemm as Gm
+    from oracle import quantize as Q
+    X = d["X"][:Ms].float().numpy()
+    W = d["W"][:Ns].float().numpy()
+    dY = d["dY"][:Ms, :Ns].float().numpy()
+    t0 = time.perf_counter()
+    qX = Q.quantize(X, "E4M3", "rne", 0)
+    qXt = Q.quantize(X, "E4M3", "sr", 1236, transpose=True)
+    qW = Q.quantize(W, "E4M3", "rne", 0)
+    qWt = Q.quantize(W, "E4M3", "rne", 0, transpose=True)
+    qd = Q.quantize(dY, "E4M3", "sr", 1234)
+    qdt = Q.quantize(dY, "E4M3", "sr", 1235, transpose=True)
+    for a, b in [(qX, qW), (qd, qWt), (qdt, qXt)]:
+        Gm.gemm_ref(a["codes"], a["scales"], a["amax"], b["codes"], b["scales"], b["amax"], "E4M3")
+    dt = time.perf_counter() - t0
+    return 3 * 2 * Ms * Ns * K_HID, dt
+
+
+def cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+# ---------------------------------------------------------------------------
+# the GPU step
+# ---------------------------------------------------------------------------
+
+class LinearStep:
+    """Device buffers of one step and the sequence of library calls."""
+
+    def __init__(self, d, device):
+        from fp4_block_scaled_amax_gb300 import fp4
+        self.fp4 = fp4
+        self.dev = device
+        M, K, N = M_TOK, K_HID, N_FFN
+        u8 = dict(dtype=torch.uint8, device=device)
+        self.X = d["X"].to(device)
+        self.W = d["W"].to(device)
+        self.dY = d["dY"].to(device)
+        self.amax = torch.zeros(3, dtype=torch.float32, device=device)
+        self.q = {}
+        for name, (R, C) in {"X": (M, K), "W": (N, K), "dY": (M, N)}.items():
+            self.q[name] = (torch.empty((R, C // 2), **u8), torch.empty(R * C // 16, **u8),
+                            torch.empty((C, R // 2), **u8), torch.empty(R * C // 16, **u8))
+        self.Y = torch.empty((M, N), dtype=torch.bfloat16, device=device)
+        self.dX = torch.empty((M, K), dtype=torch.bfloat16, device=device)
+        self.dW = torch.empty((N, K), dtype=torch.bfloat16, device=device)
+        # weight-only decode operand: W quantized once (plain scale layout)
+        self.Wg_codes = torch.empty((N, K // 2), **u8)
+        self.Wg_scales = torch.empty(N * K // 16, **u8)
+        self.Wg_amax = torch.zeros(1, dtype=torch.float32, device=device)
+        fp4.fp4_quantize(self.W, "E4M3", fp4.FP4_ROUND_RNE, 0, None, False, fp4.FP4_SFLAYOUT_PLAIN,
+                         self.Wg_codes, self.Wg_scales, self.Wg_amax)
+        self.xg = d["x_dec"].to(device)
+        self.yg = torch.empty((GEMV_BATCH, N), dtype=torch.bfloat16, device=device)
+        self.status = torch.zeros(1, dtype=torch.int32, device=device)
+        self.launches_per_step = 10
+
+    def run(self, ev=None):
+        """One step; ev: optional list of 11 CUDA events recorded between kernels."""
+        fp4 = self.fp4
+        RNE, SR, MMA = fp4.FP4_ROUND_RNE, fp4.FP4_ROUND_STOCHASTIC, fp4.FP4_SFLAYOUT_MMA
+        M, K, N = M_TOK, K_HID, N_FFN
+        st = torch.cuda.current_stream()
+
+        def mark(i):
+            if ev is not None:
+                ev[i].record(st)
+
+        mark(0)
+        for j, (name, rr, sr, rc, sc) in enumerate([("X", RNE, 0, SR, 1236), ("W", RNE, 0, RNE, 0),
+                                                     ("dY", SR, 1234, SR, 1235)]):
+            x = getattr(self, name)
+            a = self.amax[j:j + 1]
+            fp4.fp4_amax(x, a)
+            mark(1 + 2 * j)
+            cr, srs, cc, scs = self.q[name]
+            fp4.fp4_quantize_dual(x, "E4M3", rr, sr, rc, sc, a, MMA, cr, srs, cc, scs, None, self.status)
+            mark(2 + 2 * j)
+        qX, qW, qd = self.q["X"], self.q["W"], self.q["dY"]
+        aX, aW, ad = self.amax[0:1], self.amax[1:2], self.amax[2:3]
+        BF = fp4.FP4_OUT_BF16
+        fp4.fp4_gemm(qX[0], qX[1], qW[0], qW[1], aX, aW, None, None, M, N, K, "E4M3", BF, self.Y,
+                     dev_status=self.status)
+        mark(7)
+        fp4.fp4_gemm(qd[0], qd[1], qW[2], qW[3], ad, aW, None, None, M, K, N, "E4M3", BF, self.dX,
+                     dev_status=self.status)
+        mark(8)
+        fp4.fp4_gemm(qd[2], qd[3], qX[2], qX[3], ad, aX, None, None, N, K, M, "E4M3", BF, self.dW,
+                     dev_status=self.status)
+        mark(9)
+        fp4.fp4_gemv_w4a16(self.Wg_codes, self.Wg_scales, self.Wg_amax, self.xg, GEMV_BATCH, N, K, BF, self.yg)
+        mark(10)
+
+
+def make_inputs():
+    from fp4_block_scaled_amax_gb300 import synth
+    d = synth.config3()
+    if M_TOK != d["X"].shape[0]:
+        d["X"], d["dY"] = d["X"][:M_TOK].contiguous(), d["dY"][:M_TOK].contiguous()
+    d["x_dec"] = synth.normal((GEMV_BATCH, K_HID), 3, 50)
+    return d
+
+
+def src_hash(name):
+    with open(os.path.join(ROOT, "fp4_block_scaled_amax_gb300", "csrc", name), "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def run_ours(args, rank, world, local):
+    from fp4_block_scaled_amax_gb300 import build as b
+    if rank == 0:
+        b.build()
+    barrier(world)
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    d = make_inputs()
+    step = LinearStep(d, device)
+    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=device)  # > 129 MB L2
+
+    for _ in range(args.warmup):
+        step.run()
+    torch.cuda.synchronize()
+    if int(step.status.item()) != 0:
+        raise RuntimeError(f"device status {int(step.status.item())} during warm-up")
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(11)] for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(device) as clk:
+        for i in range(args.steps):
+            flush.zero_()  # L2 flush between timed steps, outside the events
+            step.run(evs[i])
+        torch.cuda.synchronize()
+    barrier(world)
+    if int(step.status.item()) != 0:
+        raise RuntimeError(f"device status {int(step.status.item())}")
+
+    def span(e, a, z):
+        return e[a].elapsed_time(e[z])
+
+    step_ms = [span(e, 0, 10) for e in evs]
+    ms = statistics.mean(step_ms)
+    ms_max = max_over_ranks(ms, world, device)
+    gemm_ms = [span(e, i, i + 1) for e in evs for i in (6, 7, 8)]
+    fwd_ms = [span(e, 6, 7) for e in evs]
+    quant_ms = [span(e, 2 * j + 1, 2 * j + 2) for e in evs for j in range(3)]
+    amax_ms = [span(e, 2 * j, 2 * j + 1) for e in evs for j in range(3)]
+    gemv_ms = [span(e, 9, 10) for e in evs]
+
+    hbm, bf16, src = peaks()
+    fp4_peak = bf16 * FP4_PER_BF16
+    gemm_tflops = 2 * M_TOK * N_FFN * K_HID / (statistics.mean(gemm_ms) * 1e-3) / 1e12
+    elems = [M_TOK * K_HID, N_FFN * K_HID, M_TOK * N_FFN]
+    q_bytes = sum(e * 3.125 for e in elems)          # per step, three dual quantizations
+    q_gbs = q_bytes / (sum(quant_ms) / args.steps * 1e-3) / 1e9
+    a_gbs = sum(e * 2 for e in elems) / (sum(amax_ms) / args.steps * 1e-3) / 1e9
+    gv_bytes = N_FFN * K_HID * (0.5 + 1 / 16) + 2 * GEMV_BATCH * (N_FFN + K_HID)
+    gv_gbs = gv_bytes / (statistics.mean(gemv_ms) * 1e-3) / 1e9
+    traffic = NCU_TRAFFIC.get("gemm")
+    traffic_v = traffic["bytes"] if traffic and traffic["src"] == src_hash("gemm_sm103.cu") else None
+    qtraffic = NCU_TRAFFIC.get("quant_dual")
+    qtraffic_v = qtraffic["bytes"] if qtraffic and qtraffic["src"] == src_hash("quantize.cu") else None
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(step, d, args, world, device)
+
+    line = {
+        "metric": METRIC,
+        "value": round(world * STEP_FLOPS / (ms_max * 1e-3) / 1e12, 2),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_max, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "e2m1xe2m1->f32 (tcgen05 kind::mxf4nvf4), bf16 in/out",
+        "data": "synthetic (seeded; shapes and distributions of the Llama-2-7B MLP workload)",
+        "config": {"workload": WORKLOAD if M_TOK == 16384 else WORKLOAD + "-reduced-tokens",
+                   "tokens": M_TOK, "hidden": K_HID, "ffn": N_FFN, "scale_fmt": "E4M3",
+                   "group": 16, "amax": "fresh per step", "gemm_out": "bf16", "gemv_batch": GEMV_BATCH,
+                   "l2": "512 MB buffer written between timed steps (outside the events); X and dY also exceed L2",
+                   "parallelism": f"dp{world} (independent batches)"},
+        "roofline": {"kernel": "k_gemm_fp4 (mean of fwd, dgrad, wgrad)", "bound": "tensor",
+                     "achieved": round(gemm_tflops, 1), "peak": round(fp4_peak, 1), "unit": "TFLOP/s",
+                     "frac": round(gemm_tflops / fp4_peak, 4), "traffic": traffic_v,
+                     "peak_source": f"{src}: bf16 burst {bf16} x {FP4_PER_BF16} (nominal FP4/bf16)"},
+        "roofline_quantize": {"kernel": "k_quant_tile (dual, 3.125 B/elem)", "bound": "hbm",
+                              "achieved": round(q_gbs, 1), "peak": hbm, "unit": "GB/s",
+                              "frac": round(q_gbs / hbm, 4), "traffic": qtraffic_v, "peak_source": src},
+        "amax_gbs": round(a_gbs, 1),
+        "gemv_w4a16": {"batch": GEMV_BATCH, "N": N_FFN, "K": K_HID, "us": round(statistics.mean(gemv_ms) * 1e3, 2),
+                       "GB/s": round(gv_gbs, 1), "frac": round(gv_gbs / hbm, 4)},
+        "kernel_ms": {"fwd_gemm": round(statistics.mean(fwd_ms), 4),
+                      "gemm_mean": round(statistics.mean(gemm_ms), 4),
+                      "quant_dual_total": round(sum(quant_ms) / args.steps, 4),
+                      "amax_total": round(sum(amax_ms) / args.steps, 4)},
+        "gpu_launches": step.launches_per_step * args.steps,
+        "clocks": clk.summary(),
+    }
+    if e2e is not None:
+        line["e2e"] = e2e
+    if rank == 0 and not args.no_cpu_baseline:
+        flops, dt = oracle_slice_step(d)
+        line["cpu_baseline"] = {"value": round(flops / dt / 1e12, 6), "unit": "TFLOP/s", "cores": cores(),
+                                "kind": "oracle",
+                                "sample": "oracle step on 1024 tokens x 1024 output features at K=4096 "
+                                          f"(quantize 6 operands + 3 float64 GEMMs), {dt:.1f} s"}
+    return line
+
+
+def run_e2e(step, d, args, world, device):
+    """Same metric through the C ABI with host buffers: H2D of X, W, dY and
+    D2H of Y, dX, dW inside the timed region (pinned host memory)."""
+    hX, hW, hdY = (d[k].pin_memory() for k in ("X", "W", "dY"))
+    hY = torch.empty(step.Y.shape, dtype=torch.bfloat16).pin_memory()
+    hdX = torch.empty(step.dX.shape, dtype=torch.bfloat16).pin_memory()
+    hdW = torch.empty(step.dW.shape, dtype=torch.bfloat16).pin_memory()
+
+    def one():
+        step.X.copy_(hX, non_blocking=True)
+        step.W.copy_(hW, non_blocking=True)
+        step.dY.copy_(hdY, non_blocking=True)
+        step.run()
+        hY.copy_(step.Y, non_blocking=True)
+        hdX.copy_(step.dX, non_blocking=True)
+        hdW.copy_(step.dW, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        one()
+    torch.cuda.synchronize()
+    barrier(world)
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record()
+    for _ in range(args.steps):
+        one()
+    e.record()
+    torch.cuda.synchronize()
+    ms = max_over_ranks(s.elapsed_time(e) / args.steps, world, device)
+    h2d = sum(t.numel() * t.element_size() for t in (hX, hW, hdY))
+    d2h = sum(t.numel() * t.element_size() for t in (hY, hdX, hdW))
+    return {"value": round(world * STEP_FLOPS / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+            "ms_per_step": round(ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+def run_reference(args, rank, world):
+    """The CPU oracle, timed as it stands, on a bounded slice of the step."""
+    if rank != 0:
+        return None
+    d = make_inputs()
+    for _ in range(args.warmup):
+        oracle_slice_step(d, 512, 512)
+    times = []
+    flops = 0
+    for _ in range(args.steps):
+        flops, dt = oracle_slice_step(d, 512, 512)
+        times.append(dt)
+    sec = statistics.mean(times)
+    v = round(flops / sec / 1e12, 6)
+    return {
+        "impl": "reference", "metric": METRIC, "value": v, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(sec * 1e3, 2),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)",
+        "data": "synthetic (seeded)",
+        "config": {"workload": WORKLOAD, "tokens": M_TOK, "hidden": K_HID, "ffn": N_FFN, "scale_fmt": "E4M3",
+                   "group": 16, "parallelism": "cpu"},
+        "cpu_baseline": {"value": v, "unit": "TFLOP/s", "cores": cores(), "kind": "oracle",
+                         "sample": "each step: oracle step on 512 tokens x 512 output features at K=4096 "
+                                   "(quantize 6 operands + 3 float64 GEMMs)"},
+        "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    global M_TOK, STEP_FLOPS
+    args = parse()
+    if args.tokens != M_TOK:
+        if args.tokens % 256 or args.tokens <= 0:
+            raise SystemExit("--tokens must be a positive multiple of 256")
+        M_TOK = args.tokens
+        STEP_FLOPS = 3 * 2 * M_TOK * N_FFN * K_HID
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return
+    dist_init(world, "nccl")
+    line = run_ours(args, rank, world, local)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
