@@ -184,29 +184,25 @@ __device__ __forceinline__ uint32_t e2m1_rne_soft(float y) {
 
 // Stochastic rounding of one value with a 16-bit draw r: lo <= |y| < hi the
 // neighbouring grid values, round up iff r < 65536 * (|y| - lo) / (hi - lo);
-// |y| >= 6 gives 6.  Both sides of the comparison are exact in float32.
+// |y| >= 6 gives 6.  Branch-free on the float32 bits b of |y|:
+//  * |y| >= 1: the grid keeps one mantissa bit, and f * 2^22 is the low 22
+//    bits m22, so "up" is 64 r < m22, i.e. the carry out of
+//    m22 + (2^22 - 1 - 64 r) into bit 22; the truncated sum then holds the
+//    code: (b' >> 22) - 252 = 2 (e - 127) + 2 + m1 + up.
+//  * 0.5 <= |y| < 1: the grid step is 0.5, "up" is 128 r < m23, the carry of
+//    m23 + (2^23 - 1 - 128 r) into the exponent; code (b' >> 23) - 125.
+//  * |y| < 0.5: up iff r < |y| * 2^17, compared in float32 (both exact; r is
+//    rebuilt as 2^16 + r - 2^16 without a conversion instruction).
 __device__ __forceinline__ uint32_t e2m1_sr(float y, uint32_t r16) {
-  const float a = fabsf(y);
-  uint32_t lc;
-  float lo, sc;
-  if (a < 2.0f) {
-    lc = (uint32_t)__float2uint_rz(__fmul_rn(a, 2.0f));  // 0..3
-    lo = __fmul_rn((float)lc, 0.5f);
-    sc = 131072.0f;  // 65536 / 0.5
-  } else if (a < 4.0f) {
-    const float f = floorf(a);
-    lc = (uint32_t)f + 2u;  // 4, 5
-    lo = f;
-    sc = 65536.0f;
-  } else {
-    lc = 6u;
-    lo = 4.0f;
-    sc = 32768.0f;  // 65536 / 2
-  }
-  const float t = __fmul_rn(__fsub_rn(a, lo), sc);
-  uint32_t m = lc + (uint32_t)((float)r16 < t);
-  m = (a >= 6.0f) ? 7u : m;
-  return m | ((__float_as_uint(y) >> 28) & 8u);
+  const uint32_t yb = __float_as_uint(y);
+  const uint32_t b = yb & 0x7FFFFFFFu;
+  const uint32_t rn = (~r16) & 0xFFFFu;  // 65535 - r
+  const uint32_t c_hi = min(((b + ((rn << 6) | 63u)) >> 22) - 252u, 7u);
+  const uint32_t c_mid = ((b + ((rn << 7) | 127u)) >> 23) - 125u;
+  const float rf = __fsub_rn(__uint_as_float(0x47800000u | (r16 << 7)), 65536.0f);
+  const uint32_t c_lo = (rf < __fmul_rn(__uint_as_float(b), 131072.0f)) ? 1u : 0u;
+  const uint32_t m = b >= 0x3F800000u ? c_hi : (b >= 0x3F000000u ? c_mid : c_lo);
+  return m | ((yb >> 28) & 8u);
 }
 
 // ---------------------------------------------------------------------------

@@ -76,12 +76,81 @@ __device__ __forceinline__ uint32_t e4m3_to_bf16x2(uint32_t c) {
   return h | (h << 16);
 }
 
+// Loads of one 128-wide k chunk for one lane: 16 code bytes and 2 scale bytes
+// of its two weight rows, and its 32 activations of each batch row it feeds.
 template <int NT>
-__global__ void __launch_bounds__(256) k_gemv_w4a16(const uint8_t* __restrict__ Wq, const uint8_t* __restrict__ Ws,
+struct Chunk {
+  uint4 w0, w1;
+  uint32_t s0, s1;
+  uint4 xb[NT][4];
+};
+
+template <int NT>
+__device__ __forceinline__ void load_chunk(Chunk<NT>& ch, const uint8_t* __restrict__ Wq,
+                                           const uint8_t* __restrict__ Ws, const uint16_t* __restrict__ x,
+                                           int64_t r0, int64_t r1, bool v0, bool v1, int64_t k0, int64_t K,
+                                           int batch, int g) {
+  const bool kin = k0 < K;  // K % 32 == 0: a lane's 32 columns are all in or all out
+  ch.w0 = ch.w1 = make_uint4(0, 0, 0, 0);
+  ch.s0 = ch.s1 = 0;
+  if (kin && v0) {
+    ch.w0 = ld_stream16(Wq + r0 * (K / 2) + k0 / 2);
+    ch.s0 = *reinterpret_cast<const uint16_t*>(Ws + r0 * (K / 16) + k0 / 16);
+  }
+  if (kin && v1) {
+    ch.w1 = ld_stream16(Wq + r1 * (K / 2) + k0 / 2);
+    ch.s1 = *reinterpret_cast<const uint16_t*>(Ws + r1 * (K / 16) + k0 / 16);
+  }
+#pragma unroll
+  for (int t = 0; t < NT; ++t) {
+    const int b = t * 8 + g;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) ch.xb[t][i] = make_uint4(0, 0, 0, 0);
+    if (kin && b < batch) {
+      const uint4* src = reinterpret_cast<const uint4*>(x + (int64_t)b * K + k0);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) ch.xb[t][i] = __ldg(src + i);
+    }
+  }
+}
+
+template <int NT>
+__device__ __forceinline__ void mma_chunk(float (&acc)[NT][4], const Chunk<NT>& ch) {
+  const uint32_t sc0[2] = {e4m3_to_bf16x2(ch.s0 & 0xFFu), e4m3_to_bf16x2(ch.s0 >> 8)};
+  const uint32_t sc1[2] = {e4m3_to_bf16x2(ch.s1 & 0xFFu), e4m3_to_bf16x2(ch.s1 >> 8)};
+  const uint32_t cw0[4] = {ch.w0.x, ch.w0.y, ch.w0.z, ch.w0.w};
+  const uint32_t cw1[4] = {ch.w1.x, ch.w1.y, ch.w1.z, ch.w1.w};
+#pragma unroll
+  for (int s = 0; s < 8; ++s) {
+    const uint32_t c0 = (cw0[s >> 1] >> (16 * (s & 1))) & 0xFFFFu;
+    const uint32_t c1 = (cw1[s >> 1] >> (16 * (s & 1))) & 0xFFFFu;
+    uint32_t a0, a2, a1, a3;
+    e2m1x4_to_bf16x4(c0, a0, a2);
+    e2m1x4_to_bf16x4(c1, a1, a3);
+    a0 = bf16x2_mul(a0, sc0[s >> 2]);
+    a2 = bf16x2_mul(a2, sc0[s >> 2]);
+    a1 = bf16x2_mul(a1, sc1[s >> 2]);
+    a3 = bf16x2_mul(a3, sc1[s >> 2]);
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+      const uint4 xv = ch.xb[t][s >> 1];
+      const uint32_t b0 = (s & 1) ? xv.z : xv.x;
+      const uint32_t b1 = (s & 1) ? xv.w : xv.y;
+      mma_bf16_16816(acc[t], a0, a1, a2, a3, b0, b1);
+    }
+  }
+}
+
+constexpr int MAX_WARPS = 16;
+
+template <int NT>
+__global__ void __launch_bounds__(NT <= 2 ? 512 : 256) k_gemv_w4a16(const uint8_t* __restrict__ Wq, const uint8_t* __restrict__ Ws,
                                                      const float* __restrict__ gw, const uint16_t* __restrict__ x,
                                                      int batch, int64_t N, int64_t K, bool bf16_out,
                                                      void* __restrict__ y) {
-  __shared__ float red[8][16][8 * NT];
+  // partial sums [warp][row][batch]; 16 warps x 16 rows x 32 (NT <= 4) or
+  // 8 warps x 16 x 64 (NT = 8): 32 KB either way
+  __shared__ float red[MAX_WARPS * 16 * 32];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nwarps = blockDim.x >> 5;
   const int g = lane >> 2, q = lane & 3;
@@ -97,75 +166,41 @@ __global__ void __launch_bounds__(256) k_gemv_w4a16(const uint8_t* __restrict__ 
 #pragma unroll
   for (int t = 0; t < NT; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.0f;
 
-  const int64_t row_bytes = K / 2, row_scales = K / 16;
-  for (int64_t c = c_begin; c < c_end; ++c) {
-    const int64_t k0 = c * 128 + 32 * q;  // first actual column of this lane
-    const bool kin = k0 < K;              // K % 32 == 0: a lane's 32 columns are all in or all out
-    uint4 w0 = make_uint4(0, 0, 0, 0), w1 = make_uint4(0, 0, 0, 0);
-    uint32_t s0 = 0, s1 = 0;
-    if (kin) {
-      if (v0) {
-        w0 = ld_stream16(Wq + r0 * row_bytes + k0 / 2);
-        s0 = *reinterpret_cast<const uint16_t*>(Ws + r0 * row_scales + k0 / 16);
-      }
-      if (v1) {
-        w1 = ld_stream16(Wq + r1 * row_bytes + k0 / 2);
-        s1 = *reinterpret_cast<const uint16_t*>(Ws + r1 * row_scales + k0 / 16);
-      }
+  if constexpr (NT <= 2) {
+    // software pipeline: the next chunk's loads are in flight during this chunk's MMAs
+    Chunk<NT> cur, nxt;
+    if (c_begin < c_end) load_chunk<NT>(cur, Wq, Ws, x, r0, r1, v0, v1, c_begin * 128 + 32 * q, K, batch, g);
+    for (int64_t c = c_begin; c < c_end; ++c) {
+      if (c + 1 < c_end) load_chunk<NT>(nxt, Wq, Ws, x, r0, r1, v0, v1, (c + 1) * 128 + 32 * q, K, batch, g);
+      mma_chunk<NT>(acc, cur);
+      cur = nxt;
     }
-    // activations for this lane's columns, one 8-row batch tile per t
-    uint4 xb[NT][4];
-#pragma unroll
-    for (int t = 0; t < NT; ++t) {
-      const int b = t * 8 + g;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) xb[t][i] = make_uint4(0, 0, 0, 0);
-      if (kin && b < batch) {
-        const uint4* src = reinterpret_cast<const uint4*>(x + (int64_t)b * K + k0);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) xb[t][i] = __ldg(src + i);
-      }
-    }
-    const uint32_t sc0[2] = {e4m3_to_bf16x2(s0 & 0xFFu), e4m3_to_bf16x2(s0 >> 8)};
-    const uint32_t sc1[2] = {e4m3_to_bf16x2(s1 & 0xFFu), e4m3_to_bf16x2(s1 >> 8)};
-    const uint32_t cw0[4] = {w0.x, w0.y, w0.z, w0.w};
-    const uint32_t cw1[4] = {w1.x, w1.y, w1.z, w1.w};
-#pragma unroll
-    for (int s = 0; s < 8; ++s) {
-      const uint32_t c0 = (cw0[s >> 1] >> (16 * (s & 1))) & 0xFFFFu;
-      const uint32_t c1 = (cw1[s >> 1] >> (16 * (s & 1))) & 0xFFFFu;
-      uint32_t a0, a2, a1, a3;
-      e2m1x4_to_bf16x4(c0, a0, a2);
-      e2m1x4_to_bf16x4(c1, a1, a3);
-      a0 = bf16x2_mul(a0, sc0[s >> 2]);
-      a2 = bf16x2_mul(a2, sc0[s >> 2]);
-      a1 = bf16x2_mul(a1, sc1[s >> 2]);
-      a3 = bf16x2_mul(a3, sc1[s >> 2]);
-#pragma unroll
-      for (int t = 0; t < NT; ++t) {
-        const uint4 xv = xb[t][s >> 1];
-        const uint32_t b0 = (s & 1) ? xv.z : xv.x;
-        const uint32_t b1 = (s & 1) ? xv.w : xv.y;
-        mma_bf16_16816(acc[t], a0, a1, a2, a3, b0, b1);
-      }
+  } else {
+    // larger batches: 32 MMAs per chunk hide the load latency; one buffer keeps
+    // the activations in registers without spilling
+    for (int64_t c = c_begin; c < c_end; ++c) {
+      Chunk<NT> cur;
+      load_chunk<NT>(cur, Wq, Ws, x, r0, r1, v0, v1, c * 128 + 32 * q, K, batch, g);
+      mma_chunk<NT>(acc, cur);
     }
   }
   // D fragment: (row g, cols 2q, 2q+1) and (row g+8, cols 2q, 2q+1)
+  constexpr int BW = 8 * NT;
 #pragma unroll
   for (int t = 0; t < NT; ++t) {
-    red[warp][g][t * 8 + 2 * q] = acc[t][0];
-    red[warp][g][t * 8 + 2 * q + 1] = acc[t][1];
-    red[warp][g + 8][t * 8 + 2 * q] = acc[t][2];
-    red[warp][g + 8][t * 8 + 2 * q + 1] = acc[t][3];
+    red[(warp * 16 + g) * BW + t * 8 + 2 * q] = acc[t][0];
+    red[(warp * 16 + g) * BW + t * 8 + 2 * q + 1] = acc[t][1];
+    red[(warp * 16 + g + 8) * BW + t * 8 + 2 * q] = acc[t][2];
+    red[(warp * 16 + g + 8) * BW + t * 8 + 2 * q + 1] = acc[t][3];
   }
   __syncthreads();
   const float s_enc = fp4dev::global_encode_scale<fp4dev::SF_E4M3>(__ldg(gw), nullptr);
-  for (int i = threadIdx.x; i < 16 * 8 * NT; i += blockDim.x) {
-    const int r = i / (8 * NT), b = i % (8 * NT);
+  for (int i = threadIdx.x; i < 16 * BW; i += blockDim.x) {
+    const int r = i / BW, b = i % BW;
     const int64_t n = n0 + r;
     if (n >= N || b >= batch) continue;
     float v = 0.0f;
-    for (int w = 0; w < nwarps; ++w) v = __fadd_rn(v, red[w][r][b]);
+    for (int w = 0; w < nwarps; ++w) v = __fadd_rn(v, red[(w * 16 + r) * BW + b]);
     v = __fdiv_rn(v, s_enc);
     if (bf16_out) static_cast<__nv_bfloat16*>(y)[(int64_t)b * N + n] = __float2bfloat16_rn(v);
     else static_cast<float*>(y)[(int64_t)b * N + n] = v;
@@ -177,14 +212,26 @@ __global__ void __launch_bounds__(256) k_gemv_w4a16(const uint8_t* __restrict__ 
 namespace fp4lib {
 
 cudaError_t launch_gemv(const GemvArgs& a, cudaStream_t st) {
-  const unsigned grid = (unsigned)((a.N + 15) / 16);
+  // 16 weight rows per CTA; enough warps per CTA (split K) to put about 16
+  // warps on each of the GPU's SMs in a single wave
+  const int64_t ctas = (a.N + 15) / 16;
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int64_t kchunks = (a.K + 127) / 128;
+  int64_t warps = (int64_t)sms * 16 / ctas;
+  warps = warps < 4 ? 4 : (warps > MAX_WARPS ? MAX_WARPS : warps);
+  if (warps > kchunks) warps = kchunks < 1 ? 1 : kchunks;
   const int nt = (int)((a.batch + 7) / 8);
+  if (nt > 2 && warps > 8) warps = 8;  // the larger batch tiles launch with at most 256 threads
+  const unsigned grid = (unsigned)ctas;
+  const unsigned threads = (unsigned)(32 * warps);
   const auto* x = static_cast<const uint16_t*>(a.x);
   const int b = (int)a.batch;
-  if (nt == 1) k_gemv_w4a16<1><<<grid, 256, 0, st>>>(a.Wq, a.Ws, a.gw, x, b, a.N, a.K, a.bf16_out, a.y);
-  else if (nt == 2) k_gemv_w4a16<2><<<grid, 256, 0, st>>>(a.Wq, a.Ws, a.gw, x, b, a.N, a.K, a.bf16_out, a.y);
-  else if (nt <= 4) k_gemv_w4a16<4><<<grid, 256, 0, st>>>(a.Wq, a.Ws, a.gw, x, b, a.N, a.K, a.bf16_out, a.y);
-  else k_gemv_w4a16<8><<<grid, 256, 0, st>>>(a.Wq, a.Ws, a.gw, x, b, a.N, a.K, a.bf16_out, a.y);
+  if (nt == 1) k_gemv_w4a16<1><<<grid, threads, 0, st>>>(a.Wq, a.Ws, a.gw, x, b, a.N, a.K, a.bf16_out, a.y);
+  else if (nt == 2) k_gemv_w4a16<2><<<grid, threads, 0, st>>>(a.Wq, a.Ws, a.gw, x, b, a.N, a.K, a.bf16_out, a.y);
+  else if (nt <= 4) k_gemv_w4a16<4><<<grid, threads, 0, st>>>(a.Wq, a.Ws, a.gw, x, b, a.N, a.K, a.bf16_out, a.y);
+  else k_gemv_w4a16<8><<<grid, threads, 0, st>>>(a.Wq, a.Ws, a.gw, x, b, a.N, a.K, a.bf16_out, a.y);
   return cudaGetLastError();
 }
 
