@@ -14,18 +14,25 @@
 // scales arrive re-encoded as E4M3 of s * 2^-t (exact) and 2^(tA + tB) folds
 // into alpha (the software emulation of the "UE5M3 ..." blog, "Ограничения").
 //
-// Kernel structure (one CTA per SM, persistent over 128 x 256 output tiles):
-//   warp 0      TMA producer: A/B code tiles (128-byte swizzle) by
-//               cp.async.bulk.tensor, scale atoms by cp.async.bulk, into a
-//               4-stage shared-memory ring guarded by mbarriers;
-//   warp 1      allocates tensor memory; one lane moves each stage's scales
-//               into tensor memory (tcgen05.cp 32x128b.warpx4) and issues the
-//               4 tcgen05.mma of the 256-wide K step; tcgen05.commit frees the
-//               stage and, after the last K step, hands the accumulator over;
-//   warps 2-9   epilogue: tcgen05.ld the 128 x 256 float32 accumulator into
-//               registers (each warp 32 rows x 128 columns), release the
-//               tensor memory at once so the next tile's MMAs overlap the
-//               conversion and the global stores.
+// Kernel structure (one CTA per SM, persistent over 128 x 256 output tiles,
+// 22 warps):
+//   warp 0       TMA producer: A/B code tiles (128-byte swizzle) by
+//                cp.async.bulk.tensor, scale atoms by cp.async.bulk, into a
+//                3-stage shared-memory ring guarded by mbarriers;
+//   warp 1       allocates tensor memory; one lane issues the 4 tcgen05.mma of
+//                each 256-wide K step once its scales sit in tensor memory, and
+//                tcgen05.commit frees the stage (and, after the last K step,
+//                hands the accumulator over);
+//   warps 2-5    scale writers, one per 32-lane quarter of tensor memory: each
+//                lane reads its row of every 512-byte scale atom from shared
+//                memory and writes it with tcgen05.st into the replicated
+//                layout the MMA reads (row r's scales in column r/32 of lane
+//                r%32 of every quarter);
+//   warps 6-21   epilogue: each warp drains 32 rows x 64 columns of the
+//                float32 accumulator with tcgen05.ld, releases the tensor
+//                memory at once (the next tile's MMAs overlap the rest), scales,
+//                converts and stages 32 x 64-byte blocks in 64-byte-swizzled
+//                shared memory, and writes them with TMA bulk-tensor stores.
 // Every mbarrier wait is bounded: on expiry the CTA records FP4_ERR_TIMEOUT in
 // the status word and winds down instead of spinning.
 #include <cstdint>
@@ -42,26 +49,37 @@ namespace {
 constexpr int BM = 128;
 constexpr int BN = 256;
 constexpr int BK = 256;  // FP4 elements per K step = 128 bytes per row
-constexpr int STAGES = 4;
-constexpr int A_BYTES = BM * BK / 2;     // 16 KB
-constexpr int B_BYTES = BN * BK / 2;     // 32 KB
-constexpr int SFA_MAX = BM * BK / 16;    // 2 KB (NVFP4); MXFP4 uses half
-constexpr int SFB_MAX = BN * BK / 16;    // 4 KB
+constexpr int STAGES = 3;
+constexpr int A_BYTES = BM * BK / 2;   // 16 KB
+constexpr int B_BYTES = BN * BK / 2;   // 32 KB
+constexpr int SFA_MAX = BM * BK / 16;  // 2 KB (NVFP4); MXFP4 uses half
+constexpr int SFB_MAX = BN * BK / 16;  // 4 KB
+
+constexpr int NUM_SF_WARPS = 4;
+constexpr int NUM_EPI_WARPS = 16;
+constexpr int FIRST_SF_WARP = 2;
+constexpr int FIRST_EPI_WARP = FIRST_SF_WARP + NUM_SF_WARPS;
+constexpr int NUM_THREADS = 32 * (FIRST_EPI_WARP + NUM_EPI_WARPS);
+constexpr int EPI_COLS = BN / (NUM_EPI_WARPS / 4);  // 64 accumulator columns per epilogue warp
+constexpr int STAGE_BYTES = 32 * 64;                 // one 32-row x 64-byte output block
+
 constexpr int SMEM_A = 0;
 constexpr int SMEM_B = SMEM_A + STAGES * A_BYTES;
 constexpr int SMEM_SFA = SMEM_B + STAGES * B_BYTES;
 constexpr int SMEM_SFB = SMEM_SFA + STAGES * SFA_MAX;
-constexpr int SMEM_BAR = SMEM_SFB + STAGES * SFB_MAX;
+constexpr int SMEM_OUT = SMEM_SFB + STAGES * SFB_MAX;  // 1024-aligned
+constexpr int SMEM_BAR = SMEM_OUT + NUM_EPI_WARPS * STAGE_BYTES;
 constexpr int SMEM_TOTAL = SMEM_BAR + 256;
 constexpr int SMEM_LAUNCH = SMEM_TOTAL + 1024;  // room to align the base to 1024
+static_assert(SMEM_OUT % 1024 == 0, "output staging must stay 1024-byte aligned");
+static_assert(SMEM_LAUNCH <= 232448, "shared memory over the sm_103a per-CTA limit");
 
-constexpr int NUM_EPI_WARPS = 8;
-constexpr int NUM_THREADS = 32 * (2 + NUM_EPI_WARPS);
-
-// tensor memory columns: accumulator 0..255, scales for 4 stages after it
+// tensor memory columns: accumulator 0..255, then per stage 16 columns of A
+// scales (4 K64 steps x 4) and 32 of B scales (4 K64 steps x 2 halves x 4)
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t TMEM_SFA = 256;             // 16 columns per stage
-constexpr uint32_t TMEM_SFB = 256 + 16 * STAGES;  // 32 columns per stage
+constexpr uint32_t TMEM_SFA = 256;
+constexpr uint32_t TMEM_SFB = TMEM_SFA + 16 * STAGES;
+static_assert(TMEM_SFB + 32 * STAGES <= TMEM_COLS, "tensor memory budget");
 
 constexpr long long WAIT_LIMIT_CYCLES = 4000000000LL;  // ~2 s at 2 GHz
 
@@ -116,6 +134,15 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
       : "memory");
 }
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int x, int y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(src), "r"(x), "r"(y)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
   asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
                "l"(src), "r"(bytes), "r"(bar)
@@ -133,7 +160,7 @@ __device__ __forceinline__ void tc_commit(uint32_t bar) {
 
 // Shared-memory matrix descriptor: start address, leading/stride byte offsets
 // (16-byte units), fixed version field 1 at bit 46, layout type at bits 61-63
-// (0 = no swizzle, 2 = 128-byte swizzle).
+// (2 = 128-byte swizzle).
 __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo, uint32_t layout) {
   uint64_t d = 0;
   d |= (uint64_t)((addr >> 4) & 0x3FFFu);
@@ -172,12 +199,6 @@ __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a_desc, uint64_
   }
 }
 
-// 512 bytes of scales (32 rows x 16 bytes) -> 4 tensor-memory columns,
-// replicated into each 32-lane quarter.
-__device__ __forceinline__ void tc_cp_sf(uint32_t taddr, uint64_t sdesc) {
-  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
-}
-
 #define TC_LD32(taddr, r)                                                                                          \
   asm volatile(                                                                                                    \
       "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18," \
@@ -188,6 +209,18 @@ __device__ __forceinline__ void tc_cp_sf(uint32_t taddr, uint64_t sdesc) {
         "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])     \
       : "r"(taddr))
 
+// 8 consecutive tensor-memory columns of this warp's 32 lanes <- 8 registers
+__device__ __forceinline__ void tc_st8(uint32_t taddr, const uint32_t* v) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(v[0]),
+               "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+               : "memory");
+}
+__device__ __forceinline__ void tc_st4(uint32_t taddr, const uint32_t* v) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1,%2,%3,%4};" ::"r"(taddr), "r"(v[0]), "r"(v[1]),
+               "r"(v[2]), "r"(v[3])
+               : "memory");
+}
+
 struct Params {
   const uint8_t* As;
   const uint8_t* Bs;
@@ -195,31 +228,31 @@ struct Params {
   const float* gb;
   const int32_t* tA;
   const int32_t* tB;
-  void* C;
-  int64_t ldc;
   int M, N, K;
   int32_t* status;
 };
 
 template <int FMT, bool BF16>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
-    k_gemm_fp4(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b, Params p) {
+    k_gemm_fp4(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
+               const __grid_constant__ CUtensorMap tmap_c, Params p) {
   constexpr bool MX = FMT == fp4dev::SF_E8M0;
-  constexpr int SFA_BYTES = MX ? SFA_MAX / 2 : SFA_MAX;  // scales of one K step for 128 rows
-  constexpr int SFB_HALF = SFA_BYTES;                    // per 128 rows of B
+  constexpr int ATOMS = MX ? 2 : 4;         // 512-byte scale atoms per 128 rows per K step
+  constexpr int SFA_BYTES = 512 * ATOMS;    // scales of one K step for 128 rows
+  constexpr int SFB_HALF = SFA_BYTES;       // per 128 rows of B
   constexpr uint32_t IDESC = make_idesc(BM, BN, MX);
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SMEM_BAR);
-  // bars[0..S-1] full, bars[S..2S-1] empty, bars[2S] acc_full, bars[2S+1] acc_empty
-  const uint32_t bar_full = smem_u32(bars);
-  const uint32_t bar_empty = bar_full + 8 * STAGES;
-  const uint32_t bar_acc_full = bar_full + 16 * STAGES;
+  // barriers: full[S], sf_full[S], empty[S], acc_full, acc_empty
+  const uint32_t bar_full = sbase + SMEM_BAR;
+  const uint32_t bar_sf = bar_full + 8 * STAGES;
+  const uint32_t bar_empty = bar_sf + 8 * STAGES;
+  const uint32_t bar_acc_full = bar_empty + 8 * STAGES;
   const uint32_t bar_acc_empty = bar_acc_full + 8;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + SMEM_BAR + 8 * (2 * STAGES + 2));
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + SMEM_BAR + 8 * (2 * STAGES + 2) + 8);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + SMEM_BAR + 8 * (3 * STAGES + 2));
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + SMEM_BAR + 8 * (3 * STAGES + 2) + 8);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int m_tiles = p.M / BM, n_tiles = p.N / BN;
@@ -230,6 +263,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(bar_full + 8 * s, 1);
+      mbar_init(bar_sf + 8 * s, NUM_SF_WARPS);
       mbar_init(bar_empty + 8 * s, 1);
     }
     mbar_init(bar_acc_full, 1);
@@ -297,24 +331,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           tc_fence_after();
         }
         for (int ks = 0; ks < k_steps; ++ks) {
-          if (!wait_bounded(bar_full + 8 * stage, phase, abort_flag, p.status)) {
+          // the scale writers' arrival implies the stage's TMA data has landed
+          if (!wait_bounded(bar_sf + 8 * stage, phase, abort_flag, p.status)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t sfa_smem = sbase + SMEM_SFA + stage * SFA_MAX;
-          const uint32_t sfb_smem = sbase + SMEM_SFB + stage * SFB_MAX;
           const uint32_t sfa_t = tmem_base + TMEM_SFA + 16 * stage;
           const uint32_t sfb_t = tmem_base + TMEM_SFB + 32 * stage;
-          // each 512-byte scale atom covers 128 rows x 4 blocks: one MMA K step
-          // for NVFP4, two for MXFP4
-          constexpr int ATOMS = MX ? 2 : 4;
-#pragma unroll
-          for (int j = 0; j < ATOMS; ++j) {
-            tc_cp_sf(sfa_t + 4 * j, smem_desc(sfa_smem + 512 * j, 0, 128, 0));
-            tc_cp_sf(sfb_t + 8 * j, smem_desc(sfb_smem + 512 * j, 0, 128, 0));
-            tc_cp_sf(sfb_t + 8 * j + 4, smem_desc(sfb_smem + SFB_HALF + 512 * j, 0, 128, 0));
-          }
           const uint32_t a_smem = sbase + SMEM_A + stage * A_BYTES;
           const uint32_t b_smem = sbase + SMEM_B + stage * B_BYTES;
 #pragma unroll
@@ -333,7 +357,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
             tc_mma<MX>(tmem_base, ad, bd, idesc, sfa_col, sfb_col, (ks > 0 || j > 0) ? 1u : 0u);
           }
-          tc_commit(bar_empty + 8 * stage);  // stage free once these MMAs finish
+          tc_commit(bar_empty + 8 * stage);  // stage (smem and its scale columns) free once these finish
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
@@ -345,69 +369,121 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
     }
     __syncwarp();
+  } else if (warp < FIRST_EPI_WARP) {
+    // ------------------------------ scale writers -------------------------
+    // Lane i of the warp serving quarter q writes, for every 512-byte atom
+    // (rows 0..127 x 4 blocks), the atom's 16-byte row i -- the scales of rows
+    // i, i+32, i+64, i+96 -- into 4 consecutive columns of lane 32q+i.
+    const int quarter = warp & 3;
+    int stage = 0;
+    uint32_t phase = 0;
+    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+      bool ok = true;
+      for (int ks = 0; ks < k_steps; ++ks) {
+        // the new phase of full[s] comes after the producer saw empty[s], so the
+        // MMAs that read this stage's scale columns last time have finished
+        if (!wait_bounded(bar_full + 8 * stage, phase, abort_flag, p.status)) {
+          ok = false;
+          break;
+        }
+        const uint8_t* sfa = smem + SMEM_SFA + stage * SFA_MAX + 16 * lane;
+        const uint8_t* sfb = smem + SMEM_SFB + stage * SFB_MAX + 16 * lane;
+        const uint32_t lane_base = tmem_base + ((uint32_t)(32 * quarter) << 16);
+        uint32_t va[4 * ATOMS], vb[8 * ATOMS];
+#pragma unroll
+        for (int j = 0; j < ATOMS; ++j) {
+          const uint4 a = *reinterpret_cast<const uint4*>(sfa + 512 * j);
+          const uint4 b0 = *reinterpret_cast<const uint4*>(sfb + 512 * j);
+          const uint4 b1 = *reinterpret_cast<const uint4*>(sfb + SFB_HALF + 512 * j);
+          va[4 * j + 0] = a.x; va[4 * j + 1] = a.y; va[4 * j + 2] = a.z; va[4 * j + 3] = a.w;
+          vb[8 * j + 0] = b0.x; vb[8 * j + 1] = b0.y; vb[8 * j + 2] = b0.z; vb[8 * j + 3] = b0.w;
+          vb[8 * j + 4] = b1.x; vb[8 * j + 5] = b1.y; vb[8 * j + 6] = b1.z; vb[8 * j + 7] = b1.w;
+        }
+#pragma unroll
+        for (int j = 0; j < ATOMS; ++j) {
+          tc_st4(lane_base + TMEM_SFA + 16 * stage + 4 * j, va + 4 * j);
+          tc_st8(lane_base + TMEM_SFB + 32 * stage + 8 * j, vb + 8 * j);
+        }
+        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_sf + 8 * stage);
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (!ok) break;
+    }
   } else {
     // ------------------------------ epilogue ------------------------------
-    const int ew = warp - 2;          // 0..7
-    const int quarter = warp & 3;     // tensor-memory lanes this warp may access
-    const int half = ew >> 2;         // columns 0..127 or 128..255
+    const int ew = warp - FIRST_EPI_WARP;  // 0..15
+    const int quarter = warp & 3;          // tensor-memory lanes this warp may access
+    const int cblk = ew >> 2;              // 64-column block of the accumulator
     float alpha = 1.0f;
     if constexpr (!MX) {
-      const float sa = fp4dev::global_encode_scale<FMT == fp4dev::SF_UE5M3 ? fp4dev::SF_E4M3 : FMT>(__ldg(p.ga), nullptr);
-      const float sb = fp4dev::global_encode_scale<FMT == fp4dev::SF_UE5M3 ? fp4dev::SF_E4M3 : FMT>(__ldg(p.gb), nullptr);
+      constexpr int SFMT = FMT == fp4dev::SF_UE5M3 ? fp4dev::SF_E4M3 : FMT;
+      const float sa = fp4dev::global_encode_scale<SFMT>(__ldg(p.ga), nullptr);
+      const float sb = fp4dev::global_encode_scale<SFMT>(__ldg(p.gb), nullptr);
       alpha = __fdiv_rn(1.0f, __fmul_rn(sa, sb));
       if (FMT == fp4dev::SF_UE5M3) alpha = ldexpf(alpha, __ldg(p.tA) + __ldg(p.tB));
     }
+    uint8_t* stage_buf = smem + SMEM_OUT + ew * STAGE_BYTES;
+    const uint32_t stage_addr = smem_u32(stage_buf);
     uint32_t acc_phase = 0;
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
       const int mt = tile % m_tiles, nt = tile / m_tiles;
       if (!wait_bounded(bar_acc_full, acc_phase, abort_flag, p.status)) break;
       acc_phase ^= 1u;
       tc_fence_after();
-      uint32_t r[4][32];
-      const uint32_t t0 = tmem_base + ((uint32_t)(32 * quarter) << 16) + 128 * half;
-      TC_LD32(t0 + 0, r[0]);
+      uint32_t r[2][32];
+      const uint32_t t0 = tmem_base + ((uint32_t)(32 * quarter) << 16) + EPI_COLS * cblk;
+      TC_LD32(t0, r[0]);
       TC_LD32(t0 + 32, r[1]);
-      TC_LD32(t0 + 64, r[2]);
-      TC_LD32(t0 + 96, r[3]);
       asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_acc_empty);
-      const int64_t row = (int64_t)mt * BM + 32 * quarter + lane;
-      const int64_t col0 = (int64_t)nt * BN + 128 * half;
-      if constexpr (BF16) {
-        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.C) + row * p.ldc + col0;
+      const int row0 = mt * BM + 32 * quarter;
+      const int col0 = nt * BN + EPI_COLS * cblk;
+      // 64-byte rows of the staged block: bf16 -> 32 columns, float32 -> 16
+      constexpr int BLK_COLS = BF16 ? 32 : 16;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
+      for (int b = 0; b < EPI_COLS / BLK_COLS; ++b) {
+        uint32_t w[16];
+        if constexpr (BF16) {
 #pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            uint32_t w[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const float x0 = __fmul_rn(__uint_as_float(r[c][8 * v + 2 * i]), alpha);
-              const float x1 = __fmul_rn(__uint_as_float(r[c][8 * v + 2 * i + 1]), alpha);
-              const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
-              w[i] = *reinterpret_cast<const uint32_t*>(&h);
-            }
-            *reinterpret_cast<uint4*>(out + 32 * c + 8 * v) = make_uint4(w[0], w[1], w[2], w[3]);
+          for (int i = 0; i < 16; ++i) {
+            const float x0 = __fmul_rn(__uint_as_float(r[b][2 * i]), alpha);
+            const float x1 = __fmul_rn(__uint_as_float(r[b][2 * i + 1]), alpha);
+            const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
+            w[i] = *reinterpret_cast<const uint32_t*>(&h);
           }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) w[i] = __float_as_uint(__fmul_rn(__uint_as_float(r[b >> 1][16 * (b & 1) + i]), alpha));
         }
-      } else {
-        float* out = static_cast<float*>(p.C) + row * p.ldc + col0;
+        // the previous block's store must have read the staging buffer
+        if (lane == 0) bulk_wait_read0();
+        __syncwarp();
+        // row `lane`, 16-byte chunk v at chunk v ^ ((lane >> 1) & 3): the
+        // 64-byte swizzle the output tensor map declares (bank-conflict free)
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-#pragma unroll
-          for (int v = 0; v < 8; ++v) {
-            float4 f;
-            f.x = __fmul_rn(__uint_as_float(r[c][4 * v + 0]), alpha);
-            f.y = __fmul_rn(__uint_as_float(r[c][4 * v + 1]), alpha);
-            f.z = __fmul_rn(__uint_as_float(r[c][4 * v + 2]), alpha);
-            f.w = __fmul_rn(__uint_as_float(r[c][4 * v + 3]), alpha);
-            *reinterpret_cast<float4*>(out + 32 * c + 4 * v) = f;
-          }
+        for (int v = 0; v < 4; ++v) {
+          const int pc = v ^ ((lane >> 1) & 3);
+          *reinterpret_cast<uint4*>(stage_buf + lane * 64 + pc * 16) =
+              make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_2d(&tmap_c, stage_addr, col0 + BLK_COLS * b, row0);
+          bulk_commit();
         }
       }
     }
+    if (lane == 0) bulk_wait0();
+    __syncwarp();
   }
 
   // ------------------------------ teardown --------------------------------
@@ -450,6 +526,21 @@ bool make_code_map(CUtensorMap* map, const void* base, int64_t rows, int64_t row
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Output C [M, N] (leading dimension ldc elements): 32-row x 64-byte boxes
+// with the 64-byte swizzle the epilogue's staging writes use.
+bool make_out_map(CUtensorMap* map, void* base, int64_t M, int64_t N, int64_t ldc, bool bf16) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t esz = bf16 ? 2 : 4;
+  cuuint64_t dims[2] = {(cuuint64_t)N, (cuuint64_t)M};
+  cuuint64_t strides[1] = {(cuuint64_t)(ldc * esz)};
+  cuuint32_t box[2] = {(cuuint32_t)(64 / esz), 32u};
+  cuuint32_t estr[2] = {1u, 1u};
+  return fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, strides,
+            box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 int sm_count() {
   static int n = 0;
   if (n == 0) {
@@ -470,8 +561,9 @@ cudaError_t launch_t(const fp4lib::GemmArgs& a, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  CUtensorMap ma, mb;
-  if (!make_code_map(&ma, a.Aq, a.M, a.K / 2, BM) || !make_code_map(&mb, a.Bq, a.N, a.K / 2, BN))
+  CUtensorMap ma, mb, mc;
+  if (!make_code_map(&ma, a.Aq, a.M, a.K / 2, BM) || !make_code_map(&mb, a.Bq, a.N, a.K / 2, BN) ||
+      !make_out_map(&mc, a.C, a.M, a.N, a.ldc, BF16))
     return cudaErrorInvalidValue;
   Params p;
   p.As = a.As;
@@ -480,15 +572,13 @@ cudaError_t launch_t(const fp4lib::GemmArgs& a, cudaStream_t st) {
   p.gb = a.gb;
   p.tA = a.tA;
   p.tB = a.tB;
-  p.C = a.C;
-  p.ldc = a.ldc;
   p.M = (int)a.M;
   p.N = (int)a.N;
   p.K = (int)a.K;
   p.status = a.status;
   const int tiles = (int)((a.M / BM) * (a.N / BN));
   const int grid = tiles < sm_count() ? tiles : sm_count();
-  k_gemm_fp4<FMT, BF16><<<grid, NUM_THREADS, SMEM_LAUNCH, st>>>(ma, mb, p);
+  k_gemm_fp4<FMT, BF16><<<grid, NUM_THREADS, SMEM_LAUNCH, st>>>(ma, mb, mc, p);
   return cudaGetLastError();
 }
 
@@ -497,7 +587,7 @@ cudaError_t launch_t(const fp4lib::GemmArgs& a, cudaStream_t st) {
 namespace fp4lib {
 
 cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t st) {
-  if (a.N % BN != 0) return cudaErrorNotSupported;  // 128-wide N tail not built yet
+  if (a.N % BN != 0) return cudaErrorNotSupported;
   switch (a.fmt) {
     case FP4_SF_E4M3: return a.bf16_out ? launch_t<fp4dev::SF_E4M3, true>(a, st) : launch_t<fp4dev::SF_E4M3, false>(a, st);
     case FP4_SF_UE5M3: return a.bf16_out ? launch_t<fp4dev::SF_UE5M3, true>(a, st) : launch_t<fp4dev::SF_UE5M3, false>(a, st);
