@@ -18,7 +18,7 @@
 // 22 warps):
 //   warp 0       TMA producer: A/B code tiles (128-byte swizzle) by
 //                cp.async.bulk.tensor, scale atoms by cp.async.bulk, into a
-//                3-stage shared-memory ring guarded by mbarriers;
+//                4-stage shared-memory ring guarded by mbarriers;
 //   warp 1       allocates tensor memory; one lane issues the 4 tcgen05.mma of
 //                each 256-wide K step once its scales sit in tensor memory, and
 //                tcgen05.commit frees the stage (and, after the last K step,
@@ -31,8 +31,9 @@
 //   warps 6-21   epilogue: each warp drains 32 rows x 64 columns of the
 //                float32 accumulator with tcgen05.ld, releases the tensor
 //                memory at once (the next tile's MMAs overlap the rest), scales,
-//                converts and stages 32 x 64-byte blocks in 64-byte-swizzled
-//                shared memory, and writes them with TMA bulk-tensor stores.
+//                converts and stages 32-row x 16-byte blocks in shared memory
+//                (512 bytes per warp, which leaves room for a 4-stage ring), and
+//                writes them with TMA bulk-tensor stores.
 // Every mbarrier wait is bounded: on expiry the CTA records FP4_ERR_TIMEOUT in
 // the status word and winds down instead of spinning.
 #include <cstdint>
@@ -49,7 +50,6 @@ namespace {
 constexpr int BM = 128;
 constexpr int BN = 256;
 constexpr int BK = 256;  // FP4 elements per K step = 128 bytes per row
-constexpr int STAGES = 3;
 constexpr int A_BYTES = BM * BK / 2;   // 16 KB
 constexpr int B_BYTES = BN * BK / 2;   // 32 KB
 constexpr int SFA_MAX = BM * BK / 16;  // 2 KB (NVFP4); MXFP4 uses half
@@ -61,25 +61,35 @@ constexpr int FIRST_SF_WARP = 2;
 constexpr int FIRST_EPI_WARP = FIRST_SF_WARP + NUM_SF_WARPS;
 constexpr int NUM_THREADS = 32 * (FIRST_EPI_WARP + NUM_EPI_WARPS);
 constexpr int EPI_COLS = BN / (NUM_EPI_WARPS / 4);  // 64 accumulator columns per epilogue warp
-constexpr int STAGE_BYTES = 32 * 64;                 // one 32-row x 64-byte output block
 
-constexpr int SMEM_A = 0;
-constexpr int SMEM_B = SMEM_A + STAGES * A_BYTES;
-constexpr int SMEM_SFA = SMEM_B + STAGES * B_BYTES;
-constexpr int SMEM_SFB = SMEM_SFA + STAGES * SFA_MAX;
-constexpr int SMEM_OUT = SMEM_SFB + STAGES * SFB_MAX;  // 1024-aligned
-constexpr int SMEM_BAR = SMEM_OUT + NUM_EPI_WARPS * STAGE_BYTES;
-constexpr int SMEM_TOTAL = SMEM_BAR + 256;
-constexpr int SMEM_LAUNCH = SMEM_TOTAL + 1024;  // room to align the base to 1024
-static_assert(SMEM_OUT % 1024 == 0, "output staging must stay 1024-byte aligned");
-static_assert(SMEM_LAUNCH <= 232448, "shared memory over the sm_103a per-CTA limit");
-
-// tensor memory columns: accumulator 0..255, then per stage 16 columns of A
-// scales (4 K64 steps x 4) and 32 of B scales (4 K64 steps x 2 halves x 4)
-constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t TMEM_SFA = 256;
-constexpr uint32_t TMEM_SFB = TMEM_SFA + 16 * STAGES;
-static_assert(TMEM_SFB + 32 * STAGES <= TMEM_COLS, "tensor memory budget");
+// Shared-memory plan of one configuration: S stages of the code/scale ring
+// and, per epilogue warp, one 32-row output block with OB-byte rows (OB = 64:
+// 64-byte-swizzled blocks; OB = 16: plain 512-byte blocks).  Short K (an
+// output-heavy GEMM) wants wide blocks; long K wants the deeper ring.
+template <int S, int OB>
+struct Plan {
+  static constexpr int STAGES = S;
+  static constexpr int OUT_ROW_BYTES = OB;
+  static constexpr int STAGE_BYTES = 32 * OB;
+  static constexpr int SMEM_A = 0;
+  static constexpr int SMEM_B = SMEM_A + S * A_BYTES;
+  static constexpr int SMEM_SFA = SMEM_B + S * B_BYTES;
+  static constexpr int SMEM_SFB = SMEM_SFA + S * SFA_MAX;
+  static constexpr int SMEM_OUT = SMEM_SFB + S * SFB_MAX;
+  static constexpr int SMEM_BAR = SMEM_OUT + NUM_EPI_WARPS * STAGE_BYTES;
+  static constexpr int SMEM_TOTAL = SMEM_BAR + 256;
+  static constexpr int SMEM_LAUNCH = SMEM_TOTAL + 1024;  // room to align the base to 1024
+  // tensor memory columns: accumulator 0..255, then per stage 16 columns of
+  // A scales (4 K64 steps x 4) and 32 of B scales (4 K64 steps x 2 halves x 4)
+  static constexpr uint32_t TMEM_COLS = 512;
+  static constexpr uint32_t TMEM_SFA = 256;
+  static constexpr uint32_t TMEM_SFB = TMEM_SFA + 16 * S;
+  static_assert(SMEM_OUT % 1024 == 0, "output staging must stay 1024-byte aligned");
+  static_assert(SMEM_LAUNCH <= 232448, "shared memory over the sm_103a per-CTA limit");
+  static_assert(TMEM_SFB + 32 * S <= TMEM_COLS, "tensor memory budget");
+};
+using PlanShortK = Plan<3, 64>;
+using PlanLongK = Plan<4, 16>;
 
 constexpr long long WAIT_LIMIT_CYCLES = 4000000000LL;  // ~2 s at 2 GHz
 
@@ -134,6 +144,33 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
       : "memory");
 }
+// The same box into every CTA of the cluster in `mask` (same shared offsets),
+// each CTA's mbarrier at `bar` receiving the bytes.
+__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y,
+                                               uint16_t mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster [%0], "
+      "[%1, {%3, %4}], [%2], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "h"(mask)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_load_mc(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar,
+                                             uint16_t mask) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster [%0], [%1], %2, [%3], "
+      "%4;" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar), "h"(mask)
+      : "memory");
+}
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int x, int y) {
   asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
                    reinterpret_cast<uint64_t>(map)),
@@ -155,6 +192,14 @@ __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::
 
 __device__ __forceinline__ void tc_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+               : "memory");
+}
+// Arrive on the mbarrier at `bar` in every CTA of the cluster in `mask` once
+// this thread's prior tcgen05 operations have completed.
+__device__ __forceinline__ void tc_commit_mc(uint32_t bar, uint16_t mask) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+                   bar),
+               "h"(mask)
                : "memory");
 }
 
@@ -209,16 +254,29 @@ __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a_desc, uint64_
         "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])     \
       : "r"(taddr))
 
-// 8 consecutive tensor-memory columns of this warp's 32 lanes <- 8 registers
+// N consecutive tensor-memory columns of this warp's 32 lanes <- N registers
 __device__ __forceinline__ void tc_st8(uint32_t taddr, const uint32_t* v) {
   asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(v[0]),
                "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
                : "memory");
 }
-__device__ __forceinline__ void tc_st4(uint32_t taddr, const uint32_t* v) {
-  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1,%2,%3,%4};" ::"r"(taddr), "r"(v[0]), "r"(v[1]),
-               "r"(v[2]), "r"(v[3])
-               : "memory");
+__device__ __forceinline__ void tc_st16(uint32_t taddr, const uint32_t* v) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+          taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+      "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+      : "memory");
+}
+__device__ __forceinline__ void tc_st32(uint32_t taddr, const uint32_t* v) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,"
+      "%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+      "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]),
+      "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]),
+      "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+      : "memory");
 }
 
 struct Params {
@@ -232,7 +290,11 @@ struct Params {
   int32_t* status;
 };
 
-template <int FMT, bool BF16>
+// CM CTAs of a cluster take CM consecutive M tiles of the same N tile: each
+// loads its own A tile and 1/CM of the shared B tile (and of its scales),
+// multicast to all of them, so the L2 -> SM traffic per K step drops from
+// A + B to A + B/CM.
+template <int FMT, bool BF16, int CM, class PL>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     k_gemm_fp4(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                const __grid_constant__ CUtensorMap tmap_c, Params p) {
@@ -241,30 +303,42 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   constexpr int SFA_BYTES = 512 * ATOMS;    // scales of one K step for 128 rows
   constexpr int SFB_HALF = SFA_BYTES;       // per 128 rows of B
   constexpr uint32_t IDESC = make_idesc(BM, BN, MX);
+  constexpr int STAGES = PL::STAGES;
+  constexpr int SMEM_A = PL::SMEM_A, SMEM_B = PL::SMEM_B, SMEM_SFA = PL::SMEM_SFA, SMEM_SFB = PL::SMEM_SFB;
+  constexpr int SMEM_OUT = PL::SMEM_OUT, SMEM_BAR = PL::SMEM_BAR, STAGE_BYTES = PL::STAGE_BYTES;
+  constexpr uint32_t TMEM_COLS = PL::TMEM_COLS, TMEM_SFA = PL::TMEM_SFA, TMEM_SFB = PL::TMEM_SFB;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
-  // barriers: full[S], sf_full[S], empty[S], acc_full, acc_empty
+  // barriers: full[S] (codes landed), sfdata[S] (scales landed), sf[S]
+  // (scales written to tensor memory), empty[S], acc_full, acc_empty
   const uint32_t bar_full = sbase + SMEM_BAR;
-  const uint32_t bar_sf = bar_full + 8 * STAGES;
+  const uint32_t bar_sfdata = bar_full + 8 * STAGES;
+  const uint32_t bar_sf = bar_sfdata + 8 * STAGES;
   const uint32_t bar_empty = bar_sf + 8 * STAGES;
   const uint32_t bar_acc_full = bar_empty + 8 * STAGES;
   const uint32_t bar_acc_empty = bar_acc_full + 8;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + SMEM_BAR + 8 * (3 * STAGES + 2));
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + SMEM_BAR + 8 * (3 * STAGES + 2) + 8);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + SMEM_BAR + 8 * (4 * STAGES + 2));
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + SMEM_BAR + 8 * (4 * STAGES + 2) + 8);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int m_tiles = p.M / BM, n_tiles = p.N / BN;
-  const int num_tiles = m_tiles * n_tiles;
+  // work unit = CM consecutive M tiles of one N tile, one per cluster CTA
+  const int m_groups = m_tiles / CM;
+  const int num_units = m_groups * n_tiles;
+  const int crank = CM > 1 ? (int)cluster_rank() : 0;
+  const int cluster_id = blockIdx.x / CM, num_clusters = gridDim.x / CM;
+  constexpr uint16_t MC_MASK = (uint16_t)((1u << CM) - 1u);
   const int k_steps = p.K / BK;
   const int64_t sf_row_stride = (int64_t)(p.K / (MX ? 32 : 16)) / 4 * 512;  // bytes per 128-row slab
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(bar_full + 8 * s, 1);
+      mbar_init(bar_sfdata + 8 * s, 1);
       mbar_init(bar_sf + 8 * s, NUM_SF_WARPS);
-      mbar_init(bar_empty + 8 * s, 1);
+      mbar_init(bar_empty + 8 * s, CM);  // one MMA commit from each cluster CTA
     }
     mbar_init(bar_acc_full, 1);
     mbar_init(bar_acc_empty, NUM_EPI_WARPS);
@@ -280,6 +354,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   }
   tc_fence_before();
   __syncthreads();
+  if constexpr (CM > 1) cluster_sync_all();  // peers' barriers exist before any multicast
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
@@ -291,24 +366,42 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
-        const int mt = tile % m_tiles, nt = tile / m_tiles;
+      for (int u = cluster_id; u < num_units && ok; u += num_clusters) {
+        const int mt = (u % m_groups) * CM + crank, nt = u / m_groups;
         for (int ks = 0; ks < k_steps; ++ks) {
+          // own stage free in every cluster CTA (the B slice lands in all of them)
           if (!wait_bounded(bar_empty + 8 * stage, phase ^ 1u, abort_flag, p.status)) {
             ok = false;
             break;
           }
+          // scales first, on their own barrier, so the scale writers can move
+          // them into tensor memory while the code tiles are still in flight
+          const uint32_t sb = bar_sfdata + 8 * stage;
           const uint32_t fb = bar_full + 8 * stage;
-          mbar_expect_tx(fb, A_BYTES + B_BYTES + SFA_BYTES + 2 * SFB_HALF);
-          tma_load_2d(sbase + SMEM_A + stage * A_BYTES, &tmap_a, fb, ks * (BK / 2), mt * BM);
-          tma_load_2d(sbase + SMEM_B + stage * B_BYTES, &tmap_b, fb, ks * (BK / 2), nt * BN);
+          mbar_expect_tx(sb, SFA_BYTES + 2 * SFB_HALF);
           // scales of this K step: SFA_BYTES contiguous bytes per 128-row slab
           bulk_load(sbase + SMEM_SFA + stage * SFA_MAX, p.As + mt * sf_row_stride + (int64_t)ks * SFA_BYTES,
-                    SFA_BYTES, fb);
-          bulk_load(sbase + SMEM_SFB + stage * SFB_MAX, p.Bs + (2 * nt) * sf_row_stride + (int64_t)ks * SFB_HALF,
-                    SFB_HALF, fb);
-          bulk_load(sbase + SMEM_SFB + stage * SFB_MAX + SFB_HALF,
-                    p.Bs + (2 * nt + 1) * sf_row_stride + (int64_t)ks * SFB_HALF, SFB_HALF, fb);
+                    SFA_BYTES, sb);
+          mbar_expect_tx(fb, A_BYTES + B_BYTES);
+          tma_load_2d(sbase + SMEM_A + stage * A_BYTES, &tmap_a, fb, ks * (BK / 2), mt * BM);
+          if constexpr (CM == 1) {
+            bulk_load(sbase + SMEM_SFB + stage * SFB_MAX, p.Bs + (2 * nt) * sf_row_stride + (int64_t)ks * SFB_HALF,
+                      SFB_HALF, sb);
+            bulk_load(sbase + SMEM_SFB + stage * SFB_MAX + SFB_HALF,
+                      p.Bs + (2 * nt + 1) * sf_row_stride + (int64_t)ks * SFB_HALF, SFB_HALF, sb);
+            tma_load_2d(sbase + SMEM_B + stage * B_BYTES, &tmap_b, fb, ks * (BK / 2), nt * BN);
+          } else {
+            // rows [crank*BN/CM, +BN/CM) of the B tile: 128-byte rows, so the
+            // slice starts crank*BN/CM*128 bytes into the swizzled stage
+            constexpr int ROWS = BN / CM;
+            tma_load_2d_mc(sbase + SMEM_B + stage * B_BYTES + crank * ROWS * 128, &tmap_b, fb, ks * (BK / 2),
+                           nt * BN + crank * ROWS, MC_MASK);
+            // 1/CM of the two 128-row scale halves
+            constexpr int PIECE = 2 * SFB_HALF / CM;
+            const int half = (crank * PIECE) / SFB_HALF, off = (crank * PIECE) % SFB_HALF;
+            bulk_load_mc(sbase + SMEM_SFB + stage * SFB_MAX + half * SFB_HALF + off,
+                         p.Bs + (2 * nt + half) * sf_row_stride + (int64_t)ks * SFB_HALF + off, PIECE, sb, MC_MASK);
+          }
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
@@ -325,14 +418,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       uint32_t acc_phase = 0;
       bool ok = true;
       int iter = 0;
-      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x, ++iter) {
+      for (int u = cluster_id; u < num_units && ok; u += num_clusters, ++iter) {
         if (iter > 0) {
           if (!wait_bounded(bar_acc_empty, acc_phase ^ 1u, abort_flag, p.status)) break;
           tc_fence_after();
         }
         for (int ks = 0; ks < k_steps; ++ks) {
-          // the scale writers' arrival implies the stage's TMA data has landed
-          if (!wait_bounded(bar_sf + 8 * stage, phase, abort_flag, p.status)) {
+          // scales in tensor memory, then the code tiles in shared memory
+          if (!wait_bounded(bar_sf + 8 * stage, phase, abort_flag, p.status) ||
+              !wait_bounded(bar_full + 8 * stage, phase, abort_flag, p.status)) {
             ok = false;
             break;
           }
@@ -357,7 +451,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
             tc_mma<MX>(tmem_base, ad, bd, idesc, sfa_col, sfb_col, (ks > 0 || j > 0) ? 1u : 0u);
           }
-          tc_commit(bar_empty + 8 * stage);  // stage (smem and its scale columns) free once these finish
+          // stage (smem and its scale columns) free once these finish, in every cluster CTA
+          if constexpr (CM == 1) tc_commit(bar_empty + 8 * stage);
+          else tc_commit_mc(bar_empty + 8 * stage, MC_MASK);
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
@@ -377,12 +473,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int quarter = warp & 3;
     int stage = 0;
     uint32_t phase = 0;
-    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+    for (int u = cluster_id; u < num_units; u += num_clusters) {
       bool ok = true;
       for (int ks = 0; ks < k_steps; ++ks) {
-        // the new phase of full[s] comes after the producer saw empty[s], so the
-        // MMAs that read this stage's scale columns last time have finished
-        if (!wait_bounded(bar_full + 8 * stage, phase, abort_flag, p.status)) {
+        // the new phase of sfdata[s] comes after the producer saw empty[s], so
+        // the MMAs that read this stage's scale columns last time have finished
+        if (!wait_bounded(bar_sfdata + 8 * stage, phase, abort_flag, p.status)) {
           ok = false;
           break;
         }
@@ -399,10 +495,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           vb[8 * j + 0] = b0.x; vb[8 * j + 1] = b0.y; vb[8 * j + 2] = b0.z; vb[8 * j + 3] = b0.w;
           vb[8 * j + 4] = b1.x; vb[8 * j + 5] = b1.y; vb[8 * j + 6] = b1.z; vb[8 * j + 7] = b1.w;
         }
-#pragma unroll
-        for (int j = 0; j < ATOMS; ++j) {
-          tc_st4(lane_base + TMEM_SFA + 16 * stage + 4 * j, va + 4 * j);
-          tc_st8(lane_base + TMEM_SFB + 32 * stage + 8 * j, vb + 8 * j);
+        if constexpr (ATOMS == 4) {
+          tc_st16(lane_base + TMEM_SFA + 16 * stage, va);
+          tc_st32(lane_base + TMEM_SFB + 32 * stage, vb);
+        } else {
+          tc_st8(lane_base + TMEM_SFA + 16 * stage, va);
+          tc_st16(lane_base + TMEM_SFB + 32 * stage, vb);
         }
         asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
         tc_fence_before();
@@ -431,8 +529,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint8_t* stage_buf = smem + SMEM_OUT + ew * STAGE_BYTES;
     const uint32_t stage_addr = smem_u32(stage_buf);
     uint32_t acc_phase = 0;
-    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
-      const int mt = tile % m_tiles, nt = tile / m_tiles;
+    for (int u = cluster_id; u < num_units; u += num_clusters) {
+      const int mt = (u % m_groups) * CM + crank, nt = u / m_groups;
       if (!wait_bounded(bar_acc_full, acc_phase, abort_flag, p.status)) break;
       acc_phase ^= 1u;
       tc_fence_after();
@@ -446,32 +544,37 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (lane == 0) mbar_arrive(bar_acc_empty);
       const int row0 = mt * BM + 32 * quarter;
       const int col0 = nt * BN + EPI_COLS * cblk;
-      // 64-byte rows of the staged block: bf16 -> 32 columns, float32 -> 16
-      constexpr int BLK_COLS = BF16 ? 32 : 16;
+      constexpr int OB = PL::OUT_ROW_BYTES;
+      constexpr int BLK_COLS = OB / (BF16 ? 2 : 4);  // columns per staged row
+      constexpr int VECS = OB / 16;                  // 16-byte vectors per staged row
 #pragma unroll
       for (int b = 0; b < EPI_COLS / BLK_COLS; ++b) {
-        uint32_t w[16];
+        uint32_t w[4 * VECS];
         if constexpr (BF16) {
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const float x0 = __fmul_rn(__uint_as_float(r[b][2 * i]), alpha);
-            const float x1 = __fmul_rn(__uint_as_float(r[b][2 * i + 1]), alpha);
+          for (int i = 0; i < 2 * VECS * 2; ++i) {
+            const int c = BLK_COLS * b + 2 * i;
+            const float x0 = __fmul_rn(__uint_as_float(r[c >> 5][c & 31]), alpha);
+            const float x1 = __fmul_rn(__uint_as_float(r[c >> 5][(c & 31) + 1]), alpha);
             const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
             w[i] = *reinterpret_cast<const uint32_t*>(&h);
           }
         } else {
 #pragma unroll
-          for (int i = 0; i < 16; ++i) w[i] = __float_as_uint(__fmul_rn(__uint_as_float(r[b >> 1][16 * (b & 1) + i]), alpha));
+          for (int i = 0; i < 4 * VECS; ++i) {
+            const int c = BLK_COLS * b + i;
+            w[i] = __float_as_uint(__fmul_rn(__uint_as_float(r[c >> 5][c & 31]), alpha));
+          }
         }
         // the previous block's store must have read the staging buffer
         if (lane == 0) bulk_wait_read0();
         __syncwarp();
-        // row `lane`, 16-byte chunk v at chunk v ^ ((lane >> 1) & 3): the
-        // 64-byte swizzle the output tensor map declares (bank-conflict free)
+        // row `lane`; with 64-byte rows, 16-byte chunk v goes to chunk
+        // v ^ ((lane >> 1) & 3), the 64-byte swizzle the output map declares
 #pragma unroll
-        for (int v = 0; v < 4; ++v) {
-          const int pc = v ^ ((lane >> 1) & 3);
-          *reinterpret_cast<uint4*>(stage_buf + lane * 64 + pc * 16) =
+        for (int v = 0; v < VECS; ++v) {
+          const int pc = VECS == 4 ? (v ^ ((lane >> 1) & 3)) : v;
+          *reinterpret_cast<uint4*>(stage_buf + lane * OB + pc * 16) =
               make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
         }
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -489,6 +592,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   // ------------------------------ teardown --------------------------------
   tc_fence_before();
   __syncthreads();
+  // no CTA leaves while a peer may still multicast into it or arrive on it
+  if constexpr (CM > 1) cluster_sync_all();
   if (warp == 1) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS)
@@ -526,18 +631,19 @@ bool make_code_map(CUtensorMap* map, const void* base, int64_t rows, int64_t row
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Output C [M, N] (leading dimension ldc elements): 32-row x 64-byte boxes
-// with the 64-byte swizzle the epilogue's staging writes use.
-bool make_out_map(CUtensorMap* map, void* base, int64_t M, int64_t N, int64_t ldc, bool bf16) {
+// Output C [M, N] (leading dimension ldc elements): 32-row x `row_bytes`
+// boxes, 64-byte swizzle for 64-byte rows, none for 16-byte rows.
+bool make_out_map(CUtensorMap* map, void* base, int64_t M, int64_t N, int64_t ldc, bool bf16, int row_bytes) {
   auto fn = encode_fn();
   if (fn == nullptr) return false;
   const cuuint64_t esz = bf16 ? 2 : 4;
   cuuint64_t dims[2] = {(cuuint64_t)N, (cuuint64_t)M};
   cuuint64_t strides[1] = {(cuuint64_t)(ldc * esz)};
-  cuuint32_t box[2] = {(cuuint32_t)(64 / esz), 32u};
+  cuuint32_t box[2] = {(cuuint32_t)(row_bytes / esz), 32u};
   cuuint32_t estr[2] = {1u, 1u};
   return fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, strides,
-            box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+            box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            row_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -552,18 +658,39 @@ int sm_count() {
   return n;
 }
 
-template <int FMT, bool BF16>
+template <int FMT, bool BF16, int CM, class PL>
 cudaError_t launch_t(const fp4lib::GemmArgs& a, cudaStream_t st) {
+  auto kern = k_gemm_fp4<FMT, BF16, CM, PL>;
+  constexpr int SMEM_LAUNCH = PL::SMEM_LAUNCH;
   static bool attr_set = false;
+  static int max_clusters = 0;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = CM;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = SMEM_LAUNCH;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(k_gemm_fp4<FMT, BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         SMEM_LAUNCH);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_LAUNCH);
     if (e != cudaSuccess) return e;
+    cfg.gridDim = dim3(sm_count(), 1, 1);
+    if (CM > 1) {
+      e = cudaOccupancyMaxActiveClusters(&max_clusters, kern, &cfg);
+      if (e != cudaSuccess) return e;
+    } else {
+      max_clusters = sm_count();
+    }
+    if (max_clusters <= 0) return cudaErrorInvalidConfiguration;
     attr_set = true;
   }
   CUtensorMap ma, mb, mc;
-  if (!make_code_map(&ma, a.Aq, a.M, a.K / 2, BM) || !make_code_map(&mb, a.Bq, a.N, a.K / 2, BN) ||
-      !make_out_map(&mc, a.C, a.M, a.N, a.ldc, BF16))
+  if (!make_code_map(&ma, a.Aq, a.M, a.K / 2, BM) || !make_code_map(&mb, a.Bq, a.N, a.K / 2, BN / CM) ||
+      !make_out_map(&mc, a.C, a.M, a.N, a.ldc, BF16, PL::OUT_ROW_BYTES))
     return cudaErrorInvalidValue;
   Params p;
   p.As = a.As;
@@ -576,10 +703,25 @@ cudaError_t launch_t(const fp4lib::GemmArgs& a, cudaStream_t st) {
   p.N = (int)a.N;
   p.K = (int)a.K;
   p.status = a.status;
-  const int tiles = (int)((a.M / BM) * (a.N / BN));
-  const int grid = tiles < sm_count() ? tiles : sm_count();
-  k_gemm_fp4<FMT, BF16><<<grid, NUM_THREADS, SMEM_LAUNCH, st>>>(ma, mb, mc, p);
-  return cudaGetLastError();
+  const int units = (int)((a.M / BM / CM) * (a.N / BN));
+  const int clusters = units < max_clusters ? units : max_clusters;
+  cfg.gridDim = dim3((unsigned)(clusters * CM), 1, 1);
+  return cudaLaunchKernelEx(&cfg, kern, ma, mb, mc, p);
+}
+
+// Cluster size along M.  Multicasting the B tile halves or quarters the
+// L2 -> SM bytes per K step, but on the 7B shapes it measured no faster
+// (2 CTAs) or slower (4 CTAs: fewer co-resident clusters) than independent
+// CTAs, so independent CTAs are the default.
+constexpr int GEMM_CLUSTER_M = 1;
+
+template <int FMT, bool BF16>
+cudaError_t launch_cm(const fp4lib::GemmArgs& a, cudaStream_t st) {
+  const int64_t m_tiles = a.M / BM;
+  const bool long_k = a.K >= 8192;
+  if (GEMM_CLUSTER_M == 2 && m_tiles % 2 == 0)
+    return long_k ? launch_t<FMT, BF16, 2, PlanLongK>(a, st) : launch_t<FMT, BF16, 2, PlanShortK>(a, st);
+  return long_k ? launch_t<FMT, BF16, 1, PlanLongK>(a, st) : launch_t<FMT, BF16, 1, PlanShortK>(a, st);
 }
 
 }  // namespace
@@ -589,9 +731,9 @@ namespace fp4lib {
 cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t st) {
   if (a.N % BN != 0) return cudaErrorNotSupported;
   switch (a.fmt) {
-    case FP4_SF_E4M3: return a.bf16_out ? launch_t<fp4dev::SF_E4M3, true>(a, st) : launch_t<fp4dev::SF_E4M3, false>(a, st);
-    case FP4_SF_UE5M3: return a.bf16_out ? launch_t<fp4dev::SF_UE5M3, true>(a, st) : launch_t<fp4dev::SF_UE5M3, false>(a, st);
-    case FP4_SF_E8M0: return a.bf16_out ? launch_t<fp4dev::SF_E8M0, true>(a, st) : launch_t<fp4dev::SF_E8M0, false>(a, st);
+    case FP4_SF_E4M3: return a.bf16_out ? launch_cm<fp4dev::SF_E4M3, true>(a, st) : launch_cm<fp4dev::SF_E4M3, false>(a, st);
+    case FP4_SF_UE5M3: return a.bf16_out ? launch_cm<fp4dev::SF_UE5M3, true>(a, st) : launch_cm<fp4dev::SF_UE5M3, false>(a, st);
+    case FP4_SF_E8M0: return a.bf16_out ? launch_cm<fp4dev::SF_E8M0, true>(a, st) : launch_cm<fp4dev::SF_E8M0, false>(a, st);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -134,3 +134,14 @@ def test_config3_fwd_dgrad_wgrad_scaled():
     for a, b in [(qX, qW), (qdY, qWt), (qdYt, qXt)]:
         C, S = Gm.gemm_ref(a["codes"], a["scales"], a["amax"], b["codes"], b["scales"], b["amax"], "E4M3")
         check_bound(gpu_gemm(a, b, "E4M3", "bf16"), C, S, bf16=True)
+
+
+@pytest.mark.parametrize("fmt", ["E4M3", "E8M0"])
+def test_long_k_plan(fmt):
+    # K >= 8192 takes the deeper 4-stage ring with 16-byte output blocks
+    A = synth.normal((256, 8192), 23, 0, outlier_p=0.01, outlier_mult=50.0)
+    B = synth.normal((512, 8192), 23, 1, std=0.02)
+    qa, qb = oracle_q(A, fmt), oracle_q(B, fmt)
+    C, S = Gm.gemm_ref(qa["codes"], qa["scales"], qa["amax"], qb["codes"], qb["scales"], qb["amax"], fmt)
+    check_bound(gpu_gemm(qa, qb, fmt), C, S)
+    check_bound(gpu_gemm(qa, qb, fmt, "bf16"), C, S, bf16=True)
