@@ -15,20 +15,24 @@
 // into alpha (the software emulation of the "UE5M3 ..." blog, "Ограничения").
 //
 // Kernel structure (one CTA per SM, persistent over 128 x 256 output tiles,
-// 22 warps):
-//   warp 0       TMA producer: A/B code tiles (128-byte swizzle) by
-//                cp.async.bulk.tensor, scale atoms by cp.async.bulk, into a
-//                4-stage shared-memory ring guarded by mbarriers;
+// 23 warps):
+//   warp 0       code producer: A/B code tiles (128-byte swizzle) by
+//                cp.async.bulk.tensor into a 3- or 4-stage shared-memory ring;
 //   warp 1       allocates tensor memory; one lane issues the 4 tcgen05.mma of
-//                each 256-wide K step once its scales sit in tensor memory, and
-//                tcgen05.commit frees the stage (and, after the last K step,
-//                hands the accumulator over);
-//   warps 2-5    scale writers, one per 32-lane quarter of tensor memory: each
+//                each 256-wide K step once its scales sit in tensor memory and
+//                its codes in shared memory; tcgen05.commit frees the stage
+//                (and, after the last K step, hands the accumulator over);
+//   warp 2       scale producer: the K step's scale atoms by cp.async.bulk into
+//                a separate 4-slot ring that runs ahead of the code ring (a slot
+//                frees as soon as the scale writers have read it);
+//   warps 3-6    scale writers, one per 32-lane quarter of tensor memory: each
 //                lane reads its row of every 512-byte scale atom from shared
-//                memory and writes it with tcgen05.st into the replicated
-//                layout the MMA reads (row r's scales in column r/32 of lane
-//                r%32 of every quarter);
-//   warps 6-21   epilogue: each warp drains 32 rows x 64 columns of the
+//                memory and, once the MMAs of K step k - STAGES have released
+//                the stage's tensor-memory columns, writes it with tcgen05.st
+//                into the replicated layout the MMA reads (row r's scales in
+//                column r/32 of lane r%32 of every quarter), off the MMA's
+//                critical path;
+//   warps 7-22   epilogue: each warp drains 32 rows x 64 columns of the
 //                float32 accumulator with tcgen05.ld, releases the tensor
 //                memory at once (the next tile's MMAs overlap the rest), scales,
 //                converts and stages 32-row x 16-byte blocks in shared memory
@@ -57,7 +61,9 @@ constexpr int SFB_MAX = BN * BK / 16;  // 4 KB
 
 constexpr int NUM_SF_WARPS = 4;
 constexpr int NUM_EPI_WARPS = 16;
-constexpr int FIRST_SF_WARP = 2;
+constexpr int SF_PRODUCER_WARP = 2;
+constexpr int FIRST_SF_WARP = 3;
+constexpr int SF_SLOTS = 4;  // scale ring depth
 constexpr int FIRST_EPI_WARP = FIRST_SF_WARP + NUM_SF_WARPS;
 constexpr int NUM_THREADS = 32 * (FIRST_EPI_WARP + NUM_EPI_WARPS);
 constexpr int EPI_COLS = BN / (NUM_EPI_WARPS / 4);  // 64 accumulator columns per epilogue warp
@@ -74,8 +80,8 @@ struct Plan {
   static constexpr int SMEM_A = 0;
   static constexpr int SMEM_B = SMEM_A + S * A_BYTES;
   static constexpr int SMEM_SFA = SMEM_B + S * B_BYTES;
-  static constexpr int SMEM_SFB = SMEM_SFA + S * SFA_MAX;
-  static constexpr int SMEM_OUT = SMEM_SFB + S * SFB_MAX;
+  static constexpr int SMEM_SFB = SMEM_SFA + SF_SLOTS * SFA_MAX;
+  static constexpr int SMEM_OUT = SMEM_SFB + SF_SLOTS * SFB_MAX;
   static constexpr int SMEM_BAR = SMEM_OUT + NUM_EPI_WARPS * STAGE_BYTES;
   static constexpr int SMEM_TOTAL = SMEM_BAR + 256;
   static constexpr int SMEM_LAUNCH = SMEM_TOTAL + 1024;  // room to align the base to 1024
@@ -311,16 +317,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
-  // barriers: full[S] (codes landed), sfdata[S] (scales landed), sf[S]
-  // (scales written to tensor memory), empty[S], acc_full, acc_empty
+  // barriers: full[S] (codes landed), sf[S] (scales written to tensor
+  // memory), empty[S] (stage's MMAs done), sfd_full[F] / sfd_empty[F] (scale
+  // ring slot landed / read), acc_full, acc_empty
   const uint32_t bar_full = sbase + SMEM_BAR;
-  const uint32_t bar_sfdata = bar_full + 8 * STAGES;
-  const uint32_t bar_sf = bar_sfdata + 8 * STAGES;
+  const uint32_t bar_sf = bar_full + 8 * STAGES;
   const uint32_t bar_empty = bar_sf + 8 * STAGES;
-  const uint32_t bar_acc_full = bar_empty + 8 * STAGES;
+  const uint32_t bar_sfd_full = bar_empty + 8 * STAGES;
+  const uint32_t bar_sfd_empty = bar_sfd_full + 8 * SF_SLOTS;
+  const uint32_t bar_acc_full = bar_sfd_empty + 8 * SF_SLOTS;
   const uint32_t bar_acc_empty = bar_acc_full + 8;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + SMEM_BAR + 8 * (4 * STAGES + 2));
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + SMEM_BAR + 8 * (4 * STAGES + 2) + 8);
+  constexpr int BAR_BYTES = 8 * (3 * STAGES + 2 * SF_SLOTS + 2);
+  static_assert(BAR_BYTES + 16 <= 256, "barrier area");
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + SMEM_BAR + BAR_BYTES);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + SMEM_BAR + BAR_BYTES + 8);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int m_tiles = p.M / BM, n_tiles = p.N / BN;
@@ -336,9 +346,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(bar_full + 8 * s, 1);
-      mbar_init(bar_sfdata + 8 * s, 1);
       mbar_init(bar_sf + 8 * s, NUM_SF_WARPS);
       mbar_init(bar_empty + 8 * s, CM);  // one MMA commit from each cluster CTA
+    }
+    for (int s = 0; s < SF_SLOTS; ++s) {
+      mbar_init(bar_sfd_full + 8 * s, 1);
+      mbar_init(bar_sfd_empty + 8 * s, NUM_SF_WARPS);
     }
     mbar_init(bar_acc_full, 1);
     mbar_init(bar_acc_empty, NUM_EPI_WARPS);
@@ -374,21 +387,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             ok = false;
             break;
           }
-          // scales first, on their own barrier, so the scale writers can move
-          // them into tensor memory while the code tiles are still in flight
-          const uint32_t sb = bar_sfdata + 8 * stage;
           const uint32_t fb = bar_full + 8 * stage;
-          mbar_expect_tx(sb, SFA_BYTES + 2 * SFB_HALF);
-          // scales of this K step: SFA_BYTES contiguous bytes per 128-row slab
-          bulk_load(sbase + SMEM_SFA + stage * SFA_MAX, p.As + mt * sf_row_stride + (int64_t)ks * SFA_BYTES,
-                    SFA_BYTES, sb);
           mbar_expect_tx(fb, A_BYTES + B_BYTES);
           tma_load_2d(sbase + SMEM_A + stage * A_BYTES, &tmap_a, fb, ks * (BK / 2), mt * BM);
           if constexpr (CM == 1) {
-            bulk_load(sbase + SMEM_SFB + stage * SFB_MAX, p.Bs + (2 * nt) * sf_row_stride + (int64_t)ks * SFB_HALF,
-                      SFB_HALF, sb);
-            bulk_load(sbase + SMEM_SFB + stage * SFB_MAX + SFB_HALF,
-                      p.Bs + (2 * nt + 1) * sf_row_stride + (int64_t)ks * SFB_HALF, SFB_HALF, sb);
             tma_load_2d(sbase + SMEM_B + stage * B_BYTES, &tmap_b, fb, ks * (BK / 2), nt * BN);
           } else {
             // rows [crank*BN/CM, +BN/CM) of the B tile: 128-byte rows, so the
@@ -396,11 +398,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             constexpr int ROWS = BN / CM;
             tma_load_2d_mc(sbase + SMEM_B + stage * B_BYTES + crank * ROWS * 128, &tmap_b, fb, ks * (BK / 2),
                            nt * BN + crank * ROWS, MC_MASK);
-            // 1/CM of the two 128-row scale halves
-            constexpr int PIECE = 2 * SFB_HALF / CM;
-            const int half = (crank * PIECE) / SFB_HALF, off = (crank * PIECE) % SFB_HALF;
-            bulk_load_mc(sbase + SMEM_SFB + stage * SFB_MAX + half * SFB_HALF + off,
-                         p.Bs + (2 * nt + half) * sf_row_stride + (int64_t)ks * SFB_HALF + off, PIECE, sb, MC_MASK);
           }
           if (++stage == STAGES) {
             stage = 0;
@@ -465,26 +462,61 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
     }
     __syncwarp();
+  } else if (warp == SF_PRODUCER_WARP) {
+    // ------------------------------ scale producer ------------------------
+    if (lane == 0) {
+      int slot = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int u = cluster_id; u < num_units && ok; u += num_clusters) {
+        const int mt = (u % m_groups) * CM + crank, nt = u / m_groups;
+        for (int ks = 0; ks < k_steps; ++ks) {
+          if (!wait_bounded(bar_sfd_empty + 8 * slot, phase ^ 1u, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          const uint32_t sb = bar_sfd_full + 8 * slot;
+          mbar_expect_tx(sb, SFA_BYTES + 2 * SFB_HALF);
+          // scales of this K step: SFA_BYTES contiguous bytes per 128-row slab
+          bulk_load(sbase + SMEM_SFA + slot * SFA_MAX, p.As + mt * sf_row_stride + (int64_t)ks * SFA_BYTES,
+                    SFA_BYTES, sb);
+          if constexpr (CM == 1) {
+            bulk_load(sbase + SMEM_SFB + slot * SFB_MAX, p.Bs + (2 * nt) * sf_row_stride + (int64_t)ks * SFB_HALF,
+                      SFB_HALF, sb);
+            bulk_load(sbase + SMEM_SFB + slot * SFB_MAX + SFB_HALF,
+                      p.Bs + (2 * nt + 1) * sf_row_stride + (int64_t)ks * SFB_HALF, SFB_HALF, sb);
+          } else {
+            // 1/CM of the two 128-row scale halves, multicast
+            constexpr int PIECE = 2 * SFB_HALF / CM;
+            const int half = (crank * PIECE) / SFB_HALF, off = (crank * PIECE) % SFB_HALF;
+            bulk_load_mc(sbase + SMEM_SFB + slot * SFB_MAX + half * SFB_HALF + off,
+                         p.Bs + (2 * nt + half) * sf_row_stride + (int64_t)ks * SFB_HALF + off, PIECE, sb, MC_MASK);
+          }
+          if (++slot == SF_SLOTS) {
+            slot = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+    }
+    __syncwarp();
   } else if (warp < FIRST_EPI_WARP) {
     // ------------------------------ scale writers -------------------------
     // Lane i of the warp serving quarter q writes, for every 512-byte atom
     // (rows 0..127 x 4 blocks), the atom's 16-byte row i -- the scales of rows
     // i, i+32, i+64, i+96 -- into 4 consecutive columns of lane 32q+i.
     const int quarter = warp & 3;
-    int stage = 0;
-    uint32_t phase = 0;
+    int stage = 0, slot = 0;
+    uint32_t phase = 0, sphase = 0;
     for (int u = cluster_id; u < num_units; u += num_clusters) {
       bool ok = true;
       for (int ks = 0; ks < k_steps; ++ks) {
-        // the new phase of sfdata[s] comes after the producer saw empty[s], so
-        // the MMAs that read this stage's scale columns last time have finished
-        if (!wait_bounded(bar_sfdata + 8 * stage, phase, abort_flag, p.status)) {
+        if (!wait_bounded(bar_sfd_full + 8 * slot, sphase, abort_flag, p.status)) {
           ok = false;
           break;
         }
-        const uint8_t* sfa = smem + SMEM_SFA + stage * SFA_MAX + 16 * lane;
-        const uint8_t* sfb = smem + SMEM_SFB + stage * SFB_MAX + 16 * lane;
-        const uint32_t lane_base = tmem_base + ((uint32_t)(32 * quarter) << 16);
+        const uint8_t* sfa = smem + SMEM_SFA + slot * SFA_MAX + 16 * lane;
+        const uint8_t* sfb = smem + SMEM_SFB + slot * SFB_MAX + 16 * lane;
         uint32_t va[4 * ATOMS], vb[8 * ATOMS];
 #pragma unroll
         for (int j = 0; j < ATOMS; ++j) {
@@ -495,6 +527,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           vb[8 * j + 0] = b0.x; vb[8 * j + 1] = b0.y; vb[8 * j + 2] = b0.z; vb[8 * j + 3] = b0.w;
           vb[8 * j + 4] = b1.x; vb[8 * j + 5] = b1.y; vb[8 * j + 6] = b1.z; vb[8 * j + 7] = b1.w;
         }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_sfd_empty + 8 * slot);  // the scale slot may refill
+        // this stage's tensor-memory columns are free once the MMAs of K step
+        // k - STAGES have completed (their commit to empty[stage])
+        if (!wait_bounded(bar_empty + 8 * stage, phase ^ 1u, abort_flag, p.status)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t lane_base = tmem_base + ((uint32_t)(32 * quarter) << 16);
         if constexpr (ATOMS == 4) {
           tc_st16(lane_base + TMEM_SFA + 16 * stage, va);
           tc_st32(lane_base + TMEM_SFB + 32 * stage, vb);
@@ -509,6 +551,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (++stage == STAGES) {
           stage = 0;
           phase ^= 1u;
+        }
+        if (++slot == SF_SLOTS) {
+          slot = 0;
+          sphase ^= 1u;
         }
       }
       if (!ok) break;

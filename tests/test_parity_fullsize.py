@@ -1,0 +1,117 @@
+"""Full-size parity in the benchmark's launch configuration (through the C ABI).
+
+Runs one step of bench.LinearStep on the Llama-2-7B MLP workload
+(M = 16384, K = 4096, N = 11008) exactly as bench.py times it, then checks
+sampled outputs against the oracle:
+  * fresh amaxes: exact;
+  * row and transposed quantizations of X, W and dY: sampled rows and columns,
+    codes and scales bit-exact (Philox indices in the output layout);
+  * forward, dgrad and wgrad GEMMs (bf16 out): sampled output rows against the
+    oracle's float64 GEMM over the oracle's own quantization of the operands.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import gemm as Gm
+from oracle import quantize as Q
+from gpu_util import from_mma, lib
+
+pytestmark = [pytest.mark.gpu, pytest.mark.slow]
+
+
+@pytest.fixture(scope="module")
+def step():
+    lib()
+    import bench
+    d = bench.make_inputs()
+    s = bench.LinearStep(d, torch.device("cuda", 0))
+    s.run()
+    torch.cuda.synchronize()
+    assert int(s.status.item()) == 0
+    return bench, d, s
+
+
+def _rows(n, k, seed):
+    rng = np.random.default_rng(seed)
+    return np.unique(np.concatenate([[0, n - 1], rng.integers(0, n, k)]))
+
+
+def test_amax_exact(step):
+    _, d, s = step
+    a = s.amax.cpu().numpy()
+    for j, name in enumerate(["X", "W", "dY"]):
+        assert a[j] == np.float32(d[name].float().abs().max().item()), name
+
+
+@pytest.mark.parametrize("name,rr,seed_r,rc,seed_c", [("X", "rne", 0, "sr", 1236), ("W", "rne", 0, "rne", 0),
+                                                      ("dY", "sr", 1234, "sr", 1235)])
+def test_quantizer_sampled(step, name, rr, seed_r, rc, seed_c):
+    _, d, s = step
+    x = d[name]
+    R, C = x.shape
+    g = float(x.float().abs().max())
+    cr, sr, cc, sc = (t.cpu().numpy() for t in s.q[name])
+    srow = from_mma(sr, R, C // 16)
+    scol = from_mma(sc, C, R // 16)
+    for r in _rows(R, 6, 1):
+        codes, scales = Q.quantize_rows(x[r:r + 1].float().numpy(), "E4M3", rr, seed_r, g, row0=int(r))
+        assert np.array_equal(cr[r], codes[0]) and np.array_equal(srow[r], scales[0]), (name, "row", r)
+    for c in _rows(C, 6, 2):
+        col = x[:, c].float().numpy()[None, :]
+        codes, scales = Q.quantize_rows(col, "E4M3", rc, seed_c, g, row0=int(c))
+        assert np.array_equal(cc[c], codes[0]) and np.array_equal(scol[c], scales[0]), (name, "col", c)
+
+
+def _check_rows(Cg, a, b, rows):
+    C, S = Gm.gemm_ref_rows(a["codes"], a["scales"], a["amax"], b["codes"], b["scales"], b["amax"], "E4M3", rows)
+    got = Cg[rows].float().cpu().numpy()
+    bound = Gm.gemm_bound(S) + np.abs(C) * 2.0 ** -8
+    err = np.abs(got - C)
+    assert (err <= bound).all(), f"worst ratio {np.max(err / bound):.3g}"
+
+
+def test_gemms_sampled_rows(step):
+    _, d, s = step
+    X, W, dY = (d[k].float().numpy() for k in ("X", "W", "dY"))
+    M, N = dY.shape
+    qW = Q.quantize(W, "E4M3", "rne", 0, chunk_rows=512)
+    qWt = Q.quantize(W, "E4M3", "rne", 0, transpose=True, chunk_rows=512)
+    qXt = Q.quantize(X, "E4M3", "sr", 1236, transpose=True, chunk_rows=256)
+    rows_m = _rows(M, 10, 3)
+    rows_n = _rows(N, 10, 4)
+    # forward Y = X W^T: sampled token rows of Q(X)
+    g_X = np.float32(np.max(np.abs(X)))
+    qX_rows = np.zeros((M, X.shape[1] // 2), np.uint8)
+    sX_rows = np.zeros((M, X.shape[1] // 16), np.uint8)
+    for r in rows_m:
+        c, sc = Q.quantize_rows(X[r:r + 1], "E4M3", "rne", 0, g_X, row0=int(r))
+        qX_rows[r], sX_rows[r] = c[0], sc[0]
+    _check_rows(s.Y, {"codes": qX_rows, "scales": sX_rows, "amax": g_X}, qW, rows_m)
+    # dgrad dX = dY W: rows of Q(dY) on the sampled tokens, B = Q(W^T)
+    g_dY = np.float32(np.max(np.abs(dY)))
+    qdY_rows = np.zeros((M, N // 2), np.uint8)
+    sdY_rows = np.zeros((M, N // 16), np.uint8)
+    for r in rows_m:
+        c, sc = Q.quantize_rows(dY[r:r + 1], "E4M3", "sr", 1234, g_dY, row0=int(r))
+        qdY_rows[r], sdY_rows[r] = c[0], sc[0]
+    _check_rows(s.dX, {"codes": qdY_rows, "scales": sdY_rows, "amax": g_dY}, qWt, rows_m)
+    # wgrad dW = dY^T X: sampled rows of Q(dY^T) (columns of dY), B = Q(X^T)
+    qdYt_rows = np.zeros((N, M // 2), np.uint8)
+    sdYt_rows = np.zeros((N, M // 16), np.uint8)
+    for c in rows_n:
+        cd, sc = Q.quantize_rows(dY[:, c][None, :], "E4M3", "sr", 1235, g_dY, row0=int(c))
+        qdYt_rows[c], sdYt_rows[c] = cd[0], sc[0]
+    _check_rows(s.dW, {"codes": qdYt_rows, "scales": sdYt_rows, "amax": g_dY}, qXt, rows_n)
+
+
+def test_gemv_sampled(step):
+    _, d, s = step
+    W = d["W"].float().numpy()
+    qw = Q.quantize(W, "E4M3", "rne", 0)
+    x = d["x_dec"].float().numpy()
+    y, S = Gm.gemv_ref(qw["codes"], qw["scales"], qw["amax"], x)
+    got = s.yg.float().cpu().numpy()
+    bound = Gm.gemm_bound(S) + np.abs(y) * 2.0 ** -8
+    assert (np.abs(got - y) <= bound).all()
