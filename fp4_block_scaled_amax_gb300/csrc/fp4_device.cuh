@@ -89,10 +89,17 @@ __device__ __forceinline__ uint32_t exmy_encode_rne_sat(float s) {
 enum : int { SF_E4M3 = FP4_SF_E4M3, SF_UE5M3 = FP4_SF_UE5M3, SF_E8M0 = FP4_SF_E8M0, SF_E1M6 = FP4_SF_E1M6 };
 
 template <int FMT> struct ScaleFmt;
+// E4M3 (FN) nearest-even with saturation to 448 is the hardware conversion;
+// it equals exmy_encode_rne_sat<3, 7, 0x7E> for every non-negative input.
+__device__ __forceinline__ uint32_t e4m3_encode_hw(float s) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(0.0f), "f"(s));
+  return (uint32_t)(r & 0xFFu);
+}
 template <> struct ScaleFmt<SF_E4M3> {
   static constexpr int G = 16;
   static constexpr float SIX_ST = 2688.0f;  // 6 * 448
-  __device__ static uint32_t encode(float s) { return exmy_encode_rne_sat<3, 7, 0x7Eu>(s); }
+  __device__ static uint32_t encode(float s) { return e4m3_encode_hw(s); }
   __device__ static float decode(uint32_t c) { return exmy_decode<3, 7>(c); }
 };
 template <> struct ScaleFmt<SF_UE5M3> {
@@ -139,6 +146,26 @@ struct BlockScale {
   uint32_t code;
   float r;  // element multiplier s_enc / s_b (0 when s_b == 0)
 };
+
+// Element multiplier of a scale code: s_enc / s_b (0 when s_b == 0).
+template <int FMT>
+__device__ __forceinline__ float code_multiplier(uint32_t code, float s_enc) {
+  const float s_b = ScaleFmt<FMT>::decode(code);
+  return (s_b == 0.0f) ? 0.0f : __fdiv_rn(s_enc, s_b);
+}
+
+// Block scale with the multiplier looked up in a per-CTA table of all codes.
+template <int FMT>
+__device__ __forceinline__ BlockScale block_scale_tab(float a_b, float s_enc, const float* rtab) {
+  BlockScale out;
+  if constexpr (FMT == SF_E8M0) {
+    out.code = ScaleFmt<SF_E8M0>::encode_from_amax(a_b);
+  } else {
+    out.code = ScaleFmt<FMT>::encode(__fmul_rn(__fdiv_rn(a_b, 6.0f), s_enc));
+  }
+  out.r = rtab[out.code];
+  return out;
+}
 
 template <int FMT>
 __device__ __forceinline__ BlockScale block_scale(float a_b, float s_enc) {
@@ -244,16 +271,32 @@ __device__ __forceinline__ uint32_t draw16(const uint4& w, int j) {
 // first) with block multiplier r into 8 bytes of packed codes.
 // Philox indices of the 16 elements start at idx0 (a multiple of 8).
 // ---------------------------------------------------------------------------
+// Four pairs (lo in the low nibble of each byte) -> one 32-bit word, byte 0
+// from the first pair.
+__device__ __forceinline__ uint32_t e2m1x8_rne(const float* y) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
+      "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
+      : "=r"(r)
+      : "f"(y[0]), "f"(y[1]), "f"(y[2]), "f"(y[3]), "f"(y[4]), "f"(y[5]), "f"(y[6]), "f"(y[7]));
+  return r;
+}
+
 template <bool SR>
 __device__ __forceinline__ uint2 quant16(const uint32_t* w, float r, uint64_t seed, uint64_t idx0) {
   uint32_t bytes[8];
   if constexpr (!SR) {
+    float y[16];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      const float y0 = __fmul_rn(bf16_lo(w[i]), r);
-      const float y1 = __fmul_rn(bf16_hi(w[i]), r);
-      bytes[i] = e2m1x2_rne(y0, y1);
+      y[2 * i] = __fmul_rn(bf16_lo(w[i]), r);
+      y[2 * i + 1] = __fmul_rn(bf16_hi(w[i]), r);
     }
+    return make_uint2(e2m1x8_rne(y), e2m1x8_rne(y + 8));
   } else {
 #pragma unroll
     for (int h = 0; h < 2; ++h) {

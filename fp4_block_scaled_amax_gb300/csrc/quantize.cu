@@ -13,7 +13,7 @@
 //   k_amax            max|x| of a bf16 matrix (fresh global amax), 2 B/elem read.
 //   k_quant_rows      blocks along K; one thread per 16 elements straight from
 //                     two 128-bit loads; 2 + 0.5 + 1/G B per element.
-//   k_quant_tile      32 x 256 tile staged in shared memory; writes the
+//   k_quant_tile      64 x 128 tile staged in shared memory; writes the
 //                     transposed quantization (blocks along M) and, in the dual
 //                     form, the row quantization from the same read:
 //                     2 + 2 * (0.5 + 1/G) B per element.
@@ -131,8 +131,18 @@ __global__ void __launch_bounds__(256) k_quant_rows(const uint16_t* __restrict__
 // ---------------------------------------------------------------------------
 // K2/K3: tile quantizer (transposed output, plus the row output when DUAL)
 // ---------------------------------------------------------------------------
-constexpr int TILE_M = 32;
-constexpr int TILE_K = 256;
+// A CTA stages a 64-row x 128-column bf16 tile in shared memory.  Row pass:
+// each thread quantizes two 16-element chunks straight from its loads.
+// Column pass: thread t takes column t/2 and the 32-row half t%2, so two
+// neighbouring lanes write one whole 32-byte sector of the transposed output.
+// Columns are stored XOR-swizzled by the half (bit 4 of the column index
+// flips for rows 32..63), which keeps the column pass free of bank conflicts.
+// The element multipliers s_enc / s_b of all 256 scale codes are computed
+// once per CTA into a shared table (the same correctly rounded division).
+constexpr int TILE_M = 64;
+constexpr int TILE_K = 128;
+
+__device__ __forceinline__ int tile_col(int r, int c) { return c ^ (((r >> 5) & 1) << 4); }
 
 template <int FMT, bool DUAL, bool ROW_SR, bool COL_SR, bool MMA, bool AMAX>
 __global__ void __launch_bounds__(256) k_quant_tile(
@@ -142,40 +152,53 @@ __global__ void __launch_bounds__(256) k_quant_tile(
     int32_t* status) {
   constexpr int G = ScaleFmt<FMT>::G;
   __shared__ __align__(16) uint16_t tile[TILE_M][TILE_K];
-  // blockIdx.x walks M fastest so neighbouring CTAs fill the two halves of each
-  // 32-byte sector of the transposed output
+  __shared__ float rtab[256];
+  // blockIdx.x walks M fastest so neighbouring CTAs write neighbouring
+  // sectors of each transposed-output row
   const int64_t m0 = (int64_t)blockIdx.x * TILE_M;
   const int64_t k0 = (int64_t)blockIdx.y * TILE_K;
   const float s_enc = global_encode_scale<FMT>(
       __ldg(gptr), (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) ? status : nullptr);
 
-  // ---- load 32 x 256 (two 16-element chunks per thread), row pass ----
+  // ---- load 64 x 128 (two 16-element chunks per thread, all loads first) ----
+  uint32_t w[2][8];
+  bool valid[2];
+#pragma unroll
+  for (int it = 0; it < 2; ++it) {
+    const int j = threadIdx.x + 256 * it;  // chunk id in the tile: 8 chunks per row
+    const int r = j >> 3, cc = j & 7;
+    const int64_t col = k0 + cc * 16;
+    // K % 32 == 0 keeps a G=32 pair valid together; M % 32 == 0 makes a
+    // 32-row half all valid or all not
+    valid[it] = col < K && m0 + r < M;
+    if (valid[it]) {
+      const uint16_t* src = x + (m0 + r) * ldx + col;
+      const uint4 v0 = ld_stream(src), v1 = ld_stream(src + 8);
+      w[it][0] = v0.x; w[it][1] = v0.y; w[it][2] = v0.z; w[it][3] = v0.w;
+      w[it][4] = v1.x; w[it][5] = v1.y; w[it][6] = v1.z; w[it][7] = v1.w;
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) w[it][i] = 0u;
+    }
+  }
+  rtab[threadIdx.x] = code_multiplier<FMT>(threadIdx.x, s_enc);
+  __syncthreads();
   float amax_local = 0.0f;
 #pragma unroll
   for (int it = 0; it < 2; ++it) {
-    const int j = threadIdx.x + 256 * it;  // chunk id in the tile
-    const int r = j >> 4;                  // 16 chunks per tile row
-    const int cc = j & 15;
-    const int64_t col = k0 + cc * 16;
-    const bool valid = col < K;  // K % 32 == 0: a G=32 pair is valid together
-    uint32_t w[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-    if (valid) {
-      const uint16_t* src = x + (m0 + r) * ldx + col;
-      const uint4 v0 = ld_stream(src), v1 = ld_stream(src + 8);
-      w[0] = v0.x; w[1] = v0.y; w[2] = v0.z; w[3] = v0.w;
-      w[4] = v1.x; w[5] = v1.y; w[6] = v1.z; w[7] = v1.w;
-    }
-    uint4* dst = reinterpret_cast<uint4*>(&tile[r][cc * 16]);
-    dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-    dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
-    float a = absmax_words(w, 8);
+    const int j = threadIdx.x + 256 * it;
+    const int r = j >> 3, cc = j & 7;
+    uint4* dst = reinterpret_cast<uint4*>(&tile[r][tile_col(r, cc * 16)]);
+    dst[0] = make_uint4(w[it][0], w[it][1], w[it][2], w[it][3]);
+    dst[1] = make_uint4(w[it][4], w[it][5], w[it][6], w[it][7]);
+    float a = absmax_words(w[it], 8);
     amax_local = fmaxf(amax_local, a);
     if constexpr (DUAL) {
       if constexpr (G == 32) a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 1));
-      if (valid) {
-        const int64_t row = m0 + r;
-        const BlockScale bs = block_scale<FMT>(a, s_enc);
-        const uint2 q = quant16<ROW_SR>(w, bs.r, seed_row, (uint64_t)(row * K + col));
+      if (valid[it]) {
+        const int64_t row = m0 + r, col = k0 + cc * 16;
+        const BlockScale bs = block_scale_tab<FMT>(a, s_enc, rtab);
+        const uint2 q = quant16<ROW_SR>(w[it], bs.r, seed_row, (uint64_t)(row * K + col));
         *reinterpret_cast<uint2*>(codes_row + row * (K / 2) + col / 2) = q;
         if (G == 16 || (cc & 1) == 0) {
           const int64_t b = col / G;
@@ -191,33 +214,35 @@ __global__ void __launch_bounds__(256) k_quant_tile(
   }
   __syncthreads();
 
-  // ---- column pass: thread t owns column k0 + t, rows m0 .. m0+31 ----
-  const int t = threadIdx.x;
-  const int64_t c = k0 + t;
-  if (c >= K) return;
-  uint32_t w[16];
+  // ---- column pass: thread t owns column k0 + t/2, rows m0 + 32*(t%2) .. +31 ----
+  const int cl = threadIdx.x >> 1, h = threadIdx.x & 1;
+  const int64_t c = k0 + cl;
+  const int64_t rbase = m0 + 32 * h;
+  if (c >= K || rbase >= M) return;
+  const int pc = cl ^ (h << 4);
+  uint32_t v[16];
 #pragma unroll
   for (int i = 0; i < 16; ++i)
-    w[i] = (uint32_t)tile[2 * i][t] | ((uint32_t)tile[2 * i + 1][t] << 16);
-  const uint64_t idx0 = (uint64_t)(c * M + m0);
+    v[i] = (uint32_t)tile[32 * h + 2 * i][pc] | ((uint32_t)tile[32 * h + 2 * i + 1][pc] << 16);
+  const uint64_t idx0 = (uint64_t)(c * M + rbase);
   uint2 q0, q1;
   uint32_t sc0, sc1 = 0;
   if constexpr (G == 16) {
-    const BlockScale b0 = block_scale<FMT>(absmax_words(w, 8), s_enc);
-    const BlockScale b1 = block_scale<FMT>(absmax_words(w + 8, 8), s_enc);
-    q0 = quant16<COL_SR>(w, b0.r, seed_col, idx0);
-    q1 = quant16<COL_SR>(w + 8, b1.r, seed_col, idx0 + 16);
+    const BlockScale b0 = block_scale_tab<FMT>(absmax_words(v, 8), s_enc, rtab);
+    const BlockScale b1 = block_scale_tab<FMT>(absmax_words(v + 8, 8), s_enc, rtab);
+    q0 = quant16<COL_SR>(v, b0.r, seed_col, idx0);
+    q1 = quant16<COL_SR>(v + 8, b1.r, seed_col, idx0 + 16);
     sc0 = b0.code;
     sc1 = b1.code;
   } else {
-    const BlockScale b0 = block_scale<FMT>(absmax_words(w, 16), s_enc);
-    q0 = quant16<COL_SR>(w, b0.r, seed_col, idx0);
-    q1 = quant16<COL_SR>(w + 8, b0.r, seed_col, idx0 + 16);
+    const BlockScale b0 = block_scale_tab<FMT>(absmax_words(v, 16), s_enc, rtab);
+    q0 = quant16<COL_SR>(v, b0.r, seed_col, idx0);
+    q1 = quant16<COL_SR>(v + 8, b0.r, seed_col, idx0 + 16);
     sc0 = b0.code;
   }
-  *reinterpret_cast<uint4*>(codes_col + c * (M / 2) + m0 / 2) = make_uint4(q0.x, q0.y, q1.x, q1.y);
+  *reinterpret_cast<uint4*>(codes_col + c * (M / 2) + rbase / 2) = make_uint4(q0.x, q0.y, q1.x, q1.y);
   const int64_t nb = M / G;
-  const int64_t b = m0 / G;
+  const int64_t b = rbase / G;
   if constexpr (G == 16) {
     // blocks b, b+1 (b even) are adjacent bytes in both layouts
     const int64_t off = MMA ? mma_sf_offset(c, b, nb) : c * nb + b;
@@ -372,7 +397,7 @@ static void rows_t(const QuantArgs& a, cudaStream_t st) {
 template <int FMT, bool DUAL, bool RSR, bool CSR, bool MMA, bool AMAX>
 static void tile_t(const QuantArgs& a, cudaStream_t st) {
   if (a.M == 0 || a.K == 0) return;
-  dim3 grid((unsigned)(a.M / TILE_M), (unsigned)((a.K + TILE_K - 1) / TILE_K));
+  dim3 grid((unsigned)((a.M + TILE_M - 1) / TILE_M), (unsigned)((a.K + TILE_K - 1) / TILE_K));
   k_quant_tile<FMT, DUAL, RSR, CSR, MMA, AMAX><<<grid, 256, 0, st>>>(
       static_cast<const uint16_t*>(a.x), a.M, a.K, a.ldx, a.gptr, a.seed_row, a.seed_col, a.codes_row,
       a.scales_row, a.codes_col, a.scales_col, a.amax_out, a.status);
