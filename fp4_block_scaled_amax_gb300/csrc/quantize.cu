@@ -51,18 +51,20 @@ __global__ void __launch_bounds__(256) k_amax(const uint16_t* __restrict__ x, in
   const int64_t per_row = K / 8;  // 16-byte chunks per row
   const int64_t total = M * per_row;
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  const bool dense = ldx == K;  // rows back to back: one flat array, no index division
   uint32_t m = 0;
   int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  for (; i + 3 * stride < total; i += 4 * stride) {
-    uint4 v[4];
+  auto addr = [&](int64_t c) -> const uint16_t* {
+    if (dense) return x + c * 8;
+    const int64_t r = c / per_row;
+    return x + r * ldx + (c - r * per_row) * 8;
+  };
+  for (; i + 7 * stride < total; i += 8 * stride) {
+    uint4 v[8];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int64_t c = i + u * stride;
-      const int64_t r = c / per_row;
-      v[u] = ld_stream(x + r * ldx + (c - r * per_row) * 8);
-    }
+    for (int u = 0; u < 8; ++u) v[u] = ld_stream(addr(i + u * stride));
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
+    for (int u = 0; u < 8; ++u) {
       m = absmax2(m, v[u].x & 0x7FFF7FFFu);
       m = absmax2(m, v[u].y & 0x7FFF7FFFu);
       m = absmax2(m, v[u].z & 0x7FFF7FFFu);
@@ -70,8 +72,7 @@ __global__ void __launch_bounds__(256) k_amax(const uint16_t* __restrict__ x, in
     }
   }
   for (; i < total; i += stride) {
-    const int64_t r = i / per_row;
-    const uint4 v = ld_stream(x + r * ldx + (i - r * per_row) * 8);
+    const uint4 v = ld_stream(addr(i));
     m = absmax2(m, v.x & 0x7FFF7FFFu);
     m = absmax2(m, v.y & 0x7FFF7FFFu);
     m = absmax2(m, v.z & 0x7FFF7FFFu);
