@@ -50,9 +50,13 @@ STEP_FLOPS = 3 * 2 * M_TOK * N_FFN * K_HID
 WORKLOAD = "llama2-7b-mlp-linear-fwd-bwd"
 METRIC = "NVFP4 GEMM TFLOPS & quantize GB/s at 7B shapes, % of FP4-MMA/HBM peak"
 FP4_PER_BF16 = 6.0  # nominal dense FP4 / bf16 tensor ratio on GB300 (13.5 / 2.25 PFLOP/s)
-# DRAM traffic per launch from one ncu capture, valid only while the kernel
-# source hashes to the recorded value.
-NCU_TRAFFIC = {}
+# DRAM bytes (read + write) from one ncu capture, valid only while the kernel
+# sources still hash to the recorded value.  quant_dual: the step's three dual
+# quantizations, captured at 8192 tokens and scaled by the rows processed
+# (streaming kernel: X and dY scale with tokens, W does not).  The GEMM's
+# traffic does not scale in proportion with tokens and is reported as null.
+NCU_TRAFFIC = {"quant_dual": {"bytes": 687.5e6, "src": "b63730b6d234c550",
+                              "files": ["quantize.cu", "fp4_device.cuh"]}}
 
 
 def parse():
@@ -277,9 +281,12 @@ def make_inputs():
     return d
 
 
-def src_hash(name):
-    with open(os.path.join(ROOT, "fp4_block_scaled_amax_gb300", "csrc", name), "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+def src_hash(names):
+    h = hashlib.sha256()
+    for name in names:
+        with open(os.path.join(ROOT, "fp4_block_scaled_amax_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 def run_ours(args, rank, world, local):
@@ -332,10 +339,11 @@ def run_ours(args, rank, world, local):
     a_gbs = sum(e * 2 for e in elems) / (sum(amax_ms) / args.steps * 1e-3) / 1e9
     gv_bytes = N_FFN * K_HID * (0.5 + 1 / 16) + 2 * GEMV_BATCH * (N_FFN + K_HID)
     gv_gbs = gv_bytes / (statistics.mean(gemv_ms) * 1e-3) / 1e9
-    traffic = NCU_TRAFFIC.get("gemm")
-    traffic_v = traffic["bytes"] if traffic and traffic["src"] == src_hash("gemm_sm103.cu") else None
-    qtraffic = NCU_TRAFFIC.get("quant_dual")
-    qtraffic_v = qtraffic["bytes"] if qtraffic and qtraffic["src"] == src_hash("quantize.cu") else None
+    def traffic_of(key):
+        t = NCU_TRAFFIC.get(key)
+        return t["bytes"] if t and t["src"] == src_hash(t["files"]) and M_TOK == 16384 else None
+    traffic_v = traffic_of("gemm")
+    qtraffic_v = traffic_of("quant_dual")
 
     e2e = None
     if not args.no_e2e:
@@ -363,7 +371,7 @@ def run_ours(args, rank, world, local):
                      "achieved": round(gemm_tflops, 1), "peak": round(fp4_peak, 1), "unit": "TFLOP/s",
                      "frac": round(gemm_tflops / fp4_peak, 4), "traffic": traffic_v,
                      "peak_source": f"{src}: bf16 burst {bf16} x {FP4_PER_BF16} (nominal FP4/bf16)"},
-        "roofline_quantize": {"kernel": "k_quant_tile (dual, 3.125 B/elem)", "bound": "hbm",
+        "roofline_quantize": {"kernel": "k_quant_tile (dual, 3.125 B/elem; X, W, dY per step)", "bound": "hbm",
                               "achieved": round(q_gbs, 1), "peak": hbm, "unit": "GB/s",
                               "frac": round(q_gbs / hbm, 4), "traffic": qtraffic_v, "peak_source": src},
         "amax_gbs": round(a_gbs, 1),
