@@ -115,3 +115,75 @@ def test_gemv_sampled(step):
     got = s.yg.float().cpu().numpy()
     bound = Gm.gemm_bound(S) + np.abs(y) * 2.0 ** -8
     assert (np.abs(got - y) <= bound).all()
+
+
+# ---------------------------------------------------------------------------
+# 350M-parameter MLP linear (8192 x 4096 x 1024) at full size, three formats
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("fmt", ["E4M3", "UE5M3", "E8M0"])
+def test_config2_fullsize(fmt):
+    from fp4_block_scaled_amax_gb300 import synth
+    from gpu_util import dev, host, to_mma
+    fp4 = lib()
+    d = synth.config2()
+    X, W = d["X"], d["W"]
+    M, K = X.shape
+    N = W.shape[0]
+    G = Q.group_size(fmt)
+    out = {}
+    for name, x in (("X", X), ("W", W)):
+        R = x.shape[0]
+        codes = torch.empty((R, K // 2), dtype=torch.uint8, device="cuda")
+        scales = torch.empty(R * K // G, dtype=torch.uint8, device="cuda")
+        amax = torch.zeros(1, dtype=torch.float32, device="cuda")
+        fp4.fp4_quantize(dev(x), fmt, fp4.FP4_ROUND_RNE, 0, None, False, fp4.FP4_SFLAYOUT_MMA, codes, scales, amax)
+        ref = Q.quantize(x.float().numpy(), fmt, "rne", 0)
+        assert np.array_equal(host(codes), ref["codes"]), (fmt, name)
+        assert np.array_equal(from_mma(host(scales), R, K // G), ref["scales"]), (fmt, name)
+        out[name] = (codes, scales, amax, ref)
+    (xc, xs, xa, qx), (wc, ws, wa, qw) = out["X"], out["W"]
+    ta = tb = None
+    if fmt == "UE5M3":
+        ta, tb = torch.zeros(1, dtype=torch.int32, device="cuda"), torch.zeros(1, dtype=torch.int32, device="cuda")
+        xs2, ws2 = torch.empty_like(xs), torch.empty_like(ws)
+        fp4.fp4_ue5m3_to_e4m3(xs, ta, xs2)
+        fp4.fp4_ue5m3_to_e4m3(ws, tb, ws2)
+        xs, ws = xs2, ws2
+    C = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    fp4.fp4_gemm(xc, xs, wc, ws, xa, wa, ta, tb, M, N, K, fmt, fp4.FP4_OUT_F32, C, dev_status=st)
+    assert int(host(st)[0]) == 0
+    rows = _rows(M, 24, 5)
+    Cr, S = Gm.gemm_ref_rows(qx["codes"], qx["scales"], qx["amax"], qw["codes"], qw["scales"], qw["amax"], fmt, rows)
+    got = host(C)[rows]
+    assert (np.abs(got - Cr) <= Gm.gemm_bound(S)).all()
+
+
+# ---------------------------------------------------------------------------
+# Weight-only decode (Qwen2.5-7B-like MLP shapes) at full size
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("wname", ["W_up", "W_down"])
+def test_config5_fullsize(wname):
+    from fp4_block_scaled_amax_gb300 import synth
+    from gpu_util import dev, host
+    fp4 = lib()
+    W = synth.config5(1)[wname]
+    N, K = W.shape
+    codes = torch.empty((N, K // 2), dtype=torch.uint8, device="cuda")
+    scales = torch.empty(N * K // 16, dtype=torch.uint8, device="cuda")
+    amax = torch.zeros(1, dtype=torch.float32, device="cuda")
+    fp4.fp4_quantize(dev(W), "E4M3", fp4.FP4_ROUND_RNE, 0, None, False, fp4.FP4_SFLAYOUT_PLAIN, codes, scales, amax)
+    ref = Q.quantize(W.float().numpy(), "E4M3", "rne", 0, chunk_rows=2048)
+    assert np.array_equal(host(codes), ref["codes"])
+    assert np.array_equal(host(scales).reshape(N, -1), ref["scales"])
+    for b in (1, 8, 64):
+        xk = "x_up" if wname == "W_up" else "x_down"
+        x = synth.config5(b)[xk]
+        y = torch.empty((b, N), dtype=torch.bfloat16, device="cuda")
+        fp4.fp4_gemv_w4a16(codes, scales, amax, dev(x), b, N, K, fp4.FP4_OUT_BF16, y)
+        yr, S = Gm.gemv_ref(ref["codes"], ref["scales"], ref["amax"], x.float().numpy())
+        got = host(y.float())
+        bound = Gm.gemm_bound(S) + np.abs(yr) * 2.0 ** -8
+        assert (np.abs(got - yr) <= bound).all(), (wname, b)
