@@ -199,38 +199,34 @@ __device__ __forceinline__ uint32_t e2m1x2_rne(float lo, float hi) {
   return r;
 }
 
-// Software RNE of one value (|y| thresholds at the grid midpoints; a tie goes
-// to the even code): magnitude code with the sign of y in bit 3.
-__device__ __forceinline__ uint32_t e2m1_rne_soft(float y) {
-  const float a = fabsf(y);
-  uint32_t m = (uint32_t)(a > 0.25f) + (uint32_t)(a >= 0.75f) + (uint32_t)(a > 1.25f) +
-               (uint32_t)(a >= 1.75f) + (uint32_t)(a > 2.5f) + (uint32_t)(a >= 3.5f) +
-               (uint32_t)(a > 5.0f);
-  return m | ((__float_as_uint(y) >> 28) & 8u);
-}
-
 // Stochastic rounding of one value with a 16-bit draw r: lo <= |y| < hi the
 // neighbouring grid values, round up iff r < 65536 * (|y| - lo) / (hi - lo);
-// |y| >= 6 gives 6.  Branch-free on the float32 bits b of |y|:
-//  * |y| >= 1: the grid keeps one mantissa bit, and f * 2^22 is the low 22
-//    bits m22, so "up" is 64 r < m22, i.e. the carry out of
-//    m22 + (2^22 - 1 - 64 r) into bit 22; the truncated sum then holds the
-//    code: (b' >> 22) - 252 = 2 (e - 127) + 2 + m1 + up.
-//  * 0.5 <= |y| < 1: the grid step is 0.5, "up" is 128 r < m23, the carry of
-//    m23 + (2^23 - 1 - 128 r) into the exponent; code (b' >> 23) - 125.
-//  * |y| < 0.5: up iff r < |y| * 2^17, compared in float32 (both exact; r is
-//    rebuilt as 2^16 + r - 2^16 without a conversion instruction).
-__device__ __forceinline__ uint32_t e2m1_sr(float y, uint32_t r16) {
-  const uint32_t yb = __float_as_uint(y);
-  const uint32_t b = yb & 0x7FFFFFFFu;
-  const uint32_t rn = (~r16) & 0xFFFFu;  // 65535 - r
-  const uint32_t c_hi = min(((b + ((rn << 6) | 63u)) >> 22) - 252u, 7u);
-  const uint32_t c_mid = ((b + ((rn << 7) | 127u)) >> 23) - 125u;
-  const float rf = __fsub_rn(__uint_as_float(0x47800000u | (r16 << 7)), 65536.0f);
-  const uint32_t c_lo = (rf < __fmul_rn(__uint_as_float(b), 131072.0f)) ? 1u : 0u;
-  const uint32_t m = b >= 0x3F800000u ? c_hi : (b >= 0x3F000000u ? c_mid : c_lo);
-  return m | ((yb >> 28) & 8u);
+// |y| >= 6 gives 6.  Written on the float pipe, returning the rounded grid
+// value with the sign of x (the caller converts exact grid values to codes):
+//  * the grid step around |y| is 2^(k-1) with k = clamp(floor(log2|y|), 0, 2);
+//    z = |y| * 2^(1-k) is exact and puts the step at 1;
+//  * with rho = r * 2^-16, "up" is frac(z) > rho, so the rounded value in
+//    step units is ceil(z - rho).  z - rho rounded once to float32 (one fma)
+//    has the same ceiling: next to an integer n >= 1 the difference is a
+//    multiple of ulp(z), larger than half an ulp of n, and below 1 it is exact
+//    (or lies in (-1, 0], whose ceiling is 0 either way);
+//  * ceil of t in (-1, 2^22) is (t + 1.5*2^23 rounded up) - 1.5*2^23, both
+//    steps exact; larger t (and +Inf) only ever saturate.
+// The value ceil(.) * 2^(k-1) is a grid value, or 8 and above, which the
+// saturating E2M1 conversion maps to 6.  A zero result keeps the sign of x.
+// rbits is the float32 pattern of 1 + r * 2^-16 (0x3F800000 | r << 7).
+__device__ __forceinline__ float e2m1_sr_value(float x, float r, uint32_t rbits) {
+  const float ay = __fmul_rn(fabsf(x), r);
+  const uint32_t eb = min(max(__float_as_uint(ay) & 0x7F800000u, 0x3F800000u), 0x40800000u);  // 2^k
+  const float m = __uint_as_float(0x7F800000u - eb);                                              // 2^(1-k)
+  const float rho = __fsub_rn(__uint_as_float(rbits), 1.0f);
+  const float t = __fmaf_rn(ay, m, -rho);
+  const float c = __fsub_rn(__fadd_ru(t, 12582912.0f), 12582912.0f);
+  return __fmul_rn(c, __uint_as_float((eb - 0x00800000u) | (__float_as_uint(x) & 0x80000000u)));
 }
+// 1 + r * 2^-16 for the low and high 16-bit halves of a Philox word.
+__device__ __forceinline__ uint32_t sr_rbits_lo(uint32_t w) { return 0x3F800000u | ((w << 7) & 0x007FFF80u); }
+__device__ __forceinline__ uint32_t sr_rbits_hi(uint32_t w) { return 0x3F800000u | ((w >> 9) & 0x007FFF80u); }
 
 // ---------------------------------------------------------------------------
 // Philox4x32-10 (Salmon, Moraes, Dror, Shaw, SC'11): 10 rounds of
@@ -288,32 +284,27 @@ __device__ __forceinline__ uint32_t e2m1x8_rne(const float* y) {
 
 template <bool SR>
 __device__ __forceinline__ uint2 quant16(const uint32_t* w, float r, uint64_t seed, uint64_t idx0) {
-  uint32_t bytes[8];
+  float y[16];
   if constexpr (!SR) {
-    float y[16];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       y[2 * i] = __fmul_rn(bf16_lo(w[i]), r);
       y[2 * i + 1] = __fmul_rn(bf16_hi(w[i]), r);
     }
-    return make_uint2(e2m1x8_rne(y), e2m1x8_rne(y + 8));
   } else {
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const uint4 d = sr_draws8(seed, (idx0 >> 3) + h);
+      const uint32_t dw[4] = {d.x, d.y, d.z, d.w};
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const uint32_t wi = w[4 * h + i];
-        const float y0 = __fmul_rn(bf16_lo(wi), r);
-        const float y1 = __fmul_rn(bf16_hi(wi), r);
-        bytes[4 * h + i] = e2m1_sr(y0, draw16(d, 2 * i)) | (e2m1_sr(y1, draw16(d, 2 * i + 1)) << 4);
+        y[8 * h + 2 * i] = e2m1_sr_value(bf16_lo(wi), r, sr_rbits_lo(dw[i]));
+        y[8 * h + 2 * i + 1] = e2m1_sr_value(bf16_hi(wi), r, sr_rbits_hi(dw[i]));
       }
     }
   }
-  uint2 out;
-  out.x = bytes[0] | (bytes[1] << 8) | (bytes[2] << 16) | (bytes[3] << 24);
-  out.y = bytes[4] | (bytes[5] << 8) | (bytes[6] << 16) | (bytes[7] << 24);
-  return out;
+  return make_uint2(e2m1x8_rne(y), e2m1x8_rne(y + 8));
 }
 
 // Byte offset of scale (row r, block b) in the tiled MMA scale layout with nb
