@@ -14,6 +14,11 @@
 // scales arrive re-encoded as E4M3 of s * 2^-t (exact) and 2^(tA + tB) folds
 // into alpha (the software emulation of the "UE5M3 ..." blog, "Ограничения").
 //
+// Two forms share the roles below.  When M is a multiple of 256, clusters of
+// two CTAs run cta_group::2 MMAs on 256 x 256 output tiles (k_gemm_fp4_pair):
+// each SM holds half of the B tile, so it streams A + B/2 per K step.
+// Otherwise one CTA per SM runs 128 x 256 tiles (k_gemm_fp4).
+//
 // Kernel structure (one CTA per SM, persistent over 128 x 256 output tiles,
 // 23 warps):
 //   warp 0       code producer: A/B code tiles (128-byte swizzle) by
@@ -72,14 +77,15 @@ constexpr int EPI_COLS = BN / (NUM_EPI_WARPS / 4);  // 64 accumulator columns pe
 // and, per epilogue warp, one 32-row output block with OB-byte rows (OB = 64:
 // 64-byte-swizzled blocks; OB = 16: plain 512-byte blocks).  Short K (an
 // output-heavy GEMM) wants wide blocks; long K wants the deeper ring.
-template <int S, int OB>
+template <int S, int OB, int BB = B_BYTES>
 struct Plan {
   static constexpr int STAGES = S;
   static constexpr int OUT_ROW_BYTES = OB;
   static constexpr int STAGE_BYTES = 32 * OB;
+  static constexpr int B_STAGE = BB;  // B code bytes per stage (half the tile for a CTA pair)
   static constexpr int SMEM_A = 0;
   static constexpr int SMEM_B = SMEM_A + S * A_BYTES;
-  static constexpr int SMEM_SFA = SMEM_B + S * B_BYTES;
+  static constexpr int SMEM_SFA = SMEM_B + S * BB;
   static constexpr int SMEM_SFB = SMEM_SFA + SF_SLOTS * SFA_MAX;
   static constexpr int SMEM_OUT = SMEM_SFB + SF_SLOTS * SFB_MAX;
   static constexpr int SMEM_BAR = SMEM_OUT + NUM_EPI_WARPS * STAGE_BYTES;
@@ -96,6 +102,8 @@ struct Plan {
 };
 using PlanShortK = Plan<3, 64>;
 using PlanLongK = Plan<4, 16>;
+// CTA pair: each CTA holds half of B, so five stages fit beside wide output blocks
+using PlanPair = Plan<5, 64, B_BYTES / 2>;
 
 constexpr long long WAIT_LIMIT_CYCLES = 4000000000LL;  // ~2 s at 2 GHz
 
@@ -250,6 +258,54 @@ __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a_desc, uint64_
   }
 }
 
+// ---- CTA pair (cta_group::2) ----------------------------------------------
+// Address of the same shared-memory object in cluster CTA `rank`.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+// Arrive on an mbarrier given by its cluster address (own or peer CTA).
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+// TMA load into this CTA's shared memory whose byte count completes on the
+// mbarrier at cluster address `bar`, which may sit in the peer CTA of the pair.
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, "
+      "%4}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
+      : "memory");
+}
+// Arrive on the mbarrier at `bar` in both CTAs of the pair once the pair's
+// prior tcgen05 operations issued by this thread have completed.
+__device__ __forceinline__ void tc_commit_pair(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+      "h"((uint16_t)3)
+      : "memory");
+}
+template <bool MX>
+__device__ __forceinline__ void tc_mma_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  if constexpr (MX) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+            d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+  } else {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+            d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+  }
+}
+
 #define TC_LD32(taddr, r)                                                                                          \
   asm volatile(                                                                                                    \
       "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18," \
@@ -295,6 +351,70 @@ struct Params {
   int M, N, K;
   int32_t* status;
 };
+
+// Epilogue of one warp: 32 accumulator rows (row0.., one per lane) x 64
+// columns held in r, scaled by alpha, converted, staged in shared memory as
+// 32-row blocks of PL::OUT_ROW_BYTES-byte rows and written by TMA stores.
+template <bool BF16, class PL>
+__device__ __forceinline__ void store_block(const uint32_t (&r)[2][32], float alpha, uint8_t* stage_buf,
+                                            uint32_t stage_addr, const CUtensorMap* tmap_c, int row0, int col0,
+                                            int lane) {
+  constexpr int OB = PL::OUT_ROW_BYTES;
+  constexpr int BLK_COLS = OB / (BF16 ? 2 : 4);  // columns per staged row
+  constexpr int VECS = OB / 16;                  // 16-byte vectors per staged row
+#pragma unroll
+  for (int b = 0; b < EPI_COLS / BLK_COLS; ++b) {
+    uint32_t w[4 * VECS];
+    if constexpr (BF16) {
+#pragma unroll
+      for (int i = 0; i < 2 * VECS * 2; ++i) {
+        const int c = BLK_COLS * b + 2 * i;
+        const float x0 = __fmul_rn(__uint_as_float(r[c >> 5][c & 31]), alpha);
+        const float x1 = __fmul_rn(__uint_as_float(r[c >> 5][(c & 31) + 1]), alpha);
+        const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
+        w[i] = *reinterpret_cast<const uint32_t*>(&h);
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 4 * VECS; ++i) {
+        const int c = BLK_COLS * b + i;
+        w[i] = __float_as_uint(__fmul_rn(__uint_as_float(r[c >> 5][c & 31]), alpha));
+      }
+    }
+    // the previous block's store must have read the staging buffer
+    if (lane == 0) bulk_wait_read0();
+    __syncwarp();
+    // row `lane`; with 64-byte rows, 16-byte chunk v goes to chunk
+    // v ^ ((lane >> 1) & 3), the 64-byte swizzle the output map declares
+#pragma unroll
+    for (int v = 0; v < VECS; ++v) {
+      const int pc = VECS == 4 ? (v ^ ((lane >> 1) & 3)) : v;
+      *reinterpret_cast<uint4*>(stage_buf + lane * OB + pc * 16) =
+          make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
+    }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    __syncwarp();
+    if (lane == 0) {
+      tma_store_2d(tmap_c, stage_addr, col0 + BLK_COLS * b, row0);
+      bulk_commit();
+    }
+  }
+}
+
+// Epilogue scale of the accumulator: alpha = 1 / (s_encA * s_encB), times
+// 2^(tA + tB) for UE5M3 (1 for MXFP4).
+template <int FMT>
+__device__ __forceinline__ float epilogue_alpha(const Params& p) {
+  float alpha = 1.0f;
+  if constexpr (FMT != fp4dev::SF_E8M0) {
+    constexpr int SFMT = FMT == fp4dev::SF_UE5M3 ? fp4dev::SF_E4M3 : FMT;
+    const float sa = fp4dev::global_encode_scale<SFMT>(__ldg(p.ga), nullptr);
+    const float sb = fp4dev::global_encode_scale<SFMT>(__ldg(p.gb), nullptr);
+    alpha = __fdiv_rn(1.0f, __fmul_rn(sa, sb));
+    if (FMT == fp4dev::SF_UE5M3) alpha = ldexpf(alpha, __ldg(p.tA) + __ldg(p.tB));
+  }
+  return alpha;
+}
 
 // CM CTAs of a cluster take CM consecutive M tiles of the same N tile: each
 // loads its own A tile and 1/CM of the shared B tile (and of its scales),
@@ -564,14 +684,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int ew = warp - FIRST_EPI_WARP;  // 0..15
     const int quarter = warp & 3;          // tensor-memory lanes this warp may access
     const int cblk = ew >> 2;              // 64-column block of the accumulator
-    float alpha = 1.0f;
-    if constexpr (!MX) {
-      constexpr int SFMT = FMT == fp4dev::SF_UE5M3 ? fp4dev::SF_E4M3 : FMT;
-      const float sa = fp4dev::global_encode_scale<SFMT>(__ldg(p.ga), nullptr);
-      const float sb = fp4dev::global_encode_scale<SFMT>(__ldg(p.gb), nullptr);
-      alpha = __fdiv_rn(1.0f, __fmul_rn(sa, sb));
-      if (FMT == fp4dev::SF_UE5M3) alpha = ldexpf(alpha, __ldg(p.tA) + __ldg(p.tB));
-    }
+    const float alpha = epilogue_alpha<FMT>(p);
     uint8_t* stage_buf = smem + SMEM_OUT + ew * STAGE_BYTES;
     const uint32_t stage_addr = smem_u32(stage_buf);
     uint32_t acc_phase = 0;
@@ -588,48 +701,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_acc_empty);
-      const int row0 = mt * BM + 32 * quarter;
-      const int col0 = nt * BN + EPI_COLS * cblk;
-      constexpr int OB = PL::OUT_ROW_BYTES;
-      constexpr int BLK_COLS = OB / (BF16 ? 2 : 4);  // columns per staged row
-      constexpr int VECS = OB / 16;                  // 16-byte vectors per staged row
-#pragma unroll
-      for (int b = 0; b < EPI_COLS / BLK_COLS; ++b) {
-        uint32_t w[4 * VECS];
-        if constexpr (BF16) {
-#pragma unroll
-          for (int i = 0; i < 2 * VECS * 2; ++i) {
-            const int c = BLK_COLS * b + 2 * i;
-            const float x0 = __fmul_rn(__uint_as_float(r[c >> 5][c & 31]), alpha);
-            const float x1 = __fmul_rn(__uint_as_float(r[c >> 5][(c & 31) + 1]), alpha);
-            const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
-            w[i] = *reinterpret_cast<const uint32_t*>(&h);
-          }
-        } else {
-#pragma unroll
-          for (int i = 0; i < 4 * VECS; ++i) {
-            const int c = BLK_COLS * b + i;
-            w[i] = __float_as_uint(__fmul_rn(__uint_as_float(r[c >> 5][c & 31]), alpha));
-          }
-        }
-        // the previous block's store must have read the staging buffer
-        if (lane == 0) bulk_wait_read0();
-        __syncwarp();
-        // row `lane`; with 64-byte rows, 16-byte chunk v goes to chunk
-        // v ^ ((lane >> 1) & 3), the 64-byte swizzle the output map declares
-#pragma unroll
-        for (int v = 0; v < VECS; ++v) {
-          const int pc = VECS == 4 ? (v ^ ((lane >> 1) & 3)) : v;
-          *reinterpret_cast<uint4*>(stage_buf + lane * OB + pc * 16) =
-              make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
-        }
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        __syncwarp();
-        if (lane == 0) {
-          tma_store_2d(&tmap_c, stage_addr, col0 + BLK_COLS * b, row0);
-          bulk_commit();
-        }
-      }
+      store_block<BF16, PL>(r, alpha, stage_buf, stage_addr, &tmap_c, mt * BM + 32 * quarter,
+                            nt * BN + EPI_COLS * cblk, lane);
     }
     if (lane == 0) bulk_wait0();
     __syncwarp();
@@ -643,6 +716,311 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   if (warp == 1) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS)
+                 : "memory");
+  }
+}
+
+// CTA-pair form: a cluster of 2 CTAs computes a 256 x 256 output tile with
+// cta_group::2 MMAs (M = 256).  CTA r (r = 0, 1) holds rows 128r..128r+127 of
+// the A tile and of the B tile in its shared memory and rows 128r.. of the
+// accumulator in its tensor memory; the MMA of the even CTA reads both CTAs'
+// operands, so each SM streams A + B/2 per K step instead of A + B.  Roles
+// as in k_gemm_fp4, with the pair's hand-offs:
+//   * both producers' TMA loads complete on the even CTA's full[] barrier,
+//     whose expect_tx covers both CTAs' bytes;
+//   * the even CTA's MMA thread waits for full[] and for sf[] (scale writers
+//     of both CTAs), issues the MMAs and commits to empty[] / acc_full in both
+//     CTAs at once;
+//   * each CTA's scale writers fill its own tensor memory: its 128 rows of A
+//     scales and all 256 rows of B scales (each SM applies the B scales of
+//     the whole tile to its half of the product);
+//   * both CTAs' epilogue warps drain their own accumulator rows and release
+//     them on the even CTA's acc_empty.
+template <int FMT, bool BF16, class PL>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    k_gemm_fp4_pair(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
+                    const __grid_constant__ CUtensorMap tmap_c, Params p) {
+  constexpr bool MX = FMT == fp4dev::SF_E8M0;
+  constexpr int ATOMS = MX ? 2 : 4;
+  constexpr int SFA_BYTES = 512 * ATOMS;
+  constexpr int SFB_HALF = SFA_BYTES;
+  constexpr int PM = 2 * BM;  // rows of the pair's output tile
+  constexpr int B_STAGE = PL::B_STAGE;
+  static_assert(B_STAGE == B_BYTES / 2, "each CTA holds half of the B tile");
+  constexpr uint32_t IDESC = make_idesc(PM, BN, MX);
+  constexpr int STAGES = PL::STAGES;
+  constexpr int SMEM_A = PL::SMEM_A, SMEM_B = PL::SMEM_B, SMEM_SFA = PL::SMEM_SFA, SMEM_SFB = PL::SMEM_SFB;
+  constexpr int SMEM_OUT = PL::SMEM_OUT, SMEM_BAR = PL::SMEM_BAR, STAGE_BYTES = PL::STAGE_BYTES;
+  constexpr uint32_t TMEM_COLS = PL::TMEM_COLS, TMEM_SFA = PL::TMEM_SFA, TMEM_SFB = PL::TMEM_SFB;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bar_full = sbase + SMEM_BAR;
+  const uint32_t bar_sf = bar_full + 8 * STAGES;
+  const uint32_t bar_empty = bar_sf + 8 * STAGES;
+  const uint32_t bar_sfd_full = bar_empty + 8 * STAGES;
+  const uint32_t bar_sfd_empty = bar_sfd_full + 8 * SF_SLOTS;
+  const uint32_t bar_acc_full = bar_sfd_empty + 8 * SF_SLOTS;
+  const uint32_t bar_acc_empty = bar_acc_full + 8;
+  constexpr int BAR_BYTES = 8 * (3 * STAGES + 2 * SF_SLOTS + 2);
+  static_assert(BAR_BYTES + 16 <= 256, "barrier area");
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + SMEM_BAR + BAR_BYTES);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + SMEM_BAR + BAR_BYTES + 8);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t crank = cluster_rank();  // 0: issues the MMAs; 1: its peer
+  const bool leader = crank == 0;
+  const int m_pairs = p.M / PM, n_tiles = p.N / BN;
+  const int num_units = m_pairs * n_tiles;
+  const int cluster_id = blockIdx.x >> 1, num_clusters = gridDim.x >> 1;
+  const int k_steps = p.K / BK;
+  const int64_t sf_row_stride = (int64_t)(p.K / (MX ? 32 : 16)) / 4 * 512;  // bytes per 128-row slab
+  // the even CTA's barriers that the peer signals, as cluster addresses
+  const uint32_t lead_full = mapa_shared(bar_full, 0);
+  const uint32_t lead_sf = mapa_shared(bar_sf, 0);
+  const uint32_t lead_acc_empty = mapa_shared(bar_acc_empty, 0);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(bar_full + 8 * s, 1);
+      mbar_init(bar_sf + 8 * s, 2 * NUM_SF_WARPS);
+      mbar_init(bar_empty + 8 * s, 1);
+    }
+    for (int s = 0; s < SF_SLOTS; ++s) {
+      mbar_init(bar_sfd_full + 8 * s, 1);
+      mbar_init(bar_sfd_empty + 8 * s, NUM_SF_WARPS);
+    }
+    mbar_init(bar_acc_full, 1);
+    mbar_init(bar_acc_empty, 2 * NUM_EPI_WARPS);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  if (warp == 1) {
+    // one warp of each CTA of the pair allocates, together, the same columns in both
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                 "r"(TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();  // both CTAs' barriers and tensor memory exist before any cross-CTA traffic
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  if (threadIdx.x == 0) {
+    // the MMA addresses the peer's tensor memory with the even CTA's column base
+    uint32_t peer_base;
+    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(peer_base) : "r"(mapa_shared(smem_u32(tmem_slot), crank ^ 1u)));
+    if (peer_base != tmem_base) {
+      *abort_flag = 1;
+      fp4dev::set_status(p.status, FP4_ERR_CUDA);
+    }
+  }
+  __syncthreads();
+  const bool run = *abort_flag == 0;
+
+  if (warp == 0) {
+    // ------------------------------ producer ------------------------------
+    if (lane == 0 && run) {
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_a)) : "memory");
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_b)) : "memory");
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int u = cluster_id; u < num_units && ok; u += num_clusters) {
+        const int mp = u % m_pairs, nt = u / m_pairs;
+        for (int ks = 0; ks < k_steps; ++ks) {
+          if (!wait_bounded(bar_empty + 8 * stage, phase ^ 1u, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          if (leader) mbar_expect_tx(bar_full + 8 * stage, 2 * (A_BYTES + B_STAGE));
+          const uint32_t fb = lead_full + 8 * stage;
+          tma_load_2d_pair(sbase + SMEM_A + stage * A_BYTES, &tmap_a, fb, ks * (BK / 2), mp * PM + BM * (int)crank);
+          tma_load_2d_pair(sbase + SMEM_B + stage * B_STAGE, &tmap_b, fb, ks * (BK / 2),
+                           nt * BN + (BN / 2) * (int)crank);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------ MMA issuer (even CTA) -----------------
+    if (lane == 0 && leader && run) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      int iter = 0;
+      for (int u = cluster_id; u < num_units && ok; u += num_clusters, ++iter) {
+        if (iter > 0) {
+          if (!wait_bounded(bar_acc_empty, acc_phase ^ 1u, abort_flag, p.status)) break;
+          tc_fence_after();
+        }
+        for (int ks = 0; ks < k_steps; ++ks) {
+          if (!wait_bounded(bar_sf + 8 * stage, phase, abort_flag, p.status) ||
+              !wait_bounded(bar_full + 8 * stage, phase, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sfa_t = tmem_base + TMEM_SFA + 16 * stage;
+          const uint32_t sfb_t = tmem_base + TMEM_SFB + 32 * stage;
+          const uint32_t a_smem = sbase + SMEM_A + stage * A_BYTES;
+          const uint32_t b_smem = sbase + SMEM_B + stage * B_STAGE;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const uint64_t ad = smem_desc(a_smem + 32 * j, 0, 1024, 2);
+            const uint64_t bd = smem_desc(b_smem + 32 * j, 0, 1024, 2);
+            uint32_t idesc = IDESC;
+            uint32_t sfa_col = sfa_t + 4 * j, sfb_col = sfb_t + 8 * j;
+            if constexpr (MX) {
+              sfa_col = sfa_t + 4 * (j >> 1);
+              sfb_col = sfb_t + 8 * (j >> 1);
+              const uint32_t id = (j & 1) ? 2u : 0u;
+              idesc |= (id << 29) | (id << 4);
+            }
+            tc_mma_pair<MX>(tmem_base, ad, bd, idesc, sfa_col, sfb_col, (ks > 0 || j > 0) ? 1u : 0u);
+          }
+          tc_commit_pair(bar_empty + 8 * stage);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        tc_commit_pair(bar_acc_full);
+        acc_phase ^= 1u;
+      }
+    }
+    __syncwarp();
+  } else if (warp == SF_PRODUCER_WARP) {
+    // ------------------------------ scale producer ------------------------
+    if (lane == 0 && run) {
+      int slot = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int u = cluster_id; u < num_units && ok; u += num_clusters) {
+        const int mp = u % m_pairs, nt = u / m_pairs;
+        const int a_slab = 2 * mp + (int)crank;
+        for (int ks = 0; ks < k_steps; ++ks) {
+          if (!wait_bounded(bar_sfd_empty + 8 * slot, phase ^ 1u, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          const uint32_t sb = bar_sfd_full + 8 * slot;
+          mbar_expect_tx(sb, SFA_BYTES + 2 * SFB_HALF);
+          bulk_load(sbase + SMEM_SFA + slot * SFA_MAX, p.As + a_slab * sf_row_stride + (int64_t)ks * SFA_BYTES,
+                    SFA_BYTES, sb);
+          bulk_load(sbase + SMEM_SFB + slot * SFB_MAX, p.Bs + (2 * nt) * sf_row_stride + (int64_t)ks * SFB_HALF,
+                    SFB_HALF, sb);
+          bulk_load(sbase + SMEM_SFB + slot * SFB_MAX + SFB_HALF,
+                    p.Bs + (2 * nt + 1) * sf_row_stride + (int64_t)ks * SFB_HALF, SFB_HALF, sb);
+          if (++slot == SF_SLOTS) {
+            slot = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp < FIRST_EPI_WARP) {
+    // ------------------------------ scale writers -------------------------
+    const int quarter = warp & 3;
+    int stage = 0, slot = 0;
+    uint32_t phase = 0, sphase = 0;
+    for (int u = cluster_id; u < num_units && run; u += num_clusters) {
+      bool ok = true;
+      for (int ks = 0; ks < k_steps; ++ks) {
+        if (!wait_bounded(bar_sfd_full + 8 * slot, sphase, abort_flag, p.status)) {
+          ok = false;
+          break;
+        }
+        const uint8_t* sfa = smem + SMEM_SFA + slot * SFA_MAX + 16 * lane;
+        const uint8_t* sfb = smem + SMEM_SFB + slot * SFB_MAX + 16 * lane;
+        uint32_t va[4 * ATOMS], vb[8 * ATOMS];
+#pragma unroll
+        for (int j = 0; j < ATOMS; ++j) {
+          const uint4 a = *reinterpret_cast<const uint4*>(sfa + 512 * j);
+          const uint4 b0 = *reinterpret_cast<const uint4*>(sfb + 512 * j);
+          const uint4 b1 = *reinterpret_cast<const uint4*>(sfb + SFB_HALF + 512 * j);
+          va[4 * j + 0] = a.x; va[4 * j + 1] = a.y; va[4 * j + 2] = a.z; va[4 * j + 3] = a.w;
+          vb[8 * j + 0] = b0.x; vb[8 * j + 1] = b0.y; vb[8 * j + 2] = b0.z; vb[8 * j + 3] = b0.w;
+          vb[8 * j + 4] = b1.x; vb[8 * j + 5] = b1.y; vb[8 * j + 6] = b1.z; vb[8 * j + 7] = b1.w;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_sfd_empty + 8 * slot);
+        // this CTA's columns of the stage are free once the pair's MMAs of
+        // K step k - STAGES have completed (their commit reaches both CTAs)
+        if (!wait_bounded(bar_empty + 8 * stage, phase ^ 1u, abort_flag, p.status)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t lane_base = tmem_base + ((uint32_t)(32 * quarter) << 16);
+        if constexpr (ATOMS == 4) {
+          tc_st16(lane_base + TMEM_SFA + 16 * stage, va);
+          tc_st32(lane_base + TMEM_SFB + 32 * stage, vb);
+        } else {
+          tc_st8(lane_base + TMEM_SFA + 16 * stage, va);
+          tc_st16(lane_base + TMEM_SFB + 32 * stage, vb);
+        }
+        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(lead_sf + 8 * stage);
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+        if (++slot == SF_SLOTS) {
+          slot = 0;
+          sphase ^= 1u;
+        }
+      }
+      if (!ok) break;
+    }
+  } else {
+    // ------------------------------ epilogue ------------------------------
+    const int ew = warp - FIRST_EPI_WARP;
+    const int quarter = warp & 3;
+    const int cblk = ew >> 2;
+    const float alpha = epilogue_alpha<FMT>(p);
+    uint8_t* stage_buf = smem + SMEM_OUT + ew * STAGE_BYTES;
+    const uint32_t stage_addr = smem_u32(stage_buf);
+    uint32_t acc_phase = 0;
+    for (int u = cluster_id; u < num_units && run; u += num_clusters) {
+      const int mp = u % m_pairs, nt = u / m_pairs;
+      if (!wait_bounded(bar_acc_full, acc_phase, abort_flag, p.status)) break;
+      acc_phase ^= 1u;
+      tc_fence_after();
+      uint32_t r[2][32];
+      const uint32_t t0 = tmem_base + ((uint32_t)(32 * quarter) << 16) + EPI_COLS * cblk;
+      TC_LD32(t0, r[0]);
+      TC_LD32(t0 + 32, r[1]);
+      asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(lead_acc_empty);
+      store_block<BF16, PL>(r, alpha, stage_buf, stage_addr, &tmap_c, mp * PM + BM * (int)crank + 32 * quarter,
+                            nt * BN + EPI_COLS * cblk, lane);
+    }
+    if (lane == 0) bulk_wait0();
+    __syncwarp();
+  }
+
+  // ------------------------------ teardown --------------------------------
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();  // no more MMAs, TMA completions or arrivals between the two CTAs
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS)
                  : "memory");
   }
 }
@@ -755,6 +1133,56 @@ cudaError_t launch_t(const fp4lib::GemmArgs& a, cudaStream_t st) {
   return cudaLaunchKernelEx(&cfg, kern, ma, mb, mc, p);
 }
 
+// CTA-pair launch: clusters of 2 CTAs, one 256 x 256 output tile per cluster
+// and round.
+template <int FMT, bool BF16>
+cudaError_t launch_pair(const fp4lib::GemmArgs& a, cudaStream_t st) {
+  using PL = PlanPair;
+  auto kern = k_gemm_fp4_pair<FMT, BF16, PL>;
+  constexpr int SMEM_LAUNCH = PL::SMEM_LAUNCH;
+  static bool attr_set = false;
+  static int max_clusters = 0;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = SMEM_LAUNCH;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_LAUNCH);
+    if (e != cudaSuccess) return e;
+    cfg.gridDim = dim3(sm_count() & ~1, 1, 1);
+    e = cudaOccupancyMaxActiveClusters(&max_clusters, kern, &cfg);
+    if (e != cudaSuccess) return e;
+    if (max_clusters <= 0) return cudaErrorInvalidConfiguration;
+    attr_set = true;
+  }
+  CUtensorMap ma, mb, mc;
+  if (!make_code_map(&ma, a.Aq, a.M, a.K / 2, BM) || !make_code_map(&mb, a.Bq, a.N, a.K / 2, BN / 2) ||
+      !make_out_map(&mc, a.C, a.M, a.N, a.ldc, BF16, PL::OUT_ROW_BYTES))
+    return cudaErrorInvalidValue;
+  Params p;
+  p.As = a.As;
+  p.Bs = a.Bs;
+  p.ga = a.ga;
+  p.gb = a.gb;
+  p.tA = a.tA;
+  p.tB = a.tB;
+  p.M = (int)a.M;
+  p.N = (int)a.N;
+  p.K = (int)a.K;
+  p.status = a.status;
+  const int units = (int)((a.M / (2 * BM)) * (a.N / BN));
+  const int clusters = units < max_clusters ? units : max_clusters;
+  cfg.gridDim = dim3((unsigned)(2 * clusters), 1, 1);
+  return cudaLaunchKernelEx(&cfg, kern, ma, mb, mc, p);
+}
+
 // Cluster size along M.  Multicasting the B tile halves or quarters the
 // L2 -> SM bytes per K step, but on the 7B shapes it measured no faster
 // (2 CTAs) or slower (4 CTAs: fewer co-resident clusters) than independent
@@ -764,6 +1192,7 @@ constexpr int GEMM_CLUSTER_M = 1;
 template <int FMT, bool BF16>
 cudaError_t launch_cm(const fp4lib::GemmArgs& a, cudaStream_t st) {
   const int64_t m_tiles = a.M / BM;
+  if (m_tiles % 2 == 0) return launch_pair<FMT, BF16>(a, st);
   const bool long_k = a.K >= 8192;
   if (GEMM_CLUSTER_M == 2 && m_tiles % 2 == 0)
     return long_k ? launch_t<FMT, BF16, 2, PlanLongK>(a, st) : launch_t<FMT, BF16, 2, PlanShortK>(a, st);

@@ -138,9 +138,22 @@ def test_config3_fwd_dgrad_wgrad_scaled():
 
 @pytest.mark.parametrize("fmt", ["E4M3", "E8M0"])
 def test_long_k_plan(fmt):
-    # K >= 8192 takes the deeper 4-stage ring with 16-byte output blocks
+    # long K on CTA pairs (M = 256: one 256-row pair tile)
     A = synth.normal((256, 8192), 23, 0, outlier_p=0.01, outlier_mult=50.0)
     B = synth.normal((512, 8192), 23, 1, std=0.02)
+    qa, qb = oracle_q(A, fmt), oracle_q(B, fmt)
+    C, S = Gm.gemm_ref(qa["codes"], qa["scales"], qa["amax"], qb["codes"], qb["scales"], qb["amax"], fmt)
+    check_bound(gpu_gemm(qa, qb, fmt), C, S)
+    check_bound(gpu_gemm(qa, qb, fmt, "bf16"), C, S, bf16=True)
+
+
+@pytest.mark.parametrize("fmt,K", [("E4M3", 512), ("E8M0", 512), ("E4M3", 8192), ("E8M0", 8192)])
+def test_single_cta_tiles(fmt, K):
+    # M = 384 is an odd number of 128-row tiles, so the GEMM runs one CTA per
+    # 128 x 256 tile instead of CTA pairs on 256 x 256 tiles (K >= 8192: the
+    # 4-stage ring with 16-byte output blocks)
+    A = synth.normal((384, K), 24, 0, outlier_p=0.01, outlier_mult=50.0)
+    B = synth.normal((512, K), 24, 1, std=0.02)
     qa, qb = oracle_q(A, fmt), oracle_q(B, fmt)
     C, S = Gm.gemm_ref(qa["codes"], qa["scales"], qa["amax"], qb["codes"], qb["scales"], qb["amax"], fmt)
     check_bound(gpu_gemm(qa, qb, fmt), C, S)
