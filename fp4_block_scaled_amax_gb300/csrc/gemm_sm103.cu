@@ -44,7 +44,9 @@
 //                (512 bytes per warp, which leaves room for a 4-stage ring), and
 //                writes them with TMA bulk-tensor stores.
 // Every mbarrier wait is bounded: on expiry the CTA records FP4_ERR_TIMEOUT in
-// the status word and winds down instead of spinning.
+// the status word and winds down instead of spinning.  Once aborted, the
+// producers issue no further copies, and the CTA waits a fixed ~10 ms for
+// copies already in flight before it frees its tensor memory and exits.
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -106,6 +108,10 @@ using PlanLongK = Plan<4, 16>;
 using PlanPair = Plan<5, 64, B_BYTES / 2>;
 
 constexpr long long WAIT_LIMIT_CYCLES = 4000000000LL;  // ~2 s at 2 GHz
+// After an abort, copies issued before it may still be landing in shared
+// memory (or completing on a barrier); the CTA waits this long (~10 ms, far
+// beyond a copy's latency) before it frees tensor memory and exits.
+constexpr long long DRAIN_CYCLES = 20000000LL;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -148,6 +154,24 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, vola
       return false;
     }
   }
+}
+
+__device__ __forceinline__ void drain_after_abort(volatile int* abort_flag) {
+  if (threadIdx.x == 0 && *abort_flag) {
+    const long long t0 = clock64();
+    while (clock64() - t0 < DRAIN_CYCLES) {
+    }
+  }
+  __syncthreads();
+}
+
+// Bounded wait by lane 0 of a converged warp; the outcome is broadcast so the
+// warp stays converged.
+__device__ __forceinline__ bool wait_lane0(uint32_t bar, uint32_t parity, volatile int* abort_flag, int32_t* status,
+                                           int lane) {
+  int ok = 0;
+  if (lane == 0) ok = wait_bounded(bar, parity, abort_flag, status) ? 1 : 0;
+  return __shfl_sync(0xFFFFFFFFu, ok, 0) != 0;
 }
 
 // ---- TMA / bulk copies ----------------------------------------------------
@@ -283,6 +307,35 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
 __device__ __forceinline__ void tc_commit_pair(uint32_t bar) {
   asm volatile(
       "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+      "h"((uint16_t)3)
+      : "memory");
+}
+// The same, issued by one elected lane of a converged warp (the warp's
+// operands stay warp-uniform).
+template <bool MX>
+__device__ __forceinline__ void tc_mma_pair_elect(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                                  uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  if constexpr (MX) {
+    asm volatile(
+        "{\n\t.reg .pred p, e;\n\tsetp.ne.b32 p, %6, 0;\n\telect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+            d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+  } else {
+    asm volatile(
+        "{\n\t.reg .pred p, e;\n\tsetp.ne.b32 p, %6, 0;\n\telect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+            d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+  }
+}
+__device__ __forceinline__ void tc_commit_pair_elect(uint32_t bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;\n\t}" ::"r"(
+          bar),
       "h"((uint16_t)3)
       : "memory");
 }
@@ -503,7 +556,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int mt = (u % m_groups) * CM + crank, nt = u / m_groups;
         for (int ks = 0; ks < k_steps; ++ks) {
           // own stage free in every cluster CTA (the B slice lands in all of them)
-          if (!wait_bounded(bar_empty + 8 * stage, phase ^ 1u, abort_flag, p.status)) {
+          if (!wait_bounded(bar_empty + 8 * stage, phase ^ 1u, abort_flag, p.status) || *abort_flag) {
             ok = false;
             break;
           }
@@ -591,7 +644,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       for (int u = cluster_id; u < num_units && ok; u += num_clusters) {
         const int mt = (u % m_groups) * CM + crank, nt = u / m_groups;
         for (int ks = 0; ks < k_steps; ++ks) {
-          if (!wait_bounded(bar_sfd_empty + 8 * slot, phase ^ 1u, abort_flag, p.status)) {
+          if (!wait_bounded(bar_sfd_empty + 8 * slot, phase ^ 1u, abort_flag, p.status) || *abort_flag) {
             ok = false;
             break;
           }
@@ -711,6 +764,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   // ------------------------------ teardown --------------------------------
   tc_fence_before();
   __syncthreads();
+  drain_after_abort(abort_flag);
   // no CTA leaves while a peer may still multicast into it or arrive on it
   if constexpr (CM > 1) cluster_sync_all();
   if (warp == 1) {
@@ -772,19 +826,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const uint32_t crank = cluster_rank();  // 0: issues the MMAs; 1: its peer
   const bool leader = crank == 0;
   const int m_pairs = p.M / PM, n_tiles = p.N / BN;
+  // units walk N fastest: the clusters of one round share a few 256-row
+  // blocks of A and sweep B, which keeps a round's operands within L2 even
+  // when A alone approaches its size (dgrad, wgrad)
   const int num_units = m_pairs * n_tiles;
   const int cluster_id = blockIdx.x >> 1, num_clusters = gridDim.x >> 1;
   const int k_steps = p.K / BK;
   const int64_t sf_row_stride = (int64_t)(p.K / (MX ? 32 : 16)) / 4 * 512;  // bytes per 128-row slab
   // the even CTA's barriers that the peer signals, as cluster addresses
   const uint32_t lead_full = mapa_shared(bar_full, 0);
-  const uint32_t lead_sf = mapa_shared(bar_sf, 0);
   const uint32_t lead_acc_empty = mapa_shared(bar_acc_empty, 0);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(bar_full + 8 * s, 1);
-      mbar_init(bar_sf + 8 * s, 2 * NUM_SF_WARPS);
+      // one arrival with the expected bytes of both CTAs' code tiles, plus one
+      // per scale-writer warp of both CTAs
+      mbar_init(bar_full + 8 * s, 1 + 2 * NUM_SF_WARPS);
+      mbar_init(bar_sf + 8 * s, 1);  // unused in the pair form
       mbar_init(bar_empty + 8 * s, 1);
     }
     for (int s = 0; s < SF_SLOTS; ++s) {
@@ -830,9 +888,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       uint32_t phase = 0;
       bool ok = true;
       for (int u = cluster_id; u < num_units && ok; u += num_clusters) {
-        const int mp = u % m_pairs, nt = u / m_pairs;
+        const int mp = u / n_tiles, nt = u % n_tiles;
         for (int ks = 0; ks < k_steps; ++ks) {
-          if (!wait_bounded(bar_empty + 8 * stage, phase ^ 1u, abort_flag, p.status)) {
+          if (!wait_bounded(bar_empty + 8 * stage, phase ^ 1u, abort_flag, p.status) || *abort_flag) {
             ok = false;
             break;
           }
@@ -851,7 +909,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------ MMA issuer (even CTA) -----------------
-    if (lane == 0 && leader && run) {
+    // The whole warp runs the loop (its operands stay warp-uniform); one
+    // elected lane issues each tcgen05 instruction.
+    if (leader && run) {
       int stage = 0;
       uint32_t phase = 0;
       uint32_t acc_phase = 0;
@@ -859,12 +919,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       int iter = 0;
       for (int u = cluster_id; u < num_units && ok; u += num_clusters, ++iter) {
         if (iter > 0) {
-          if (!wait_bounded(bar_acc_empty, acc_phase ^ 1u, abort_flag, p.status)) break;
+          if (!wait_lane0(bar_acc_empty, acc_phase ^ 1u, abort_flag, p.status, lane)) break;
           tc_fence_after();
         }
         for (int ks = 0; ks < k_steps; ++ks) {
-          if (!wait_bounded(bar_sf + 8 * stage, phase, abort_flag, p.status) ||
-              !wait_bounded(bar_full + 8 * stage, phase, abort_flag, p.status)) {
+          // codes of both CTAs landed and both CTAs' scales written
+          if (!wait_lane0(bar_full + 8 * stage, phase, abort_flag, p.status, lane)) {
             ok = false;
             break;
           }
@@ -885,16 +945,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               const uint32_t id = (j & 1) ? 2u : 0u;
               idesc |= (id << 29) | (id << 4);
             }
-            tc_mma_pair<MX>(tmem_base, ad, bd, idesc, sfa_col, sfb_col, (ks > 0 || j > 0) ? 1u : 0u);
+            tc_mma_pair_elect<MX>(tmem_base, ad, bd, idesc, sfa_col, sfb_col, (ks > 0 || j > 0) ? 1u : 0u);
           }
-          tc_commit_pair(bar_empty + 8 * stage);
+          tc_commit_pair_elect(bar_empty + 8 * stage);
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
           }
         }
         if (!ok) break;
-        tc_commit_pair(bar_acc_full);
+        tc_commit_pair_elect(bar_acc_full);
         acc_phase ^= 1u;
       }
     }
@@ -906,10 +966,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       uint32_t phase = 0;
       bool ok = true;
       for (int u = cluster_id; u < num_units && ok; u += num_clusters) {
-        const int mp = u % m_pairs, nt = u / m_pairs;
+        const int mp = u / n_tiles, nt = u % n_tiles;
         const int a_slab = 2 * mp + (int)crank;
         for (int ks = 0; ks < k_steps; ++ks) {
-          if (!wait_bounded(bar_sfd_empty + 8 * slot, phase ^ 1u, abort_flag, p.status)) {
+          if (!wait_bounded(bar_sfd_empty + 8 * slot, phase ^ 1u, abort_flag, p.status) || *abort_flag) {
             ok = false;
             break;
           }
@@ -973,7 +1033,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive_cluster(lead_sf + 8 * stage);
+        if (lane == 0) mbar_arrive_cluster(lead_full + 8 * stage);
         if (++stage == STAGES) {
           stage = 0;
           phase ^= 1u;
@@ -995,7 +1055,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t stage_addr = smem_u32(stage_buf);
     uint32_t acc_phase = 0;
     for (int u = cluster_id; u < num_units && run; u += num_clusters) {
-      const int mp = u % m_pairs, nt = u / m_pairs;
+      const int mp = u / n_tiles, nt = u % n_tiles;
       if (!wait_bounded(bar_acc_full, acc_phase, abort_flag, p.status)) break;
       acc_phase ^= 1u;
       tc_fence_after();
@@ -1017,6 +1077,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   // ------------------------------ teardown --------------------------------
   tc_fence_before();
   __syncthreads();
+  drain_after_abort(abort_flag);
   cluster_sync_all();  // no more MMAs, TMA completions or arrivals between the two CTAs
   if (warp == 1) {
     tc_fence_after();
