@@ -55,7 +55,7 @@ FP4_PER_BF16 = 6.0  # nominal dense FP4 / bf16 tensor ratio on GB300 (13.5 / 2.2
 # quantizations, captured at 8192 tokens and scaled by the rows processed
 # (streaming kernel: X and dY scale with tokens, W does not).  The GEMM's
 # traffic does not scale in proportion with tokens and is reported as null.
-NCU_TRAFFIC = {"quant_dual": {"bytes": 687.5e6, "src": "b63730b6d234c550",
+NCU_TRAFFIC = {"quant_dual": {"bytes": 698.0e6, "src": "2fa66c14db1d343f",
                               "files": ["quantize.cu", "fp4_device.cuh"]}}
 
 
