@@ -46,6 +46,7 @@ import torch  # noqa: E402
 
 M_TOK, K_HID, N_FFN = 16384, 4096, 11008
 GEMV_BATCH = 8
+CPU_SAMPLE_TOKENS, CPU_SAMPLE_FEATURES = 4096, 4096  # oracle slice timed for cpu_baseline (~10-20 s of CPU work)
 STEP_FLOPS = 3 * 2 * M_TOK * N_FFN * K_HID
 WORKLOAD = "llama2-7b-mlp-linear-fwd-bwd"
 METRIC = "NVFP4 GEMM TFLOPS & quantize GB/s at 7B shapes, % of FP4-MMA/HBM peak"
@@ -272,6 +273,44 @@ class LinearStep:
         mark(10)
 
 
+def quantizer_modes(step, flush, reps=5):
+    """Given-amax quantizer of dY (the step's largest tensor) in each mode, timed
+    alone with CUDA events after an L2 flush: row or transposed layout at
+    2.5625 B/elem, both at once at 3.125 B/elem.  Outside the timed step."""
+    fp4 = step.fp4
+    RNE, SR, MMA = fp4.FP4_ROUND_RNE, fp4.FP4_ROUND_STOCHASTIC, fp4.FP4_SFLAYOUT_MMA
+    x, g = step.dY, step.amax[2:3]
+    cr, srs, cc, scs = step.q["dY"]
+    R, C = x.shape
+    n = R * C
+    hbm = peaks()[0]
+    modes = {
+        "rne_row": (2.5625, lambda: fp4.fp4_quantize(x, "E4M3", RNE, 0, g, False, MMA, cr, srs, None)),
+        "rne_col": (2.5625, lambda: fp4.fp4_quantize(x, "E4M3", RNE, 0, g, True, MMA, cc, scs, None)),
+        "sr_row": (2.5625, lambda: fp4.fp4_quantize(x, "E4M3", SR, 1234, g, False, MMA, cr, srs, None)),
+        "sr_col": (2.5625, lambda: fp4.fp4_quantize(x, "E4M3", SR, 1235, g, True, MMA, cc, scs, None)),
+        "dual_rne": (3.125, lambda: fp4.fp4_quantize_dual(x, "E4M3", RNE, 0, RNE, 0, g, MMA, cr, srs, cc, scs)),
+        "dual_sr": (3.125, lambda: fp4.fp4_quantize_dual(x, "E4M3", SR, 1234, SR, 1235, g, MMA, cr, srs, cc, scs)),
+    }
+    out = {"tensor": f"dY {R}x{C} bf16, E4M3 g16, given amax", "unit": "GB/s", "peak": hbm}
+    st = torch.cuda.current_stream()
+    for name, (bpe, fn) in modes.items():
+        fn()
+        ts = []
+        for _ in range(reps):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(st)
+            fn()
+            e1.record(st)
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        gbs = n * bpe / (statistics.median(ts) * 1e-3) / 1e9
+        out[name] = {"us": round(statistics.median(ts) * 1e3, 2), "achieved": round(gbs, 1),
+                     "frac": round(gbs / hbm, 4), "bytes_per_elem": bpe}
+    return out
+
+
 def make_inputs():
     from fp4_block_scaled_amax_gb300 import synth
     d = synth.config3()
@@ -345,6 +384,7 @@ def run_ours(args, rank, world, local):
     traffic_v = traffic_of("gemm")
     qtraffic_v = traffic_of("quant_dual")
 
+    qmodes = quantizer_modes(step, flush)
     e2e = None
     if not args.no_e2e:
         e2e = run_e2e(step, d, args, world, device)
@@ -374,6 +414,7 @@ def run_ours(args, rank, world, local):
         "roofline_quantize": {"kernel": "k_quant_tile (dual, 3.125 B/elem; X, W, dY per step)", "bound": "hbm",
                               "achieved": round(q_gbs, 1), "peak": hbm, "unit": "GB/s",
                               "frac": round(q_gbs / hbm, 4), "traffic": qtraffic_v, "peak_source": src},
+        "quantize_modes": qmodes,
         "amax_gbs": round(a_gbs, 1),
         "gemv_w4a16": {"batch": GEMV_BATCH, "N": N_FFN, "K": K_HID, "us": round(statistics.mean(gemv_ms) * 1e3, 2),
                        "GB/s": round(gv_gbs, 1), "frac": round(gv_gbs / hbm, 4)},
@@ -387,11 +428,11 @@ def run_ours(args, rank, world, local):
     if e2e is not None:
         line["e2e"] = e2e
     if rank == 0 and not args.no_cpu_baseline:
-        flops, dt = oracle_slice_step(d)
+        flops, dt = oracle_slice_step(d, CPU_SAMPLE_TOKENS, CPU_SAMPLE_FEATURES)
         line["cpu_baseline"] = {"value": round(flops / dt / 1e12, 6), "unit": "TFLOP/s", "cores": cores(),
                                 "kind": "oracle",
-                                "sample": "oracle step on 1024 tokens x 1024 output features at K=4096 "
-                                          f"(quantize 6 operands + 3 float64 GEMMs), {dt:.1f} s"}
+                                "sample": f"oracle step on {CPU_SAMPLE_TOKENS} tokens x {CPU_SAMPLE_FEATURES} output "
+                                          f"features at K=4096 (quantize 6 operands + 3 float64 GEMMs), {dt:.1f} s"}
     return line
 
 

@@ -182,24 +182,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
       : "memory");
 }
-// The same box into every CTA of the cluster in `mask` (same shared offsets),
-// each CTA's mbarrier at `bar` receiving the bytes.
-__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y,
-                                               uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster [%0], "
-      "[%1, {%3, %4}], [%2], %5;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "h"(mask)
-      : "memory");
-}
-__device__ __forceinline__ void bulk_load_mc(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar,
-                                             uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster [%0], [%1], %2, [%3], "
-      "%4;" ::"r"(dst),
-      "l"(src), "r"(bytes), "r"(bar), "h"(mask)
-      : "memory");
-}
 __device__ __forceinline__ uint32_t cluster_rank() {
   uint32_t r;
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
@@ -232,15 +214,6 @@ __device__ __forceinline__ void tc_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
                : "memory");
 }
-// Arrive on the mbarrier at `bar` in every CTA of the cluster in `mask` once
-// this thread's prior tcgen05 operations have completed.
-__device__ __forceinline__ void tc_commit_mc(uint32_t bar, uint16_t mask) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-                   bar),
-               "h"(mask)
-               : "memory");
-}
-
 // Shared-memory matrix descriptor: start address, leading/stride byte offsets
 // (16-byte units), fixed version field 1 at bit 46, layout type at bits 61-63
 // (2 = 128-byte swizzle).
@@ -302,16 +275,10 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
       "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
       : "memory");
 }
-// Arrive on the mbarrier at `bar` in both CTAs of the pair once the pair's
-// prior tcgen05 operations issued by this thread have completed.
-__device__ __forceinline__ void tc_commit_pair(uint32_t bar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
-      "h"((uint16_t)3)
-      : "memory");
-}
-// The same, issued by one elected lane of a converged warp (the warp's
-// operands stay warp-uniform).
+// Block-scaled FP4 MMA of the CTA pair (M = 256), and the commit that arrives
+// on the mbarrier at `bar` in both CTAs once the pair's prior tcgen05
+// operations have completed; each issued by one elected lane of a converged
+// warp (the warp's operands stay warp-uniform).
 template <bool MX>
 __device__ __forceinline__ void tc_mma_pair_elect(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                                   uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
@@ -339,26 +306,6 @@ __device__ __forceinline__ void tc_commit_pair_elect(uint32_t bar) {
       "h"((uint16_t)3)
       : "memory");
 }
-template <bool MX>
-__device__ __forceinline__ void tc_mma_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                            uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
-  if constexpr (MX) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
-        "tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
-            d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
-        : "memory");
-  } else {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
-        "tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
-            d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
-        : "memory");
-  }
-}
-
 #define TC_LD32(taddr, r)                                                                                          \
   asm volatile(                                                                                                    \
       "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18," \
@@ -469,11 +416,7 @@ __device__ __forceinline__ float epilogue_alpha(const Params& p) {
   return alpha;
 }
 
-// CM CTAs of a cluster take CM consecutive M tiles of the same N tile: each
-// loads its own A tile and 1/CM of the shared B tile (and of its scales),
-// multicast to all of them, so the L2 -> SM traffic per K step drops from
-// A + B to A + B/CM.
-template <int FMT, bool BF16, int CM, class PL>
+template <int FMT, bool BF16, class PL>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     k_gemm_fp4(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                const __grid_constant__ CUtensorMap tmap_c, Params p) {
@@ -507,12 +450,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int m_tiles = p.M / BM, n_tiles = p.N / BN;
-  // work unit = CM consecutive M tiles of one N tile, one per cluster CTA
-  const int m_groups = m_tiles / CM;
+  const int m_groups = m_tiles;
   const int num_units = m_groups * n_tiles;
-  const int crank = CM > 1 ? (int)cluster_rank() : 0;
-  const int cluster_id = blockIdx.x / CM, num_clusters = gridDim.x / CM;
-  constexpr uint16_t MC_MASK = (uint16_t)((1u << CM) - 1u);
+  const int cluster_id = blockIdx.x, num_clusters = gridDim.x;
   const int k_steps = p.K / BK;
   const int64_t sf_row_stride = (int64_t)(p.K / (MX ? 32 : 16)) / 4 * 512;  // bytes per 128-row slab
 
@@ -520,7 +460,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(bar_full + 8 * s, 1);
       mbar_init(bar_sf + 8 * s, NUM_SF_WARPS);
-      mbar_init(bar_empty + 8 * s, CM);  // one MMA commit from each cluster CTA
+      mbar_init(bar_empty + 8 * s, 1);
     }
     for (int s = 0; s < SF_SLOTS; ++s) {
       mbar_init(bar_sfd_full + 8 * s, 1);
@@ -540,7 +480,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if constexpr (CM > 1) cluster_sync_all();  // peers' barriers exist before any multicast
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
@@ -553,9 +492,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       uint32_t phase = 0;
       bool ok = true;
       for (int u = cluster_id; u < num_units && ok; u += num_clusters) {
-        const int mt = (u % m_groups) * CM + crank, nt = u / m_groups;
+        const int mt = u % m_groups, nt = u / m_groups;
         for (int ks = 0; ks < k_steps; ++ks) {
-          // own stage free in every cluster CTA (the B slice lands in all of them)
           if (!wait_bounded(bar_empty + 8 * stage, phase ^ 1u, abort_flag, p.status) || *abort_flag) {
             ok = false;
             break;
@@ -563,15 +501,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const uint32_t fb = bar_full + 8 * stage;
           mbar_expect_tx(fb, A_BYTES + B_BYTES);
           tma_load_2d(sbase + SMEM_A + stage * A_BYTES, &tmap_a, fb, ks * (BK / 2), mt * BM);
-          if constexpr (CM == 1) {
-            tma_load_2d(sbase + SMEM_B + stage * B_BYTES, &tmap_b, fb, ks * (BK / 2), nt * BN);
-          } else {
-            // rows [crank*BN/CM, +BN/CM) of the B tile: 128-byte rows, so the
-            // slice starts crank*BN/CM*128 bytes into the swizzled stage
-            constexpr int ROWS = BN / CM;
-            tma_load_2d_mc(sbase + SMEM_B + stage * B_BYTES + crank * ROWS * 128, &tmap_b, fb, ks * (BK / 2),
-                           nt * BN + crank * ROWS, MC_MASK);
-          }
+          tma_load_2d(sbase + SMEM_B + stage * B_BYTES, &tmap_b, fb, ks * (BK / 2), nt * BN);
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
@@ -621,9 +551,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
             tc_mma<MX>(tmem_base, ad, bd, idesc, sfa_col, sfb_col, (ks > 0 || j > 0) ? 1u : 0u);
           }
-          // stage (smem and its scale columns) free once these finish, in every cluster CTA
-          if constexpr (CM == 1) tc_commit(bar_empty + 8 * stage);
-          else tc_commit_mc(bar_empty + 8 * stage, MC_MASK);
+          // stage (smem and its scale columns) free once these finish
+          tc_commit(bar_empty + 8 * stage);
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
@@ -642,7 +571,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       uint32_t phase = 0;
       bool ok = true;
       for (int u = cluster_id; u < num_units && ok; u += num_clusters) {
-        const int mt = (u % m_groups) * CM + crank, nt = u / m_groups;
+        const int mt = u % m_groups, nt = u / m_groups;
         for (int ks = 0; ks < k_steps; ++ks) {
           if (!wait_bounded(bar_sfd_empty + 8 * slot, phase ^ 1u, abort_flag, p.status) || *abort_flag) {
             ok = false;
@@ -653,18 +582,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           // scales of this K step: SFA_BYTES contiguous bytes per 128-row slab
           bulk_load(sbase + SMEM_SFA + slot * SFA_MAX, p.As + mt * sf_row_stride + (int64_t)ks * SFA_BYTES,
                     SFA_BYTES, sb);
-          if constexpr (CM == 1) {
-            bulk_load(sbase + SMEM_SFB + slot * SFB_MAX, p.Bs + (2 * nt) * sf_row_stride + (int64_t)ks * SFB_HALF,
-                      SFB_HALF, sb);
-            bulk_load(sbase + SMEM_SFB + slot * SFB_MAX + SFB_HALF,
-                      p.Bs + (2 * nt + 1) * sf_row_stride + (int64_t)ks * SFB_HALF, SFB_HALF, sb);
-          } else {
-            // 1/CM of the two 128-row scale halves, multicast
-            constexpr int PIECE = 2 * SFB_HALF / CM;
-            const int half = (crank * PIECE) / SFB_HALF, off = (crank * PIECE) % SFB_HALF;
-            bulk_load_mc(sbase + SMEM_SFB + slot * SFB_MAX + half * SFB_HALF + off,
-                         p.Bs + (2 * nt + half) * sf_row_stride + (int64_t)ks * SFB_HALF + off, PIECE, sb, MC_MASK);
-          }
+          bulk_load(sbase + SMEM_SFB + slot * SFB_MAX, p.Bs + (2 * nt) * sf_row_stride + (int64_t)ks * SFB_HALF,
+                    SFB_HALF, sb);
+          bulk_load(sbase + SMEM_SFB + slot * SFB_MAX + SFB_HALF,
+                    p.Bs + (2 * nt + 1) * sf_row_stride + (int64_t)ks * SFB_HALF, SFB_HALF, sb);
           if (++slot == SF_SLOTS) {
             slot = 0;
             phase ^= 1u;
@@ -742,7 +663,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t stage_addr = smem_u32(stage_buf);
     uint32_t acc_phase = 0;
     for (int u = cluster_id; u < num_units; u += num_clusters) {
-      const int mt = (u % m_groups) * CM + crank, nt = u / m_groups;
+      const int mt = u % m_groups, nt = u / m_groups;
       if (!wait_bounded(bar_acc_full, acc_phase, abort_flag, p.status)) break;
       acc_phase ^= 1u;
       tc_fence_after();
@@ -765,8 +686,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   tc_fence_before();
   __syncthreads();
   drain_after_abort(abort_flag);
-  // no CTA leaves while a peer may still multicast into it or arrive on it
-  if constexpr (CM > 1) cluster_sync_all();
   if (warp == 1) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS)
@@ -1143,38 +1062,18 @@ int sm_count() {
   return n;
 }
 
-template <int FMT, bool BF16, int CM, class PL>
+template <int FMT, bool BF16, class PL>
 cudaError_t launch_t(const fp4lib::GemmArgs& a, cudaStream_t st) {
-  auto kern = k_gemm_fp4<FMT, BF16, CM, PL>;
+  auto kern = k_gemm_fp4<FMT, BF16, PL>;
   constexpr int SMEM_LAUNCH = PL::SMEM_LAUNCH;
   static bool attr_set = false;
-  static int max_clusters = 0;
-  cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = CM;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.blockDim = dim3(NUM_THREADS, 1, 1);
-  cfg.dynamicSmemBytes = SMEM_LAUNCH;
-  cfg.stream = st;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_LAUNCH);
     if (e != cudaSuccess) return e;
-    cfg.gridDim = dim3(sm_count(), 1, 1);
-    if (CM > 1) {
-      e = cudaOccupancyMaxActiveClusters(&max_clusters, kern, &cfg);
-      if (e != cudaSuccess) return e;
-    } else {
-      max_clusters = sm_count();
-    }
-    if (max_clusters <= 0) return cudaErrorInvalidConfiguration;
     attr_set = true;
   }
   CUtensorMap ma, mb, mc;
-  if (!make_code_map(&ma, a.Aq, a.M, a.K / 2, BM) || !make_code_map(&mb, a.Bq, a.N, a.K / 2, BN / CM) ||
+  if (!make_code_map(&ma, a.Aq, a.M, a.K / 2, BM) || !make_code_map(&mb, a.Bq, a.N, a.K / 2, BN) ||
       !make_out_map(&mc, a.C, a.M, a.N, a.ldc, BF16, PL::OUT_ROW_BYTES))
     return cudaErrorInvalidValue;
   Params p;
@@ -1188,10 +1087,10 @@ cudaError_t launch_t(const fp4lib::GemmArgs& a, cudaStream_t st) {
   p.N = (int)a.N;
   p.K = (int)a.K;
   p.status = a.status;
-  const int units = (int)((a.M / BM / CM) * (a.N / BN));
-  const int clusters = units < max_clusters ? units : max_clusters;
-  cfg.gridDim = dim3((unsigned)(clusters * CM), 1, 1);
-  return cudaLaunchKernelEx(&cfg, kern, ma, mb, mc, p);
+  const int units = (int)((a.M / BM) * (a.N / BN));
+  const int ctas = units < sm_count() ? units : sm_count();
+  kern<<<(unsigned)ctas, NUM_THREADS, SMEM_LAUNCH, st>>>(ma, mb, mc, p);
+  return cudaGetLastError();
 }
 
 // CTA-pair launch: clusters of 2 CTAs, one 256 x 256 output tile per cluster
@@ -1244,20 +1143,12 @@ cudaError_t launch_pair(const fp4lib::GemmArgs& a, cudaStream_t st) {
   return cudaLaunchKernelEx(&cfg, kern, ma, mb, mc, p);
 }
 
-// Cluster size along M.  Multicasting the B tile halves or quarters the
-// L2 -> SM bytes per K step, but on the 7B shapes it measured no faster
-// (2 CTAs) or slower (4 CTAs: fewer co-resident clusters) than independent
-// CTAs, so independent CTAs are the default.
-constexpr int GEMM_CLUSTER_M = 1;
-
+// CTA pairs whenever the 128-row tiles pair up; single CTAs otherwise.
 template <int FMT, bool BF16>
 cudaError_t launch_cm(const fp4lib::GemmArgs& a, cudaStream_t st) {
   const int64_t m_tiles = a.M / BM;
   if (m_tiles % 2 == 0) return launch_pair<FMT, BF16>(a, st);
-  const bool long_k = a.K >= 8192;
-  if (GEMM_CLUSTER_M == 2 && m_tiles % 2 == 0)
-    return long_k ? launch_t<FMT, BF16, 2, PlanLongK>(a, st) : launch_t<FMT, BF16, 2, PlanShortK>(a, st);
-  return long_k ? launch_t<FMT, BF16, 1, PlanLongK>(a, st) : launch_t<FMT, BF16, 1, PlanShortK>(a, st);
+  return a.K >= 8192 ? launch_t<FMT, BF16, PlanLongK>(a, st) : launch_t<FMT, BF16, PlanShortK>(a, st);
 }
 
 }  // namespace
