@@ -311,6 +311,49 @@ def quantizer_modes(step, flush, reps=5):
     return out
 
 
+SWEEP_FORMATS = ["E4M3", "UE5M3", "E8M0", "E1M6", "E2M5", "E3M4", "E5M2", "E6M1", "E7M0"]
+
+
+def scale_format_sweep(fp4, flush, device, reps=5):
+    """Row quantizer (RNE, fresh amax given) on the 350M-parameter MLP input
+    X 8192x1024 (per-column sigma log-uniform in [0.1, 10]) for every scale
+    format: GB/s at 2 + 0.5 + 1/G B/elem, and the relative RMS error of the
+    dequantized tensor.  Outside the timed step."""
+    from fp4_block_scaled_amax_gb300 import synth
+    x = synth.config2()["X"].to(device)
+    M, K = x.shape
+    g = x.float().abs().max().reshape(1)
+    xf = x.float()
+    ref_norm = float(xf.pow(2).mean().sqrt())
+    hbm = peaks()[0]
+    out = {"tensor": f"X {M}x{K} bf16 (350M MLP input), RNE rows, fresh amax", "unit": "GB/s", "peak": hbm}
+    st = torch.cuda.current_stream()
+    deq = torch.empty((M, K), dtype=torch.float32, device=device)
+    for f in SWEEP_FORMATS:
+        G = 32 if f == "E8M0" else 16
+        codes = torch.empty((M, K // 2), dtype=torch.uint8, device=device)
+        scales = torch.empty(M * K // G, dtype=torch.uint8, device=device)
+        def run():
+            fp4.fp4_quantize(x, f, fp4.FP4_ROUND_RNE, 0, g, False, fp4.FP4_SFLAYOUT_PLAIN, codes, scales, None)
+        run()
+        ts = []
+        for _ in range(reps):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(st)
+            run()
+            e1.record(st)
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        us = statistics.median(ts) * 1e3
+        gbs = M * K * (2 + 0.5 + 1 / G) / us / 1e3
+        fp4.fp4_dequantize(codes, scales, fp4.FP4_SFLAYOUT_PLAIN, M, K, f, g, fp4.FP4_OUT_F32, deq)
+        rel_rmse = float((deq - xf).pow(2).mean().sqrt()) / ref_norm
+        out[f] = {"us": round(us, 2), "achieved": round(gbs, 1), "frac": round(gbs / hbm, 4),
+                  "rel_rmse": round(rel_rmse, 5)}
+    return out
+
+
 def make_inputs():
     from fp4_block_scaled_amax_gb300 import synth
     d = synth.config3()
@@ -385,6 +428,7 @@ def run_ours(args, rank, world, local):
     qtraffic_v = traffic_of("quant_dual")
 
     qmodes = quantizer_modes(step, flush)
+    sweep = scale_format_sweep(step.fp4, flush, device)
     e2e = None
     if not args.no_e2e:
         e2e = run_e2e(step, d, args, world, device)
@@ -415,6 +459,7 @@ def run_ours(args, rank, world, local):
                               "achieved": round(q_gbs, 1), "peak": hbm, "unit": "GB/s",
                               "frac": round(q_gbs / hbm, 4), "traffic": qtraffic_v, "peak_source": src},
         "quantize_modes": qmodes,
+        "scale_format_sweep": sweep,
         "amax_gbs": round(a_gbs, 1),
         "gemv_w4a16": {"batch": GEMV_BATCH, "N": N_FFN, "K": K_HID, "us": round(statistics.mean(gemv_ms) * 1e3, 2),
                        "GB/s": round(gv_gbs, 1), "frac": round(gv_gbs / hbm, 4)},

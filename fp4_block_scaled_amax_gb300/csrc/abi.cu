@@ -18,16 +18,14 @@ fp4_status cuda_status(cudaError_t e) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-bool valid_fmt(int f) { return f == FP4_SF_E4M3 || f == FP4_SF_UE5M3 || f == FP4_SF_E8M0 || f == FP4_SF_E1M6; }
+bool valid_fmt(int f) { return f >= FP4_SF_E4M3 && f <= FP4_SF_E7M0; }
+
+// E2M5 .. E7M0: the rest of the scale-format sweep, row quantization only
+bool sweep_fmt(int f) { return f >= FP4_SF_E2M5 && f <= FP4_SF_E7M0; }
 
 int group_of(int f) {
-  switch (f) {
-    case FP4_SF_E4M3:
-    case FP4_SF_UE5M3:
-    case FP4_SF_E1M6: return 16;
-    case FP4_SF_E8M0: return 32;
-    default: return 0;
-  }
+  if (!valid_fmt(f)) return 0;
+  return f == FP4_SF_E8M0 ? 32 : 16;
 }
 
 // Checks shared by the quantizer entry points.  rows/cols are the OUTPUT
@@ -103,6 +101,7 @@ fp4_status fp4_quantize(const void* x_bf16, int64_t M, int64_t K, int64_t ldx, f
   const int64_t out_rows = transpose ? K : M, out_cols = transpose ? M : K;
   fp4_status s = check_quant_common(x_bf16, M, K, ldx, (int)f, (int)sfl, out_rows, out_cols);
   if (s != FP4_OK) return s;
+  if (transpose && sweep_fmt((int)f)) return FP4_ERR_UNSUPPORTED;
   if (transpose && (M % 32 != 0 || K % 32 != 0)) return FP4_ERR_SHAPE;
   if (M * K > 0 && (s = check_out(codes, scales)) != FP4_OK) return s;
   cudaStream_t st = (cudaStream_t)stream;
@@ -142,6 +141,7 @@ fp4_status fp4_quantize_dual(const void* x_bf16, int64_t M, int64_t K, int64_t l
   fp4_status s = check_quant_common(x_bf16, M, K, ldx, (int)f, (int)sfl, M, K);
   if (s != FP4_OK) return s;
   if ((s = check_quant_common(x_bf16, M, K, ldx, (int)f, (int)sfl, K, M)) != FP4_OK) return s;
+  if (sweep_fmt((int)f)) return FP4_ERR_UNSUPPORTED;
   if (M % 32 != 0 || K % 32 != 0) return FP4_ERR_SHAPE;
   if (M * K > 0) {
     if ((s = check_out(codes_row, scales_row)) != FP4_OK) return s;
@@ -199,7 +199,7 @@ fp4_status fp4_gemm(const uint8_t* Aq, const uint8_t* As, const uint8_t* Bq, con
                     int32_t* dev_status, fp4_stream_t stream) {
   if (layout != FP4_LAYOUT_TN || (od != FP4_OUT_F32 && od != FP4_OUT_BF16) || !valid_fmt((int)f))
     return FP4_ERR_INVALID_ARG;
-  if (f == FP4_SF_E1M6) return FP4_ERR_UNSUPPORTED;
+  if (f == FP4_SF_E1M6 || sweep_fmt((int)f)) return FP4_ERR_UNSUPPORTED;
   if (Aq == nullptr || As == nullptr || Bq == nullptr || Bs == nullptr || C == nullptr) return FP4_ERR_INVALID_ARG;
   if (f != FP4_SF_E8M0 && (ga == nullptr || gb == nullptr)) return FP4_ERR_INVALID_ARG;
   if (f == FP4_SF_UE5M3 && (tA == nullptr || tB == nullptr)) return FP4_ERR_INVALID_ARG;

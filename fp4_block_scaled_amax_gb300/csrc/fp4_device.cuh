@@ -86,7 +86,17 @@ __device__ __forceinline__ uint32_t exmy_encode_rne_sat(float s) {
 }
 
 // Format tags, matching fp4_scale_fmt.
-enum : int { SF_E4M3 = FP4_SF_E4M3, SF_UE5M3 = FP4_SF_UE5M3, SF_E8M0 = FP4_SF_E8M0, SF_E1M6 = FP4_SF_E1M6 };
+enum : int {
+  SF_E4M3 = FP4_SF_E4M3,
+  SF_UE5M3 = FP4_SF_UE5M3,
+  SF_E8M0 = FP4_SF_E8M0,
+  SF_E1M6 = FP4_SF_E1M6,
+  SF_E2M5 = FP4_SF_E2M5,
+  SF_E3M4 = FP4_SF_E3M4,
+  SF_E5M2 = FP4_SF_E5M2,
+  SF_E6M1 = FP4_SF_E6M1,
+  SF_E7M0 = FP4_SF_E7M0
+};
 
 template <int FMT> struct ScaleFmt;
 // E4M3 (FN) nearest-even with saturation to 448 is the hardware conversion;
@@ -114,6 +124,23 @@ template <> struct ScaleFmt<SF_E1M6> {
   __device__ static uint32_t encode(float s) { return exmy_encode_rne_sat<6, 0, 0x7Fu>(s); }
   __device__ static float decode(uint32_t c) { return exmy_decode<6, 0>(c); }
 };
+// The rest of the group-16 sweep: signed ExMy with bias 2^(E-1)-1, no NaN;
+// the non-negative codes run up to 0x7F, and the global-scale target S_T is
+// the largest finite value.
+template <int MB, int BIAS, int SIX_ST_BITS>
+struct SweepScale {
+  static constexpr int G = 16;
+  __device__ static float six_st() { return __uint_as_float((uint32_t)SIX_ST_BITS); }
+  __device__ static uint32_t encode(float s) { return exmy_encode_rne_sat<MB, BIAS, 0x7Fu>(s); }
+  __device__ static float decode(uint32_t c) { return exmy_decode<MB, BIAS>(c); }
+};
+// 6 * S_T as float32 bits: 47.25, 186, 688128, 9 * 2^32, 1.5 * 2^66
+template <> struct ScaleFmt<SF_E2M5> : SweepScale<5, 1, 0x423D0000> {};
+template <> struct ScaleFmt<SF_E3M4> : SweepScale<4, 3, 0x433A0000> {};
+template <> struct ScaleFmt<SF_E5M2> : SweepScale<2, 15, 0x49280000> {};
+template <> struct ScaleFmt<SF_E6M1> : SweepScale<1, 31, 0x51100000> {};
+template <> struct ScaleFmt<SF_E7M0> : SweepScale<0, 63, 0x60C00000> {};
+
 template <> struct ScaleFmt<SF_E8M0> {
   static constexpr int G = 32;
   static constexpr float SIX_ST = 0.0f;  // unused: no global scale
@@ -129,6 +156,12 @@ template <> struct ScaleFmt<SF_E8M0> {
   }
 };
 
+template <int FMT>
+__device__ __forceinline__ float six_st_of() {
+  if constexpr (FMT >= SF_E2M5) return ScaleFmt<FMT>::six_st();
+  else return ScaleFmt<FMT>::SIX_ST;
+}
+
 // Per-tensor encode scale from the stored amax g.
 template <int FMT>
 __device__ __forceinline__ float global_encode_scale(float g, int32_t* status) {
@@ -138,7 +171,7 @@ __device__ __forceinline__ float global_encode_scale(float g, int32_t* status) {
     return 1.0f;
   }
   if (g == 0.0f) return 1.0f;
-  const float s = __fdiv_rn(ScaleFmt<FMT>::SIX_ST, g);
+  const float s = __fdiv_rn(six_st_of<FMT>(), g);
   return (s > 3.402823466e38f) ? 3.402823466e38f : s;
 }
 

@@ -431,14 +431,35 @@ static void dispatch_fmt(const QuantArgs& a, cudaStream_t st) {
   }
 }
 
+// The rest of the scale-format sweep: row quantization only.
+template <int FMT>
+static cudaError_t dispatch_rows_only(const QuantArgs& a, cudaStream_t st) {
+  if (a.mode != QuantArgs::ROWS) return cudaErrorNotSupported;
+  const bool amax = a.amax_by_product;
+#define ROWS_CASE(SR, MMA, AM) \
+  if (a.row_sr == SR && a.mma == MMA && amax == AM) rows_t<FMT, SR, MMA, AM>(a, st);
+  ROWS_CASE(false, false, false) ROWS_CASE(false, false, true) ROWS_CASE(false, true, false)
+  ROWS_CASE(false, true, true) ROWS_CASE(true, false, false) ROWS_CASE(true, false, true)
+  ROWS_CASE(true, true, false) ROWS_CASE(true, true, true)
+#undef ROWS_CASE
+  return cudaSuccess;
+}
+
 cudaError_t launch_quantize(const QuantArgs& a, cudaStream_t st) {
+  cudaError_t e = cudaSuccess;
   switch (a.fmt) {
     case FP4_SF_E4M3: dispatch_fmt<SF_E4M3>(a, st); break;
     case FP4_SF_UE5M3: dispatch_fmt<SF_UE5M3>(a, st); break;
     case FP4_SF_E8M0: dispatch_fmt<SF_E8M0>(a, st); break;
     case FP4_SF_E1M6: dispatch_fmt<SF_E1M6>(a, st); break;
+    case FP4_SF_E2M5: e = dispatch_rows_only<SF_E2M5>(a, st); break;
+    case FP4_SF_E3M4: e = dispatch_rows_only<SF_E3M4>(a, st); break;
+    case FP4_SF_E5M2: e = dispatch_rows_only<SF_E5M2>(a, st); break;
+    case FP4_SF_E6M1: e = dispatch_rows_only<SF_E6M1>(a, st); break;
+    case FP4_SF_E7M0: e = dispatch_rows_only<SF_E7M0>(a, st); break;
     default: return cudaErrorInvalidValue;
   }
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
@@ -457,6 +478,11 @@ cudaError_t launch_dequantize(const uint8_t* codes, const uint8_t* scales, bool 
     case FP4_SF_UE5M3: DQ(SF_UE5M3) break;
     case FP4_SF_E8M0: DQ(SF_E8M0) break;
     case FP4_SF_E1M6: DQ(SF_E1M6) break;
+    case FP4_SF_E2M5: DQ(SF_E2M5) break;
+    case FP4_SF_E3M4: DQ(SF_E3M4) break;
+    case FP4_SF_E5M2: DQ(SF_E5M2) break;
+    case FP4_SF_E6M1: DQ(SF_E6M1) break;
+    case FP4_SF_E7M0: DQ(SF_E7M0) break;
     default: return cudaErrorInvalidValue;
   }
 #undef DQ
@@ -486,6 +512,11 @@ cudaError_t launch_encode_scales(const float* s, int64_t n, int fmt, uint8_t* co
     case FP4_SF_UE5M3: k_encode_scales<SF_UE5M3><<<g, 256, 0, st>>>(s, n, codes, decoded); break;
     case FP4_SF_E8M0: k_encode_scales<SF_E8M0><<<g, 256, 0, st>>>(s, n, codes, decoded); break;
     case FP4_SF_E1M6: k_encode_scales<SF_E1M6><<<g, 256, 0, st>>>(s, n, codes, decoded); break;
+    case FP4_SF_E2M5: k_encode_scales<SF_E2M5><<<g, 256, 0, st>>>(s, n, codes, decoded); break;
+    case FP4_SF_E3M4: k_encode_scales<SF_E3M4><<<g, 256, 0, st>>>(s, n, codes, decoded); break;
+    case FP4_SF_E5M2: k_encode_scales<SF_E5M2><<<g, 256, 0, st>>>(s, n, codes, decoded); break;
+    case FP4_SF_E6M1: k_encode_scales<SF_E6M1><<<g, 256, 0, st>>>(s, n, codes, decoded); break;
+    case FP4_SF_E7M0: k_encode_scales<SF_E7M0><<<g, 256, 0, st>>>(s, n, codes, decoded); break;
     default: return cudaErrorInvalidValue;
   }
   return cudaGetLastError();

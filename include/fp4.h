@@ -71,8 +71,18 @@ typedef enum {
   FP4_SF_E4M3 = 0,  /* NVFP4: E4M3 (bias 7, max 448), G = 16   [NVFP4/MX] */
   FP4_SF_UE5M3 = 1, /* unsigned 5+3 bits (bias 15, max 114688), G = 16   [UE5M3] */
   FP4_SF_E8M0 = 2,  /* MXFP4: 2^(c-127), G = 32, no global scale   [NVFP4/MX] */
-  FP4_SF_E1M6 = 3   /* narrowest format of the sweep (max 3.96875), G = 16;
+  FP4_SF_E1M6 = 3,  /* narrowest format of the sweep (max 3.96875), G = 16;
                        quantizer only, no GEMM   [FP4-REV "Форматы FP4"] */
+  /* The rest of the group-16 scale-format sweep of [FP4-REV] "Форматы FP4":
+   * signed ExMy scales with bias 2^(E-1)-1, IEEE-style subnormals and no NaN
+   * (only their non-negative codes occur).  Row quantization (fp4_quantize
+   * with transpose = 0), fp4_dequantize and fp4_encode_scales only; every
+   * other call returns FP4_ERR_UNSUPPORTED for them. */
+  FP4_SF_E2M5 = 4,  /* max 7.875 */
+  FP4_SF_E3M4 = 5,  /* max 31 */
+  FP4_SF_E5M2 = 6,  /* max 114688 */
+  FP4_SF_E6M1 = 7,  /* max 1.5 * 2^32 */
+  FP4_SF_E7M0 = 8   /* max 2^64 */
 } fp4_scale_fmt;
 
 typedef enum {
@@ -103,7 +113,8 @@ fp4_status fp4_amax(const void* x_bf16, int64_t M, int64_t K, int64_t ldx,
 /* Quantize a bf16 [M, K] matrix to FP4 codes plus block scales.
  * Method ([NVFP4/MX] "Метод", [UE5M3] "Что сделали", [FP4-REV]
  * "Стохастическая квантизация"), all float32 steps correctly rounded:
- *   s_enc = f32(f32(6*S_T) / g), S_T = 448 (E4M3, UE5M3) or 3.96875 (E1M6);
+ *   s_enc = f32(f32(6*S_T) / g), S_T = 448 (E4M3, UE5M3), otherwise the
+ *           scale format's largest finite value (3.96875 for E1M6);
  *           g == 0 -> 1, overflow -> FLT_MAX; E8M0: s_enc = 1;
  *   per block of G elements along K: a_b = max|x|;
  *           s_b = decode(encode_rne_sat(f32(f32(a_b/6) * s_enc)));

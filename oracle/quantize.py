@@ -17,7 +17,9 @@ implementation (all float32 operations are single IEEE binary32 operations with
 round-to-nearest-even; G is the group size):
 
 1. Global encode scale  s_enc = f32(f32(6 * S_T) / g), g the stored tensor amax,
-   S_T = 448 for E4M3 and UE5M3, 3.96875 for E1M6; g == 0 -> 1; an overflow ->
+   S_T = 448 for E4M3 and UE5M3, otherwise the scale format's largest finite
+   value (3.96875 for E1M6; 7.875, 31, 114688, 1.5*2^32 and 2^64 for the rest
+   of the sweep E2M5, E3M4, E5M2, E6M1, E7M0); g == 0 -> 1; an overflow ->
    FLT_MAX.  E8M0 (MXFP4) uses no global scale: s_enc = 1.
 2. Block amax a_b = max |x| over G consecutive elements along the last axis.
 3. Block scale: s_real = f32(f32(a_b / 6) * s_enc), code = nearest scale code
@@ -44,6 +46,12 @@ from .philox import sr_bits16
 
 GROUP = {"E4M3": 16, "UE5M3": 16, "E1M6": 16, "E8M0": 32}
 SCALE_TARGET = {"E4M3": 448.0, "UE5M3": 448.0, "E1M6": 3.96875}
+# the rest of the group-16 scale-format sweep (gonzo_ML #3986, "Форматы FP4"):
+# generic ExMy scales, target = the format's largest finite value
+SWEEP_FORMATS = ("E2M5", "E3M4", "E5M2", "E6M1", "E7M0")
+for _name in SWEEP_FORMATS:
+    GROUP[_name] = 16
+    SCALE_TARGET[_name] = F.SWEEP[_name].max_finite()
 FLT_MAX = np.float32(np.finfo(np.float32).max)
 
 

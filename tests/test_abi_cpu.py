@@ -38,6 +38,8 @@ def test_group_size_and_storage_bytes():
     assert fp4.fp4_group_size("UE5M3") == 16
     assert fp4.fp4_group_size("E8M0") == 32
     assert fp4.fp4_group_size("E1M6") == 16
+    for f in ("E2M5", "E3M4", "E5M2", "E6M1", "E7M0"):
+        assert fp4.fp4_group_size(f) == 16
     assert fp4._lib().fp4_group_size(9) == 0
     cb, sb = fp4.fp4_storage_bytes(64, 1024, "E4M3")
     assert (cb + sb) * 8 / (64 * 1024) == 4.5
@@ -68,7 +70,7 @@ def q(**kw):
 
 
 def test_quantize_argument_errors():
-    assert q(f=7) == fp4.FP4_ERR_INVALID_ARG
+    assert q(f=9) == fp4.FP4_ERR_INVALID_ARG
     assert q(r=3) == fp4.FP4_ERR_INVALID_ARG
     assert q(tr=2) == fp4.FP4_ERR_INVALID_ARG
     assert q(K=40, ldx=40) == fp4.FP4_ERR_SHAPE           # K not a multiple of 16
@@ -117,3 +119,15 @@ def test_gemv_and_misc_argument_errors():
     assert lib.fp4_philox_bits16(1, 0, -1, P, None) == fp4.FP4_ERR_SHAPE
     # empty tensors are valid no-ops
     assert lib.fp4_dequantize(None, None, 0, 0, 32, 0, None, 0, None, None) == fp4.FP4_OK
+
+
+def test_sweep_formats_rows_only():
+    # E2M5 .. E7M0 quantize along rows only: the transposed and dual layouts and
+    # the GEMM report FP4_ERR_UNSUPPORTED before anything is launched
+    lib = _need_lib()
+    for f in (fp4.FP4_SF_E2M5, fp4.FP4_SF_E3M4, fp4.FP4_SF_E5M2, fp4.FP4_SF_E6M1, fp4.FP4_SF_E7M0):
+        assert q(f=f, tr=1) == fp4.FP4_ERR_UNSUPPORTED
+        assert lib.fp4_quantize_dual(P, 64, 64, 64, f, 0, 0, 0, 0, P, 0, P, P, P, P, None, None,
+                                     None) == fp4.FP4_ERR_UNSUPPORTED
+        assert lib.fp4_gemm(P, P, P, P, P, P, None, None, 128, 256, 256, f, 0, 0, P, 256, None,
+                            None) == fp4.FP4_ERR_UNSUPPORTED

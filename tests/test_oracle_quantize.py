@@ -240,3 +240,61 @@ def test_ue5m3_reencode_exact_for_fresh_amax():
     assert exact
     assert np.array_equal(F.CODECS["E4M3"].decode(codes) * 2.0 ** t,
                           Q.scale_values(q["scales"], "UE5M3"))
+
+
+# ---------------------------------------------------------------------------
+# Rest of the group-16 scale-format sweep (E2M5, E3M4, E5M2, E6M1, E7M0)
+# ---------------------------------------------------------------------------
+
+SWEEP_MIN_NORMAL = {"E2M5": 1.0, "E3M4": 2.0 ** -2, "E5M2": 2.0 ** -14, "E6M1": 2.0 ** -30, "E7M0": 2.0 ** -62}
+# largest element magnitude code of a block with a normal scale: the scale's
+# relative rounding error (at most 2^-(m+1)) bounds y_max = 6 s_real / s_b from below
+SWEEP_MAX_CODES = {"E2M5": {7}, "E3M4": {7}, "E5M2": {7}, "E6M1": {6, 7}, "E7M0": {6, 7}}
+
+
+@pytest.mark.parametrize("fmt", Q.SWEEP_FORMATS)
+def test_sweep_global_scale_closed_forms(fmt):
+    st = {"E2M5": 7.875, "E3M4": 31.0, "E5M2": 114688.0, "E6M1": 1.5 * 2.0 ** 32, "E7M0": 2.0 ** 64}[fmt]
+    assert Q.SCALE_TARGET[fmt] == st
+    assert Q.global_encode_scale(6 * st, fmt) == 1.0
+    assert Q.global_encode_scale(1.0, fmt) == np.float32(6 * st)
+
+
+@pytest.mark.parametrize("fmt", Q.SWEEP_FORMATS)
+def test_sweep_amax_block_takes_the_top_code(fmt):
+    # with the fresh amax, the block that holds it has s_real = S_T (up to one
+    # float32 rounding), i.e. the largest finite scale code, and its largest
+    # element becomes 6
+    x = _data(2, (64, 256))
+    q = Q.quantize(x, fmt)
+    r, c = np.unravel_index(np.argmax(np.abs(x)), x.shape)
+    assert q["scales"][r, c // 16] == 0x7F
+    assert (Q.unpack(q["codes"])[r, c] & 7) == 7
+
+
+@pytest.mark.parametrize("fmt", Q.SWEEP_FORMATS)
+def test_sweep_block_max_code_invariant(fmt):
+    x = _data(0, (256, 512))
+    q = Q.quantize(x, fmt)
+    mag = (Q.unpack(q["codes"]) & 7).reshape(256, 32, 16).max(axis=2)
+    normal = Q.scale_values(q["scales"], fmt) >= SWEEP_MIN_NORMAL[fmt]
+    assert normal.any()
+    assert np.all(np.isin(mag[normal], list(SWEEP_MAX_CODES[fmt])))
+
+
+@pytest.mark.parametrize("fmt", Q.SWEEP_FORMATS)
+def test_sweep_requantize_fixed_point(fmt):
+    x = _data(1, (128, 512))
+    q = Q.quantize(x, fmt)
+    xd = bf16(Q.dequantize(q["codes"], q["scales"], fmt, q["amax"]))
+    q2 = Q.quantize(xd, fmt, global_amax=q["amax"])
+    # blocks with a normal scale whose largest element is 6: their re-derived
+    # s_real is s_b exactly (a block topped by 4 re-derives (4/6) s_b, which a
+    # coarse format may round to another code)
+    top6 = (Q.unpack(q["codes"]) & 7).reshape(128, -1, 16).max(axis=2) == 7
+    keep = (Q.scale_values(q["scales"], fmt) >= SWEEP_MIN_NORMAL[fmt]) & top6
+    assert keep.any()
+    assert np.array_equal(q2["scales"][keep], q["scales"][keep])
+    c1 = Q.unpack(q["codes"]).reshape(128, -1, 16)[keep]
+    c2 = Q.unpack(q2["codes"]).reshape(128, -1, 16)[keep]
+    assert np.array_equal(c1, c2)

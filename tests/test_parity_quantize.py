@@ -161,3 +161,50 @@ def test_philox_matches_oracle_10M():
         idx = np.arange(start, start + n, dtype=np.uint64)
         want = np.concatenate([P.sr_bits16(seed, idx[i:i + 1_000_000]) for i in range(0, n, 1_000_000)])
         assert np.array_equal(got.astype(np.uint32), want)
+
+
+# ---------------------------------------------------------------------------
+# The rest of the group-16 scale-format sweep (row quantization only)
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("fmt", Q.SWEEP_FORMATS)
+@pytest.mark.parametrize("rounding", ["rne", "sr"])
+def test_sweep_formats_rows(fmt, rounding):
+    # the 350M-parameter MLP input recipe (per-column sigma log-uniform in
+    # [0.1, 10]) at 1/8 size, plain and tiled scale layouts, fresh and stale amax
+    x = synth.config2(scale=8)["X"]
+    check(x, fmt, rounding, 77)
+    check(x, fmt, rounding, 78, mma=True)
+    check(x, fmt, rounding, 79, g=float(x.float().abs().max()) / 5)
+
+
+@pytest.mark.parametrize("fmt", Q.SWEEP_FORMATS)
+def test_sweep_formats_dequantize(fmt):
+    fp4 = lib()
+    x = synth.config2(scale=8)["X"]
+    M, K = x.shape
+    ref = Q.quantize(f32(x), fmt, "rne", 0)
+    g = torch.tensor([ref["amax"]], dtype=torch.float32, device="cuda")
+    out = torch.empty((M, K), dtype=torch.float32, device="cuda")
+    fp4.fp4_dequantize(dev(ref["codes"]), dev(ref["scales"].reshape(-1)), fp4.FP4_SFLAYOUT_PLAIN, M, K, fmt, g,
+                       fp4.FP4_OUT_F32, out)
+    assert np.array_equal(host(out), Q.dequantize(ref["codes"], ref["scales"], fmt, ref["amax"]))
+
+
+@pytest.mark.parametrize("fmt", Q.SWEEP_FORMATS)
+def test_sweep_formats_encode_every_code(fmt):
+    # every non-negative code's value, its neighbours' midpoints and values just
+    # around them encode as the oracle's nearest-even, saturating rule does
+    fp4 = lib()
+    vals = F.CODECS[fmt].vals
+    mids = (vals[1:] + vals[:-1]) / 2
+    probe = np.concatenate([vals, mids, np.nextafter(mids.astype(np.float32), np.float32(0)),
+                            np.nextafter(mids.astype(np.float32), np.float32(np.inf)), [vals[-1] * 2, 3e38]])
+    probe = probe.astype(np.float32)
+    s = torch.from_numpy(probe).cuda()
+    codes = torch.empty(probe.size, dtype=torch.uint8, device="cuda")
+    dec = torch.empty(probe.size, dtype=torch.float32, device="cuda")
+    fp4.fp4_encode_scales(s, fmt, codes, dec)
+    want = F.CODECS[fmt].encode(probe)
+    assert np.array_equal(host(codes), want)
+    assert np.array_equal(host(dec), F.CODECS[fmt].decode(want).astype(np.float32))
