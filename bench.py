@@ -311,14 +311,14 @@ def quantizer_modes(step, flush, reps=5):
     return out
 
 
-SWEEP_FORMATS = ["E4M3", "UE5M3", "E8M0", "E1M6", "E2M5", "E3M4", "E5M2", "E6M1", "E7M0"]
+SWEEP_FORMATS = ["E4M3", "UE5M3", "E8M0", "E1M6", "E2M5", "E3M4", "E5M2", "E6M1", "E7M0", "NVINT4", "MXINT4"]
 
 
 def scale_format_sweep(fp4, flush, device, reps=5):
     """Row quantizer (RNE, fresh amax given) on the 350M-parameter MLP input
     X 8192x1024 (per-column sigma log-uniform in [0.1, 10]) for every scale
-    format: GB/s at 2 + 0.5 + 1/G B/elem, and the relative RMS error of the
-    dequantized tensor.  Outside the timed step."""
+    format and both INT4 grids: GB/s at 2 + 0.5 + 1/G B/elem, and the relative
+    RMS error of the dequantized tensor.  Outside the timed step."""
     from fp4_block_scaled_amax_gb300 import synth
     x = synth.config2()["X"].to(device)
     M, K = x.shape
@@ -330,7 +330,7 @@ def scale_format_sweep(fp4, flush, device, reps=5):
     st = torch.cuda.current_stream()
     deq = torch.empty((M, K), dtype=torch.float32, device=device)
     for f in SWEEP_FORMATS:
-        G = 32 if f == "E8M0" else 16
+        G = 32 if f in ("E8M0", "MXINT4") else 16
         codes = torch.empty((M, K // 2), dtype=torch.uint8, device=device)
         scales = torch.empty(M * K // G, dtype=torch.uint8, device=device)
         def run():

@@ -18,14 +18,15 @@ fp4_status cuda_status(cudaError_t e) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-bool valid_fmt(int f) { return f >= FP4_SF_E4M3 && f <= FP4_SF_E7M0; }
+bool valid_fmt(int f) { return f >= FP4_SF_E4M3 && f <= FP4_SF_MXINT4; }
 
-// E2M5 .. E7M0: the rest of the scale-format sweep, row quantization only
-bool sweep_fmt(int f) { return f >= FP4_SF_E2M5 && f <= FP4_SF_E7M0; }
+// E2M5 .. E7M0 (the rest of the scale-format sweep) and the INT4 grids:
+// row quantization only
+bool sweep_fmt(int f) { return f >= FP4_SF_E2M5 && f <= FP4_SF_MXINT4; }
 
 int group_of(int f) {
   if (!valid_fmt(f)) return 0;
-  return f == FP4_SF_E8M0 ? 32 : 16;
+  return (f == FP4_SF_E8M0 || f == FP4_SF_MXINT4) ? 32 : 16;
 }
 
 // Checks shared by the quantizer entry points.  rows/cols are the OUTPUT

@@ -95,8 +95,19 @@ enum : int {
   SF_E3M4 = FP4_SF_E3M4,
   SF_E5M2 = FP4_SF_E5M2,
   SF_E6M1 = FP4_SF_E6M1,
-  SF_E7M0 = FP4_SF_E7M0
+  SF_E7M0 = FP4_SF_E7M0,
+  SF_NVINT4 = FP4_SF_NVINT4,
+  SF_MXINT4 = FP4_SF_MXINT4
 };
+
+// Element grid of a format: E2M1 (largest magnitude 6) or, for NVINT4 and
+// MXINT4, the integers -7..7 as two's-complement nibbles (largest 7).
+template <int FMT> struct Elem { static constexpr bool INT4 = false; };
+template <> struct Elem<SF_NVINT4> { static constexpr bool INT4 = true; };
+template <> struct Elem<SF_MXINT4> { static constexpr bool INT4 = true; };
+template <int FMT> __host__ __device__ constexpr float elem_max() { return Elem<FMT>::INT4 ? 7.0f : 6.0f; }
+// Power-of-two (E8M0) block scales without a global scale: MXFP4 and MXINT4
+template <int FMT> __host__ __device__ constexpr bool e8m0_scales() { return FMT == SF_E8M0 || FMT == SF_MXINT4; }
 
 template <int FMT> struct ScaleFmt;
 // E4M3 (FN) nearest-even with saturation to 448 is the hardware conversion;
@@ -156,16 +167,24 @@ template <> struct ScaleFmt<SF_E8M0> {
   }
 };
 
+// NVINT4: E4M3 scales with the numerator f32(7 * 448); MXINT4: E8M0 scales.
+template <> struct ScaleFmt<SF_NVINT4> : ScaleFmt<SF_E4M3> {
+  static constexpr float SIX_ST = 3136.0f;  // 7 * 448: the INT4 grid tops out at 7
+};
+template <> struct ScaleFmt<SF_MXINT4> : ScaleFmt<SF_E8M0> {};
+
+// f32(emax * S_T), the numerator of s_enc (SIX_ST: "6 * S_T" for E2M1 grids,
+// 7 * S_T for NVINT4).
 template <int FMT>
 __device__ __forceinline__ float six_st_of() {
-  if constexpr (FMT >= SF_E2M5) return ScaleFmt<FMT>::six_st();
+  if constexpr (FMT >= SF_E2M5 && FMT <= SF_E7M0) return ScaleFmt<FMT>::six_st();
   else return ScaleFmt<FMT>::SIX_ST;
 }
 
 // Per-tensor encode scale from the stored amax g.
 template <int FMT>
 __device__ __forceinline__ float global_encode_scale(float g, int32_t* status) {
-  if (FMT == SF_E8M0) return 1.0f;
+  if (e8m0_scales<FMT>()) return 1.0f;
   if (!(fabsf(g) <= 3.402823466e38f)) {  // Inf or NaN
     set_status(status, FP4_ERR_NONFINITE);
     return 1.0f;
@@ -191,10 +210,10 @@ __device__ __forceinline__ float code_multiplier(uint32_t code, float s_enc) {
 template <int FMT>
 __device__ __forceinline__ BlockScale block_scale_tab(float a_b, float s_enc, const float* rtab) {
   BlockScale out;
-  if constexpr (FMT == SF_E8M0) {
+  if constexpr (e8m0_scales<FMT>()) {
     out.code = ScaleFmt<SF_E8M0>::encode_from_amax(a_b);
   } else {
-    out.code = ScaleFmt<FMT>::encode(__fmul_rn(__fdiv_rn(a_b, 6.0f), s_enc));
+    out.code = ScaleFmt<FMT>::encode(__fmul_rn(__fdiv_rn(a_b, elem_max<FMT>()), s_enc));
   }
   out.r = rtab[out.code];
   return out;
@@ -204,11 +223,11 @@ template <int FMT>
 __device__ __forceinline__ BlockScale block_scale(float a_b, float s_enc) {
   BlockScale out;
   float s_b;
-  if constexpr (FMT == SF_E8M0) {
+  if constexpr (e8m0_scales<FMT>()) {
     out.code = ScaleFmt<SF_E8M0>::encode_from_amax(a_b);
     s_b = ScaleFmt<SF_E8M0>::decode(out.code);
   } else {
-    const float s_real = __fmul_rn(__fdiv_rn(a_b, 6.0f), s_enc);
+    const float s_real = __fmul_rn(__fdiv_rn(a_b, elem_max<FMT>()), s_enc);
     out.code = ScaleFmt<FMT>::encode(s_real);
     s_b = ScaleFmt<FMT>::decode(out.code);
   }
@@ -257,6 +276,26 @@ __device__ __forceinline__ float e2m1_sr_value(float x, float r, uint32_t rbits)
   const float c = __fsub_rn(__fadd_ru(t, 12582912.0f), 12582912.0f);
   return __fmul_rn(c, __uint_as_float((eb - 0x00800000u) | (__float_as_uint(x) & 0x80000000u)));
 }
+// INT4 grid (integers -7..7, two's-complement nibble): nearest with ties to
+// even after clamping to [-7, 7]; adding 1.5 * 2^23 rounds to an integer in
+// float32 and leaves it in the low mantissa bits.
+__device__ __forceinline__ uint32_t int4_rne(float y) {
+  const float yc = fminf(fmaxf(y, -7.0f), 7.0f);
+  return (__float_as_uint(__fadd_rn(yc, 12582912.0f)) - 0x4B400000u) & 0xFu;
+}
+// INT4 stochastic rounding: ceil(min(|y|, 7) - r * 2^-16) with the sign of x.
+// The grid step is 1, so the argument of e2m1_sr_value holds with z = |y|:
+// near an integer n in 1..6 the float32 difference is off by at least
+// ulp(z) >= 2^-21 > ulp(n)/2, and below 1 it is exact.  -0 becomes code 0.
+__device__ __forceinline__ uint32_t int4_sr(float x, float r, uint32_t rbits) {
+  const float ay = fminf(__fmul_rn(fabsf(x), r), 7.0f);
+  const float rho = __fsub_rn(__uint_as_float(rbits), 1.0f);
+  const float t = __fsub_rn(ay, rho);
+  const float c = __fsub_rn(__fadd_ru(t, 12582912.0f), 12582912.0f);
+  const float v = __uint_as_float(__float_as_uint(c) | (__float_as_uint(x) & 0x80000000u));
+  return (__float_as_uint(__fadd_rn(v, 12582912.0f)) - 0x4B400000u) & 0xFu;
+}
+
 // 1 + r * 2^-16 for the low and high 16-bit halves of a Philox word.
 __device__ __forceinline__ uint32_t sr_rbits_lo(uint32_t w) { return 0x3F800000u | ((w << 7) & 0x007FFF80u); }
 __device__ __forceinline__ uint32_t sr_rbits_hi(uint32_t w) { return 0x3F800000u | ((w >> 9) & 0x007FFF80u); }
@@ -315,8 +354,36 @@ __device__ __forceinline__ uint32_t e2m1x8_rne(const float* y) {
   return r;
 }
 
-template <bool SR>
+template <bool SR, bool INT4 = false>
 __device__ __forceinline__ uint2 quant16(const uint32_t* w, float r, uint64_t seed, uint64_t idx0) {
+  if constexpr (INT4) {
+    uint32_t nib[16];
+    if constexpr (!SR) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        nib[2 * i] = int4_rne(__fmul_rn(bf16_lo(w[i]), r));
+        nib[2 * i + 1] = int4_rne(__fmul_rn(bf16_hi(w[i]), r));
+      }
+    } else {
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const uint4 d = sr_draws8(seed, (idx0 >> 3) + h);
+        const uint32_t dw[4] = {d.x, d.y, d.z, d.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          nib[8 * h + 2 * i] = int4_sr(bf16_lo(w[4 * h + i]), r, sr_rbits_lo(dw[i]));
+          nib[8 * h + 2 * i + 1] = int4_sr(bf16_hi(w[4 * h + i]), r, sr_rbits_hi(dw[i]));
+        }
+      }
+    }
+    uint2 out = make_uint2(0u, 0u);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      out.x |= nib[i] << (4 * i);
+      out.y |= nib[8 + i] << (4 * i);
+    }
+    return out;
+  }
   float y[16];
   if constexpr (!SR) {
 #pragma unroll

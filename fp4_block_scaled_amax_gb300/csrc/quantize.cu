@@ -119,7 +119,7 @@ __global__ void __launch_bounds__(256) k_quant_rows(const uint16_t* __restrict__
   }
   if constexpr (G == 32) a = fmaxf(a, __shfl_xor_sync(mask, a, 1));
   const BlockScale bs = block_scale<FMT>(a, s_enc);
-  const uint2 q = quant16<SR>(w, bs.r, seed, (uint64_t)(row * K + c16 * 16));
+  const uint2 q = quant16<SR, Elem<FMT>::INT4>(w, bs.r, seed, (uint64_t)(row * K + c16 * 16));
   *reinterpret_cast<uint2*>(codes + row * (K / 2) + c16 * 8) = q;
   if (G == 16 || (c16 & 1) == 0) {
     const int64_t b = c16 * 16 / G;
@@ -282,7 +282,8 @@ __global__ void __launch_bounds__(256) k_dequant(const uint8_t* __restrict__ cod
   for (int i = 0; i < 16; ++i) {
     const uint32_t word = i < 8 ? q.x : q.y;
     const uint32_t n = (word >> (4 * (i & 7))) & 0xFu;
-    v[i] = __fdiv_rn(__fmul_rn(e2m1_value(n), s_b), s_enc);
+    const float e = Elem<FMT>::INT4 ? (float)((int)n - ((int)n & 8) * 2) : e2m1_value(n);
+    v[i] = __fdiv_rn(__fmul_rn(e, s_b), s_enc);
   }
   if constexpr (BF16) {
     uint32_t o[8];
@@ -349,7 +350,7 @@ __global__ void __launch_bounds__(256) k_encode_scales(const float* __restrict__
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= n) return;
   uint32_t c;
-  if constexpr (FMT == SF_E8M0) c = ScaleFmt<SF_E8M0>::encode_from_amax(s[i]);
+  if constexpr (e8m0_scales<FMT>()) c = ScaleFmt<SF_E8M0>::encode_from_amax(s[i]);
   else c = ScaleFmt<FMT>::encode(s[i]);
   codes[i] = (uint8_t)c;
   decoded[i] = ScaleFmt<FMT>::decode(c);
@@ -457,6 +458,8 @@ cudaError_t launch_quantize(const QuantArgs& a, cudaStream_t st) {
     case FP4_SF_E5M2: e = dispatch_rows_only<SF_E5M2>(a, st); break;
     case FP4_SF_E6M1: e = dispatch_rows_only<SF_E6M1>(a, st); break;
     case FP4_SF_E7M0: e = dispatch_rows_only<SF_E7M0>(a, st); break;
+    case FP4_SF_NVINT4: e = dispatch_rows_only<SF_NVINT4>(a, st); break;
+    case FP4_SF_MXINT4: e = dispatch_rows_only<SF_MXINT4>(a, st); break;
     default: return cudaErrorInvalidValue;
   }
   if (e != cudaSuccess) return e;
@@ -483,6 +486,8 @@ cudaError_t launch_dequantize(const uint8_t* codes, const uint8_t* scales, bool 
     case FP4_SF_E5M2: DQ(SF_E5M2) break;
     case FP4_SF_E6M1: DQ(SF_E6M1) break;
     case FP4_SF_E7M0: DQ(SF_E7M0) break;
+    case FP4_SF_NVINT4: DQ(SF_NVINT4) break;
+    case FP4_SF_MXINT4: DQ(SF_MXINT4) break;
     default: return cudaErrorInvalidValue;
   }
 #undef DQ
@@ -517,6 +522,8 @@ cudaError_t launch_encode_scales(const float* s, int64_t n, int fmt, uint8_t* co
     case FP4_SF_E5M2: k_encode_scales<SF_E5M2><<<g, 256, 0, st>>>(s, n, codes, decoded); break;
     case FP4_SF_E6M1: k_encode_scales<SF_E6M1><<<g, 256, 0, st>>>(s, n, codes, decoded); break;
     case FP4_SF_E7M0: k_encode_scales<SF_E7M0><<<g, 256, 0, st>>>(s, n, codes, decoded); break;
+    case FP4_SF_NVINT4: k_encode_scales<SF_NVINT4><<<g, 256, 0, st>>>(s, n, codes, decoded); break;
+    case FP4_SF_MXINT4: k_encode_scales<SF_MXINT4><<<g, 256, 0, st>>>(s, n, codes, decoded); break;
     default: return cudaErrorInvalidValue;
   }
   return cudaGetLastError();

@@ -23,14 +23,16 @@ FP4_OK, FP4_ERR_INVALID_ARG, FP4_ERR_SHAPE, FP4_ERR_ALIGNMENT, FP4_ERR_UNSUPPORT
 FP4_ERR_NONFINITE, FP4_ERR_UE5M3_RANGE, FP4_ERR_TIMEOUT, FP4_ERR_CUDA = 5, 6, 7, 8
 FP4_SF_E4M3, FP4_SF_UE5M3, FP4_SF_E8M0, FP4_SF_E1M6 = 0, 1, 2, 3
 FP4_SF_E2M5, FP4_SF_E3M4, FP4_SF_E5M2, FP4_SF_E6M1, FP4_SF_E7M0 = 4, 5, 6, 7, 8
+FP4_SF_NVINT4, FP4_SF_MXINT4 = 9, 10
 FP4_ROUND_RNE, FP4_ROUND_STOCHASTIC = 0, 1
 FP4_SFLAYOUT_PLAIN, FP4_SFLAYOUT_MMA = 0, 1
 FP4_OUT_F32, FP4_OUT_BF16 = 0, 1
 FP4_LAYOUT_TN = 0
 
 FMT = {"E4M3": FP4_SF_E4M3, "UE5M3": FP4_SF_UE5M3, "E8M0": FP4_SF_E8M0, "E1M6": FP4_SF_E1M6,
-       "E2M5": FP4_SF_E2M5, "E3M4": FP4_SF_E3M4, "E5M2": FP4_SF_E5M2, "E6M1": FP4_SF_E6M1, "E7M0": FP4_SF_E7M0}
-GROUP = {f: (32 if f == FP4_SF_E8M0 else 16) for f in FMT.values()}
+       "E2M5": FP4_SF_E2M5, "E3M4": FP4_SF_E3M4, "E5M2": FP4_SF_E5M2, "E6M1": FP4_SF_E6M1, "E7M0": FP4_SF_E7M0,
+       "NVINT4": FP4_SF_NVINT4, "MXINT4": FP4_SF_MXINT4}
+GROUP = {f: (32 if f in (FP4_SF_E8M0, FP4_SF_MXINT4) else 16) for f in FMT.values()}
 
 
 class Fp4Error(RuntimeError):

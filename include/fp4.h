@@ -20,6 +20,10 @@
  *   [W4A16]     weight-only NVFP4 post, quant_prune_distill #574, sections
  *               "Метод" (weights only, activations untouched) and
  *               "Эксперименты" (memory-bound kernel for small batches).
+ *   [INT-FP]    post on "INT v.s. FP: A Comprehensive Study of Fine-Grained
+ *               Low-bit Quantization Formats" (quant_prune_distill channel page),
+ *               section "Метод": MXINT4 / NVINT4 beside MXFP4 / NVFP4, the same
+ *               groups and scales on an INT grid.
  *
  * Conventions for every entry point:
  *   - Tensor pointers are DEVICE pointers owned by the caller; the library
@@ -82,7 +86,15 @@ typedef enum {
   FP4_SF_E3M4 = 5,  /* max 31 */
   FP4_SF_E5M2 = 6,  /* max 114688 */
   FP4_SF_E6M1 = 7,  /* max 1.5 * 2^32 */
-  FP4_SF_E7M0 = 8   /* max 2^64 */
+  FP4_SF_E7M0 = 8,  /* max 2^64 */
+  /* INT4 element grid instead of E2M1 ([INT-FP] "Метод": NV = groups of 16
+   * with E4M3 scales, MX = groups of 32 with E8M0 scales): elements are the
+   * integers -7..7 stored as two's-complement nibbles; every 6 of the E2M1
+   * method becomes 7 (s_enc = f32(f32(7*448)/g), s_real = f32(f32(a_b/7)*s_enc),
+   * E8M0 exponent floor(log2 a_b) - 2); RNE ties to even, SR as for E2M1.
+   * Row quantization, fp4_dequantize and fp4_encode_scales only. */
+  FP4_SF_NVINT4 = 9,
+  FP4_SF_MXINT4 = 10
 } fp4_scale_fmt;
 
 typedef enum {

@@ -35,6 +35,16 @@ round-to-nearest-even; G is the group size):
 5. Packing: byte j holds element 2j in its low nibble, element 2j+1 in its high
    nibble.  Scales: one byte per block, row-major [R, C/G].
 6. Dequantization: f32(f32(e2m1 * s_b) / s_enc).
+
+INT element grids (post on "INT v.s. FP: A Comprehensive Study of Fine-Grained
+Low-bit Quantization Formats", quant_prune_distill channel page, section
+"Метод": NVINT4 = groups of 16 with E4M3 scales, MXINT4 = groups of 32 with
+E8M0 scales, on an INT grid instead of the FP one).  Readings fixed here: the grid is the
+integers -7..7, stored as a 4-bit two's-complement nibble (no negative zero);
+every "6" above becomes 7 (s_enc = f32(f32(7 * 448) / g) for NVINT4, s_real =
+f32(f32(a_b / 7) * s_enc)); MXINT4's E8M0 block exponent is floor(log2 a_b) - 2
+(2 = floor(log2 7)); rounding is nearest with ties to even, or stochastic with
+the same 16-bit rule (up iff r < 65536 * frac(|y|)); |y| >= 7 gives 7.
 """
 
 from __future__ import annotations
@@ -44,7 +54,9 @@ import numpy as np
 from . import formats as F
 from .philox import sr_bits16
 
-GROUP = {"E4M3": 16, "UE5M3": 16, "E1M6": 16, "E8M0": 32}
+GROUP = {"E4M3": 16, "UE5M3": 16, "E1M6": 16, "E8M0": 32, "NVINT4": 16, "MXINT4": 32}
+# INT4 element grid: the scale codec each INT format uses, and the element maximum
+INT_SCALE = {"NVINT4": "E4M3", "MXINT4": "E8M0"}
 SCALE_TARGET = {"E4M3": 448.0, "UE5M3": 448.0, "E1M6": 3.96875}
 # the rest of the group-16 scale-format sweep (gonzo_ML #3986, "Форматы FP4"):
 # generic ExMy scales, target = the format's largest finite value
@@ -52,6 +64,20 @@ SWEEP_FORMATS = ("E2M5", "E3M4", "E5M2", "E6M1", "E7M0")
 for _name in SWEEP_FORMATS:
     GROUP[_name] = 16
     SCALE_TARGET[_name] = F.SWEEP[_name].max_finite()
+SCALE_TARGET["NVINT4"] = 448.0
+
+
+def is_int(fmt: str) -> bool:
+    return fmt in INT_SCALE
+
+
+def elem_max(fmt: str) -> float:
+    """Largest element magnitude of the format's grid: 6 (E2M1) or 7 (INT4)."""
+    return 7.0 if is_int(fmt) else 6.0
+
+
+def scale_codec_name(fmt: str) -> str:
+    return INT_SCALE.get(fmt, fmt)
 FLT_MAX = np.float32(np.finfo(np.float32).max)
 
 
@@ -74,7 +100,7 @@ def storage_bytes(rows: int, cols: int, fmt: str) -> tuple:
 
 def global_encode_scale(g, fmt: str) -> np.float32:
     """Step 1: the per-tensor float32 encode scale from the stored amax g."""
-    if fmt == "E8M0":
+    if scale_codec_name(fmt) == "E8M0":
         return np.float32(1.0)
     g = np.float32(g)
     if not np.isfinite(g):
@@ -82,7 +108,7 @@ def global_encode_scale(g, fmt: str) -> np.float32:
     if g == 0:
         return np.float32(1.0)
     with np.errstate(over="ignore"):
-        s = np.float32(np.float32(6.0) * np.float32(SCALE_TARGET[fmt])) / g
+        s = np.float32(np.float32(elem_max(fmt)) * np.float32(SCALE_TARGET[fmt])) / g
     if np.isinf(s):
         s = FLT_MAX
     return np.float32(s)
@@ -91,13 +117,15 @@ def global_encode_scale(g, fmt: str) -> np.float32:
 def block_scales(a_b: np.ndarray, s_enc: np.float32, fmt: str):
     """Step 3: scale codes (uint8) and their float32 values from block amaxes."""
     a_b = np.asarray(a_b, dtype=np.float32)
+    emax = np.float32(elem_max(fmt))
+    fmt = scale_codec_name(fmt)
     if fmt == "E8M0":
         e = F.f32_floor_log2_biased(a_b)  # floor(log2 a_b) + 127 for normals
         code = np.where(e > 0, e - 2, 0)
         code = np.clip(code, 0, 254).astype(np.uint8)
         s_b = np.ldexp(np.float32(1.0), code.astype(np.int32) - 127).astype(np.float32)
         return code, s_b
-    s_real = np.float32(a_b / np.float32(6.0)) * s_enc
+    s_real = np.float32(a_b / emax) * s_enc
     s_real = s_real.astype(np.float32)
     codec = F.CODECS[fmt]
     code = codec.encode(s_real)
@@ -124,6 +152,19 @@ def _round_sr(ay: np.ndarray, r16: np.ndarray) -> np.ndarray:
     return out.astype(np.uint8)
 
 
+def _int_round_rne(ay: np.ndarray) -> np.ndarray:
+    """INT4 magnitude: nearest integer, ties to even, saturating at 7."""
+    return np.minimum(np.rint(ay.astype(np.float64)), 7).astype(np.int64)
+
+
+def _int_round_sr(ay: np.ndarray, r16: np.ndarray) -> np.ndarray:
+    """INT4 magnitude by stochastic rounding with 16-bit draws (|y| >= 7 -> 7)."""
+    ay64 = ay.astype(np.float64)
+    lo = np.floor(ay64)
+    up = r16.astype(np.float64) < (ay64 - lo) * 65536.0
+    return np.minimum(lo + up, 7).astype(np.int64)
+
+
 def quantize_rows(x: np.ndarray, fmt: str, rounding: str, seed: int, g,
                   row0: int = 0):
     """Quantize row blocks of a float32 array x [R, C] (bf16 values).
@@ -147,15 +188,20 @@ def quantize_rows(x: np.ndarray, fmt: str, rounding: str, seed: int, g,
     y = (xb * r_b[:, :, None]).astype(np.float32)
     ay = np.abs(y).reshape(R, C)
     if rounding == "rne":
-        mag = _round_rne(ay)
+        mag = _int_round_rne(ay) if is_int(fmt) else _round_rne(ay)
     elif rounding == "sr":
         idx = (np.arange(R, dtype=np.uint64)[:, None] + np.uint64(row0)) * np.uint64(C) \
             + np.arange(C, dtype=np.uint64)[None, :]
-        mag = _round_sr(ay, sr_bits16(seed, idx))
+        r16 = sr_bits16(seed, idx)
+        mag = _int_round_sr(ay, r16) if is_int(fmt) else _round_sr(ay, r16)
     else:
         raise ValueError(rounding)
-    mag = np.where(np.repeat(zero_blk, G, axis=1), 0, mag).astype(np.uint8)
-    q = mag | (F.f32_sign_bit(x) << 3)
+    mag = np.where(np.repeat(zero_blk, G, axis=1), 0, mag)
+    if is_int(fmt):
+        # two's complement nibble of sign(x) * mag (no negative zero)
+        q = (np.where(F.f32_sign_bit(x) == 1, -mag, mag) & 0xF).astype(np.uint8)
+    else:
+        q = mag.astype(np.uint8) | (F.f32_sign_bit(x) << 3)
     codes = (q[:, 0::2] | (q[:, 1::2] << 4)).astype(np.uint8)
     return codes, scode
 
@@ -192,8 +238,17 @@ def unpack(codes: np.ndarray) -> np.ndarray:
     return out
 
 
+def element_values(codes: np.ndarray, fmt: str) -> np.ndarray:
+    """float64 values of 4-bit element codes: E2M1, or two's-complement INT4."""
+    codes = np.asarray(codes, dtype=np.int64)
+    if is_int(fmt):
+        return np.where(codes >= 8, codes - 16, codes).astype(np.float64)
+    return F.e2m1_decode(codes)
+
+
 def scale_values(scales: np.ndarray, fmt: str) -> np.ndarray:
     """float64 values of scale codes."""
+    fmt = scale_codec_name(fmt)
     if fmt == "E8M0":
         return np.ldexp(1.0, np.asarray(scales, dtype=np.int64) - 127)
     return F.CODECS[fmt].decode(scales)
@@ -203,7 +258,7 @@ def dequantize(codes, scales, fmt: str, global_amax) -> np.ndarray:
     """Step 6: float32 f32(f32(e2m1 * s_b) / s_enc)."""
     s_enc = global_encode_scale(global_amax, fmt)
     G = GROUP[fmt]
-    e = F.e2m1_decode(unpack(codes)).astype(np.float32)
+    e = element_values(unpack(codes), fmt).astype(np.float32)
     s_b = np.repeat(scale_values(scales, fmt).astype(np.float32), G, axis=1)
     return ((e * s_b).astype(np.float32) / s_enc).astype(np.float32)
 
@@ -212,7 +267,7 @@ def dequantize_f64(codes, scales, fmt: str, global_amax) -> np.ndarray:
     """float64 e2m1 * s_b / s_enc: the operand values of the reference GEMM."""
     s_enc = float(global_encode_scale(global_amax, fmt))
     G = GROUP[fmt]
-    e = F.e2m1_decode(unpack(codes))
+    e = element_values(unpack(codes), fmt)
     s_b = np.repeat(scale_values(scales, fmt), G, axis=1)
     return e * s_b / s_enc
 

@@ -40,7 +40,9 @@ def test_group_size_and_storage_bytes():
     assert fp4.fp4_group_size("E1M6") == 16
     for f in ("E2M5", "E3M4", "E5M2", "E6M1", "E7M0"):
         assert fp4.fp4_group_size(f) == 16
-    assert fp4._lib().fp4_group_size(9) == 0
+    assert fp4.fp4_group_size("NVINT4") == 16
+    assert fp4.fp4_group_size("MXINT4") == 32
+    assert fp4._lib().fp4_group_size(11) == 0
     cb, sb = fp4.fp4_storage_bytes(64, 1024, "E4M3")
     assert (cb + sb) * 8 / (64 * 1024) == 4.5
     cb, sb = fp4.fp4_storage_bytes(64, 1024, "E8M0")
@@ -70,7 +72,7 @@ def q(**kw):
 
 
 def test_quantize_argument_errors():
-    assert q(f=9) == fp4.FP4_ERR_INVALID_ARG
+    assert q(f=11) == fp4.FP4_ERR_INVALID_ARG
     assert q(r=3) == fp4.FP4_ERR_INVALID_ARG
     assert q(tr=2) == fp4.FP4_ERR_INVALID_ARG
     assert q(K=40, ldx=40) == fp4.FP4_ERR_SHAPE           # K not a multiple of 16
@@ -122,10 +124,11 @@ def test_gemv_and_misc_argument_errors():
 
 
 def test_sweep_formats_rows_only():
-    # E2M5 .. E7M0 quantize along rows only: the transposed and dual layouts and
+    # E2M5 .. E7M0 and the INT4 grids quantize along rows only: the transposed and dual layouts and
     # the GEMM report FP4_ERR_UNSUPPORTED before anything is launched
     lib = _need_lib()
-    for f in (fp4.FP4_SF_E2M5, fp4.FP4_SF_E3M4, fp4.FP4_SF_E5M2, fp4.FP4_SF_E6M1, fp4.FP4_SF_E7M0):
+    for f in (fp4.FP4_SF_E2M5, fp4.FP4_SF_E3M4, fp4.FP4_SF_E5M2, fp4.FP4_SF_E6M1, fp4.FP4_SF_E7M0,
+              fp4.FP4_SF_NVINT4):
         assert q(f=f, tr=1) == fp4.FP4_ERR_UNSUPPORTED
         assert lib.fp4_quantize_dual(P, 64, 64, 64, f, 0, 0, 0, 0, P, 0, P, P, P, P, None, None,
                                      None) == fp4.FP4_ERR_UNSUPPORTED

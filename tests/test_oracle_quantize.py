@@ -5,6 +5,7 @@ import pytest
 import torch
 
 from oracle import formats as F
+from oracle import philox as P
 from oracle import quantize as Q
 from oracle.amax import AmaxState
 
@@ -298,3 +299,61 @@ def test_sweep_requantize_fixed_point(fmt):
     c1 = Q.unpack(q["codes"]).reshape(128, -1, 16)[keep]
     c2 = Q.unpack(q2["codes"]).reshape(128, -1, 16)[keep]
     assert np.array_equal(c1, c2)
+
+
+# ---------------------------------------------------------------------------
+# INT4 element grids: NVINT4 (E4M3 scales, group 16), MXINT4 (E8M0, group 32)
+# ---------------------------------------------------------------------------
+
+def test_int4_closed_forms():
+    x = np.ones((4, 64), dtype=np.float32)
+    # NVINT4, fresh amax 1: s_enc = 7 * 448, s_real = 448 -> 0x7E, y = 7 -> nibble 0x7
+    q = Q.quantize(x, "NVINT4")
+    assert q["s_enc"] == np.float32(3136.0)
+    assert np.all(q["scales"] == 0x7E) and np.all(q["codes"] == 0x77)
+    q = Q.quantize(-x, "NVINT4")
+    assert np.all(q["codes"] == 0x99)  # -7 in two's complement
+    # MXINT4: integers with block maximum 4 keep scale 2^0 and their own values
+    rng = np.random.default_rng(3)
+    xi = rng.integers(-4, 5, (8, 64)).astype(np.float32)
+    xi[:, ::32] = 4.0
+    q = Q.quantize(xi, "MXINT4")
+    assert np.all(q["scales"] == 127)
+    assert np.array_equal(Q.element_values(Q.unpack(q["codes"]), "MXINT4"), xi)
+    assert np.array_equal(Q.dequantize(q["codes"], q["scales"], "MXINT4", 0), xi)
+
+
+def test_int4_rne_ties_and_no_negative_zero():
+    # one NVINT4 block with amax 7 and g = 7: s_enc = 448, s_b = 448, r = 1 -> y = x
+    x = np.array([[7, 0.5, 1.5, 2.5, -0.5, -1.5, -2.5, 3.5, -0.25, -0.0, 6.5, -6.5, 4.5, 5.5, 0.75, -7]],
+                 dtype=np.float32)
+    q = Q.quantize(x, "NVINT4")
+    assert q["scales"][0, 0] == 0x7E
+    got = Q.element_values(Q.unpack(q["codes"]), "NVINT4")[0]
+    assert np.array_equal(got, [7, 0, 2, 2, 0, -2, -2, 4, 0, 0, 6, -6, 4, 6, 1, -7])
+    nib = Q.unpack(q["codes"])[0]
+    assert nib[8] == 0 and nib[9] == 0  # -0.25 and -0.0 give code 0 (two's complement has no -0)
+
+
+@pytest.mark.parametrize("fmt,mags", [("NVINT4", {7}), ("MXINT4", {4, 5, 6, 7})])
+def test_int4_block_max_invariant(fmt, mags):
+    x = _data(0, (256, 512))
+    q = Q.quantize(x, fmt)
+    G = Q.group_size(fmt)
+    mag = np.abs(Q.element_values(Q.unpack(q["codes"]), fmt)).reshape(256, 512 // G, G).max(axis=2)
+    s = Q.scale_values(q["scales"], fmt)
+    normal = s >= (2.0 ** -6 if fmt == "NVINT4" else 0)
+    assert normal.mean() > 0.99
+    assert np.all(np.isin(mag[normal], list(mags)))
+
+
+@pytest.mark.parametrize("y", [0.30078125, 1.8125, 3.5, 6.40625])
+def test_int4_sr_unbiased_4sigma(y):
+    n = 1 << 20
+    r16 = P.sr_bits16(99, np.arange(n, dtype=np.uint64))
+    v = Q._int_round_sr(np.full(n, y, dtype=np.float32), r16).astype(np.float64)
+    lo = np.floor(y)
+    p = y - lo
+    sigma = np.sqrt(p * (1 - p) / n)
+    assert abs(v.mean() - y) < 4 * sigma + 1e-12
+    assert set(np.unique(v)) <= {lo, lo + 1}

@@ -208,3 +208,27 @@ def test_sweep_formats_encode_every_code(fmt):
     want = F.CODECS[fmt].encode(probe)
     assert np.array_equal(host(codes), want)
     assert np.array_equal(host(dec), F.CODECS[fmt].decode(want).astype(np.float32))
+
+
+@pytest.mark.parametrize("fmt", ["NVINT4", "MXINT4"])
+@pytest.mark.parametrize("rounding", ["rne", "sr"])
+def test_int4_grids_rows(fmt, rounding):
+    x = synth.config2(scale=8)["X"]
+    check(x, fmt, rounding, 81)
+    check(x, fmt, rounding, 82, mma=True)
+    check(x, fmt, rounding, 83, g=float(x.float().abs().max()) / 5)
+    y = synth.normal((128, 512), 10, 0, outlier_p=0.01, outlier_mult=50.0)
+    check(y, fmt, rounding, 84)
+
+
+@pytest.mark.parametrize("fmt", ["NVINT4", "MXINT4"])
+def test_int4_grids_dequantize(fmt):
+    fp4 = lib()
+    x = synth.config2(scale=8)["X"]
+    M, K = x.shape
+    ref = Q.quantize(f32(x), fmt, "sr", 5)
+    g = torch.tensor([ref["amax"]], dtype=torch.float32, device="cuda")
+    out = torch.empty((M, K), dtype=torch.float32, device="cuda")
+    fp4.fp4_dequantize(dev(ref["codes"]), dev(ref["scales"].reshape(-1)), fp4.FP4_SFLAYOUT_PLAIN, M, K, fmt, g,
+                       fp4.FP4_OUT_F32, out)
+    assert np.array_equal(host(out), Q.dequantize(ref["codes"], ref["scales"], fmt, ref["amax"]))
