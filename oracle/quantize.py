@@ -53,6 +53,7 @@ import numpy as np
 
 from . import formats as F
 from .philox import sr_bits16
+from .rht import rht16
 
 GROUP = {"E4M3": 16, "UE5M3": 16, "E1M6": 16, "E8M0": 32, "NVINT4": 16, "MXINT4": 32}
 # INT4 element grid: the scale codec each INT format uses, and the element maximum
@@ -207,14 +208,20 @@ def quantize_rows(x: np.ndarray, fmt: str, rounding: str, seed: int, g,
 
 
 def quantize(x: np.ndarray, fmt: str = "E4M3", rounding: str = "rne", seed: int = 0,
-             global_amax=None, transpose: bool = False, chunk_rows: int = 1024):
+             global_amax=None, transpose: bool = False, chunk_rows: int = 1024, rht_mask=None):
     """Quantize x [M, K] (float32 holding bf16 values).
 
     global_amax None -> the fresh amax of x.  transpose=True quantizes x^T
     (blocks along the original rows; output layout [K, M], Philox indices in
-    that layout).  Returns dict(codes, scales, amax, s_enc).
+    that layout).  rht_mask: apply the 16 x 16 random Hadamard transform with
+    this sign mask to every 16-element block along K first (rows only); the
+    amax is then the transformed tensor's.  Returns dict(codes, scales, amax, s_enc).
     """
     x = np.asarray(x, dtype=np.float32)
+    if rht_mask is not None:
+        if transpose:
+            raise ValueError("the Hadamard transform runs along rows only")
+        x = rht16(x, rht_mask)
     amax = np.float32(np.max(np.abs(x))) if x.size else np.float32(0)
     g = amax if global_amax is None else np.float32(global_amax)
     src = x.T if transpose else x
