@@ -354,6 +354,75 @@ def scale_format_sweep(fp4, flush, device, reps=5):
     return out
 
 
+RHT_MASK = 0xB38D  # sign mask of the 16 x 16 random Hadamard transform (any 16-bit value)
+
+
+def hadamard_study(step, fp4, flush, device, reps=5):
+    """16 x 16 random Hadamard transform before quantization, outside the timed
+    step: (1) its cost on the given-amax E4M3 row quantizer of dY (GB/s with and
+    without the transform, 2.5625 B/elem); (2) relative RMS error of NVFP4 /
+    NVINT4 / MXFP4 / MXINT4 on the 350M MLP input X 8192x1024 with and without
+    the transform (fresh amax; with it, measured against the transformed
+    tensor, whose norm the orthogonal transform keeps)."""
+    from fp4_block_scaled_amax_gb300 import synth
+    hbm = peaks()[0]
+    st = torch.cuda.current_stream()
+
+    def timed(fn):
+        fn()
+        ts = []
+        for _ in range(reps):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(st)
+            fn()
+            e1.record(st)
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        return statistics.median(ts) * 1e3
+
+    x, g = step.dY, step.amax[2:3]
+    cr, srs, _, _ = step.q["dY"]
+    n = x.numel()
+    RNE, MMA = fp4.FP4_ROUND_RNE, fp4.FP4_SFLAYOUT_MMA
+    us_plain = timed(lambda: fp4.fp4_quantize(x, "E4M3", RNE, 0, g, False, MMA, cr, srs, None))
+    us_rht = timed(lambda: fp4.fp4_quantize_rht(x, "E4M3", RNE, 0, RHT_MASK, g, MMA, cr, srs, None))
+    out = {"cost": {"tensor": f"dY {x.shape[0]}x{x.shape[1]}, E4M3 RNE rows, given amax", "unit": "GB/s",
+                    "plain": round(n * 2.5625 / us_plain / 1e3, 1), "with_rht": round(n * 2.5625 / us_rht / 1e3, 1),
+                    "us_plain": round(us_plain, 2), "us_rht": round(us_rht, 2), "peak": hbm}}
+    X = synth.config2()["X"].to(device)
+    M, K = X.shape
+    Xf = X.float()
+    i = torch.arange(16, device=device)
+    par = torch.zeros((16, 16), dtype=torch.int64, device=device)
+    for b in range(4):
+        par += ((i[:, None] & i[None, :]) >> b) & 1
+    H = 1.0 - 2.0 * (par % 2).double()
+    sgn = torch.tensor([-1.0 if (RHT_MASK >> j) & 1 else 1.0 for j in range(16)], dtype=torch.float64, device=device)
+    T = 0.25 * H * sgn[None, :]
+    Xt = (Xf.double().reshape(-1, 16) @ T.T).reshape(M, K)  # reference only (float64)
+    deq = torch.empty((M, K), dtype=torch.float32, device=device)
+    amax = torch.zeros(1, dtype=torch.float32, device=device)
+    errs = {}
+    for f in ("E4M3", "NVINT4", "E8M0", "MXINT4"):
+        G = 32 if f in ("E8M0", "MXINT4") else 16
+        codes = torch.empty((M, K // 2), dtype=torch.uint8, device=device)
+        scales = torch.empty(M * K // G, dtype=torch.uint8, device=device)
+        e = {}
+        for name, use in (("plain", False), ("rht", True)):
+            if use:
+                fp4.fp4_quantize_rht(X, f, RNE, 0, RHT_MASK, None, fp4.FP4_SFLAYOUT_PLAIN, codes, scales, amax)
+                ref = Xt
+            else:
+                fp4.fp4_quantize(X, f, RNE, 0, None, False, fp4.FP4_SFLAYOUT_PLAIN, codes, scales, amax)
+                ref = Xf.double()
+            fp4.fp4_dequantize(codes, scales, fp4.FP4_SFLAYOUT_PLAIN, M, K, f, amax, fp4.FP4_OUT_F32, deq)
+            e[name] = round(float((deq.double() - ref).norm() / ref.norm()), 5)
+        errs[{"E4M3": "NVFP4", "E8M0": "MXFP4"}.get(f, f)] = e
+    out["rel_rmse"] = {"tensor": f"X {M}x{K} (350M MLP input), RNE rows, fresh amax", **errs}
+    return out
+
+
 def make_inputs():
     from fp4_block_scaled_amax_gb300 import synth
     d = synth.config3()
@@ -429,6 +498,7 @@ def run_ours(args, rank, world, local):
 
     qmodes = quantizer_modes(step, flush)
     sweep = scale_format_sweep(step.fp4, flush, device)
+    hadamard = hadamard_study(step, step.fp4, flush, device)
     e2e = None
     if not args.no_e2e:
         e2e = run_e2e(step, d, args, world, device)
@@ -460,6 +530,7 @@ def run_ours(args, rank, world, local):
                               "frac": round(q_gbs / hbm, 4), "traffic": qtraffic_v, "peak_source": src},
         "quantize_modes": qmodes,
         "scale_format_sweep": sweep,
+        "hadamard_16x16": hadamard,
         "amax_gbs": round(a_gbs, 1),
         "gemv_w4a16": {"batch": GEMV_BATCH, "N": N_FFN, "K": K_HID, "us": round(statistics.mean(gemv_ms) * 1e3, 2),
                        "GB/s": round(gv_gbs, 1), "frac": round(gv_gbs / hbm, 4)},

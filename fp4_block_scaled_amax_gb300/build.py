@@ -24,8 +24,8 @@ ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC,
           "--expt-relaxed-constexpr"]
 # the quantizer's float32 steps must stay single correctly rounded operations
-PER_FILE = {"quantize.cu": ["-fmad=false"]}
-SOURCES = ["abi.cu", "quantize.cu", "gemv.cu", "gemm_sm103.cu"]
+PER_FILE = {"quantize.cu": ["-fmad=false"], "rht.cu": ["-fmad=false"]}
+SOURCES = ["abi.cu", "quantize.cu", "rht.cu", "gemv.cu", "gemm_sm103.cu"]
 
 
 def _nvcc() -> str:

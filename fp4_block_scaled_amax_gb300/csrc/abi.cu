@@ -131,6 +131,46 @@ fp4_status fp4_quantize(const void* x_bf16, int64_t M, int64_t K, int64_t ldx, f
   return cuda_status(fp4lib::launch_quantize(a, st));
 }
 
+fp4_status fp4_quantize_rht(const void* x_bf16, int64_t M, int64_t K, int64_t ldx, fp4_scale_fmt f, fp4_rounding r,
+                            uint64_t seed, uint32_t rht_mask, const float* global_amax, fp4_sf_layout sfl,
+                            uint8_t* codes, uint8_t* scales, float* amax_out, int32_t* dev_status,
+                            fp4_stream_t stream) {
+  if (r != FP4_ROUND_RNE && r != FP4_ROUND_STOCHASTIC) return FP4_ERR_INVALID_ARG;
+  if (rht_mask > 0xFFFFu) return FP4_ERR_INVALID_ARG;
+  fp4_status s = check_quant_common(x_bf16, M, K, ldx, (int)f, (int)sfl, M, K);
+  if (s != FP4_OK) return s;
+  if (f != FP4_SF_E4M3 && f != FP4_SF_UE5M3 && f != FP4_SF_E8M0 && f != FP4_SF_NVINT4 && f != FP4_SF_MXINT4)
+    return FP4_ERR_UNSUPPORTED;
+  if (M * K > 0 && (s = check_out(codes, scales)) != FP4_OK) return s;
+  cudaStream_t st = (cudaStream_t)stream;
+  fp4lib::QuantArgs a{};
+  a.mode = fp4lib::QuantArgs::ROWS;
+  a.fmt = (int)f;
+  a.x = x_bf16;
+  a.M = M;
+  a.K = K;
+  a.ldx = ldx;
+  a.mma = sfl == FP4_SFLAYOUT_MMA;
+  a.status = dev_status;
+  a.row_sr = r == FP4_ROUND_STOCHASTIC;
+  a.seed_row = seed;
+  a.codes_row = codes;
+  a.scales_row = scales;
+  a.amax_out = amax_out;
+  if (global_amax == nullptr) {
+    // fresh: max |x'| of the transformed tensor first
+    if (amax_out == nullptr) return FP4_ERR_INVALID_ARG;
+    if ((s = cuda_status(fp4lib::launch_amax_rht(x_bf16, M, K, ldx, rht_mask, amax_out, st))) != FP4_OK) return s;
+    a.gptr = amax_out;
+    a.amax_by_product = false;
+  } else {
+    a.gptr = global_amax;
+    a.amax_by_product = amax_out != nullptr;
+    if (a.amax_by_product && (s = cuda_status(cudaMemsetAsync(amax_out, 0, sizeof(float), st))) != FP4_OK) return s;
+  }
+  return cuda_status(fp4lib::launch_quantize_rht(a, rht_mask, st));
+}
+
 fp4_status fp4_quantize_dual(const void* x_bf16, int64_t M, int64_t K, int64_t ldx, fp4_scale_fmt f,
                              fp4_rounding r_row, uint64_t seed_row, fp4_rounding r_col, uint64_t seed_col,
                              const float* global_amax, fp4_sf_layout sfl, uint8_t* codes_row, uint8_t* scales_row,

@@ -407,6 +407,77 @@ __device__ __forceinline__ uint2 quant16(const uint32_t* w, float r, uint64_t se
   return make_uint2(e2m1x8_rne(y), e2m1x8_rne(y + 8));
 }
 
+// ---------------------------------------------------------------------------
+// 16 x 16 random Hadamard transform of one block held as 16 floats:
+// x' = 1/4 * H16 * (s . x), s[j] = -1 iff bit j of mask is set; the fast
+// Walsh-Hadamard butterflies for h = 1, 2, 4, 8, each add and subtract one
+// float32 operation, then the exact scaling by 1/4.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void rht16(float (&v)[16], uint32_t mask) {
+#pragma unroll
+  for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(__float_as_uint(v[j]) ^ (((mask >> j) & 1u) << 31));
+#pragma unroll
+  for (int h = 1; h < 16; h <<= 1) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      if ((i & h) == 0) {
+        const float a = v[i], b = v[i + h];
+        v[i] = __fadd_rn(a, b);
+        v[i + h] = __fsub_rn(a, b);
+      }
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < 16; ++j) v[j] = __fmul_rn(v[j], 0.25f);
+}
+
+// quant16 for 16 float32 inputs (the transformed block).
+template <bool SR, bool INT4>
+__device__ __forceinline__ uint2 quant16f(const float (&v)[16], float r, uint64_t seed, uint64_t idx0) {
+  if constexpr (INT4) {
+    uint32_t nib[16];
+    if constexpr (!SR) {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) nib[i] = int4_rne(__fmul_rn(v[i], r));
+    } else {
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const uint4 d = sr_draws8(seed, (idx0 >> 3) + h);
+        const uint32_t dw[4] = {d.x, d.y, d.z, d.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          nib[8 * h + 2 * i] = int4_sr(v[8 * h + 2 * i], r, sr_rbits_lo(dw[i]));
+          nib[8 * h + 2 * i + 1] = int4_sr(v[8 * h + 2 * i + 1], r, sr_rbits_hi(dw[i]));
+        }
+      }
+    }
+    uint2 out = make_uint2(0u, 0u);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      out.x |= nib[i] << (4 * i);
+      out.y |= nib[8 + i] << (4 * i);
+    }
+    return out;
+  }
+  float y[16];
+  if constexpr (!SR) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) y[i] = __fmul_rn(v[i], r);
+  } else {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const uint4 d = sr_draws8(seed, (idx0 >> 3) + h);
+      const uint32_t dw[4] = {d.x, d.y, d.z, d.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        y[8 * h + 2 * i] = e2m1_sr_value(v[8 * h + 2 * i], r, sr_rbits_lo(dw[i]));
+        y[8 * h + 2 * i + 1] = e2m1_sr_value(v[8 * h + 2 * i + 1], r, sr_rbits_hi(dw[i]));
+      }
+    }
+  }
+  return make_uint2(e2m1x8_rne(y), e2m1x8_rne(y + 8));
+}
+
 // Byte offset of scale (row r, block b) in the tiled MMA scale layout with nb
 // blocks per row: 128-row x 4-block atoms of 512 bytes, row-major over atoms;
 // inside an atom row r sits at (r%32)*16 + ((r/32)%4)*4, block b at b%4.

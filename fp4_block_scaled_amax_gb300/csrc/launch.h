@@ -28,6 +28,10 @@ cudaError_t launch_ue5m3_to_e4m3(const uint8_t* in, int64_t n, int32_t* t_out, u
 cudaError_t launch_encode_scales(const float* s, int64_t n, int fmt, uint8_t* codes, float* decoded,
                                  cudaStream_t st);
 cudaError_t launch_philox_bits16(uint64_t seed, uint64_t start, int64_t n, uint16_t* out, cudaStream_t st);
+// 16 x 16 random Hadamard transform + row quantization (rht.cu)
+cudaError_t launch_amax_rht(const void* x, int64_t M, int64_t K, int64_t ldx, uint32_t mask, float* out,
+                            cudaStream_t st);
+cudaError_t launch_quantize_rht(const QuantArgs& a, uint32_t mask, cudaStream_t st);
 
 struct GemmArgs {
   const uint8_t *Aq, *As, *Bq, *Bs;

@@ -59,6 +59,8 @@ _SIGS = {
     "fp4_storage_bytes": (_I32, [_I64, _I64, _I32, _SZP, _SZP]),
     "fp4_amax": (_I32, [_VP, _I64, _I64, _I64, _VP, _VP]),
     "fp4_quantize": (_I32, [_VP, _I64, _I64, _I64, _I32, _I32, _U64, _VP, _I32, _I32, _VP, _VP, _VP, _VP, _VP]),
+    "fp4_quantize_rht": (_I32, [_VP, _I64, _I64, _I64, _I32, _I32, _U64, ctypes.c_uint32, _VP, _I32, _VP, _VP, _VP,
+                                _VP, _VP]),
     "fp4_quantize_dual": (_I32, [_VP, _I64, _I64, _I64, _I32, _I32, _U64, _I32, _U64, _VP, _I32,
                                  _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
     "fp4_dequantize": (_I32, [_VP, _VP, _I32, _I64, _I64, _I32, _VP, _I32, _VP, _VP]),
@@ -146,6 +148,14 @@ def fp4_quantize(x, fmt, rounding, seed, global_amax, transpose, sfl, codes, sca
     _check(_lib().fp4_quantize(_ptr(x), M, K, x.stride(0), _fmt(fmt), int(rounding), int(seed),
                                _ptr(global_amax), int(transpose), int(sfl), _ptr(codes), _ptr(scales),
                                _ptr(amax_out), _ptr(dev_status), _stream(stream)), "fp4_quantize")
+
+
+def fp4_quantize_rht(x, fmt, rounding, seed, rht_mask, global_amax, sf_layout, codes, scales, amax_out=None,
+                     dev_status=None, stream=None):
+    M, K = x.shape
+    _check(_lib().fp4_quantize_rht(_ptr(x), M, K, x.stride(0), _fmt(fmt), int(rounding), int(seed), int(rht_mask),
+                                   _ptr(global_amax), int(sf_layout), _ptr(codes), _ptr(scales), _ptr(amax_out),
+                                   _ptr(dev_status), _stream(stream)), "fp4_quantize_rht")
 
 
 def fp4_quantize_dual(x, fmt, r_row, seed_row, r_col, seed_col, global_amax, sfl, codes_row, scales_row,

@@ -153,6 +153,26 @@ fp4_status fp4_quantize(const void* x_bf16, int64_t M, int64_t K, int64_t ldx,
                         uint8_t* codes, uint8_t* scales, float* amax_out,
                         int32_t* dev_status, fp4_stream_t stream);
 
+/* fp4_quantize (row layout) of the 16 x 16 random Hadamard transform of x:
+ * every 16-element block along K first becomes x' = 1/4 * H16 * (s . x), H16
+ * the Sylvester Hadamard matrix (H[i][j] = (-1)^popcount(i & j)), s[j] = -1
+ * iff bit j of rht_mask is set, computed in float32 by the fast Walsh-Hadamard
+ * butterflies (h = 1, 2, 4, 8: (a, b) -> (a + b, a - b)) and the exact 1/4;
+ * the method then runs on x' (block amax, scale, rounding; the global amax g
+ * is max |x'|, fresh when global_amax is NULL).  The transform is orthogonal:
+ * two operands transformed with the same mask along K keep their product, so
+ * fp4_gemm of such operands approximates x * w^T.  ([UE5M3] "Что сделали":
+ * the randomized transform that spreads outliers, dropped from the UE5M3
+ * recipe; [INT-FP] "Метод": Hadamard rotations before MX/NV FP or INT
+ * quantization.)  Formats: E4M3, UE5M3, E8M0, NVINT4, MXINT4 (others:
+ * FP4_ERR_UNSUPPORTED).  rht_mask < 2^16.  Other arguments and requirements
+ * as fp4_quantize with transpose = 0. */
+fp4_status fp4_quantize_rht(const void* x_bf16, int64_t M, int64_t K, int64_t ldx,
+                            fp4_scale_fmt f, fp4_rounding r, uint64_t seed, uint32_t rht_mask,
+                            const float* global_amax, fp4_sf_layout sfl,
+                            uint8_t* codes, uint8_t* scales, float* amax_out,
+                            int32_t* dev_status, fp4_stream_t stream);
+
 /* Row and transposed quantization of one bf16 [M, K] matrix from a single
  * read: writes exactly what fp4_quantize(transpose=0, r_row, seed_row) and
  * fp4_quantize(transpose=1, r_col, seed_col) would, with the same global amax.
