@@ -423,6 +423,48 @@ def hadamard_study(step, fp4, flush, device, reps=5):
     return out
 
 
+def fused_epilogue_study(step, flush, reps=5):
+    """The forward GEMM Y = X W^T with Y quantized for the next layer (NVFP4,
+    RNE rows, the stored amax of Y): the GEMM writing bf16 Y followed by the
+    row quantizer, against the GEMM quantizing Y in its epilogue
+    (fp4_gemm_quantize).  Outside the timed step."""
+    fp4 = step.fp4
+    M, N, K = M_TOK, N_FFN, K_HID
+    qX, qW = step.q["X"], step.q["W"]
+    aX, aW = step.amax[0:1], step.amax[1:2]
+    BF, RNE, MMA = fp4.FP4_OUT_BF16, fp4.FP4_ROUND_RNE, fp4.FP4_SFLAYOUT_MMA
+    dev = step.Y.device
+    codes = torch.empty((M, N // 2), dtype=torch.uint8, device=dev)
+    scales = torch.empty(M * N // 16, dtype=torch.uint8, device=dev)
+    fp4.fp4_gemm(qX[0], qX[1], qW[0], qW[1], aX, aW, None, None, M, N, K, "E4M3", BF, step.Y)
+    gY = step.Y.float().abs().max().reshape(1)  # the stored amax of Y
+    st = torch.cuda.current_stream()
+
+    def two_calls():
+        fp4.fp4_gemm(qX[0], qX[1], qW[0], qW[1], aX, aW, None, None, M, N, K, "E4M3", BF, step.Y)
+        fp4.fp4_quantize(step.Y, "E4M3", RNE, 0, gY, False, MMA, codes, scales, None)
+
+    def one_call():
+        fp4.fp4_gemm_quantize(qX[0], qX[1], qW[0], qW[1], aX, aW, None, None, M, N, K, "E4M3", gY, RNE, 0, MMA,
+                              codes, scales)
+
+    res = {}
+    for name, fn in (("gemm_then_quantize", two_calls), ("gemm_quantize_epilogue", one_call)):
+        fn()
+        ts = []
+        for _ in range(reps):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(st)
+            fn()
+            e1.record(st)
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        res[name] = round(statistics.median(ts), 4)
+    return {"gemm": f"fwd {M}x{N}x{K} E4M3, Y -> NVFP4 rows (RNE, stored amax)", "unit": "ms", **res,
+            "fused_tflops": round(2 * M * N * K / (res["gemm_quantize_epilogue"] * 1e-3) / 1e12, 1)}
+
+
 def make_inputs():
     from fp4_block_scaled_amax_gb300 import synth
     d = synth.config3()
@@ -499,6 +541,7 @@ def run_ours(args, rank, world, local):
     qmodes = quantizer_modes(step, flush)
     sweep = scale_format_sweep(step.fp4, flush, device)
     hadamard = hadamard_study(step, step.fp4, flush, device)
+    fused_ep = fused_epilogue_study(step, flush)
     e2e = None
     if not args.no_e2e:
         e2e = run_e2e(step, d, args, world, device)
@@ -531,6 +574,7 @@ def run_ours(args, rank, world, local):
         "quantize_modes": qmodes,
         "scale_format_sweep": sweep,
         "hadamard_16x16": hadamard,
+        "fused_epilogue_quantize": fused_ep,
         "amax_gbs": round(a_gbs, 1),
         "gemv_w4a16": {"batch": GEMV_BATCH, "N": N_FFN, "K": K_HID, "us": round(statistics.mean(gemv_ms) * 1e3, 2),
                        "GB/s": round(gv_gbs, 1), "frac": round(gv_gbs / hbm, 4)},

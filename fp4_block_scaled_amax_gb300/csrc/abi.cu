@@ -269,6 +269,57 @@ fp4_status fp4_gemm(const uint8_t* Aq, const uint8_t* As, const uint8_t* Bq, con
   return cuda_status(fp4lib::launch_gemm(a, (cudaStream_t)stream));
 }
 
+fp4_status fp4_gemm_quantize(const uint8_t* Aq, const uint8_t* As, const uint8_t* Bq, const uint8_t* Bs,
+                             const float* ga, const float* gb, const int32_t* tA, const int32_t* tB, int64_t M,
+                             int64_t N, int64_t K, fp4_scale_fmt f, fp4_gemm_layout layout, const float* g_out,
+                             fp4_rounding r_out, uint64_t seed_out, fp4_sf_layout sfl_out, uint8_t* C_codes,
+                             uint8_t* C_scales, float* C_amax_out, int32_t* dev_status, fp4_stream_t stream) {
+  if (layout != FP4_LAYOUT_TN || !valid_fmt((int)f)) return FP4_ERR_INVALID_ARG;
+  if (r_out != FP4_ROUND_RNE && r_out != FP4_ROUND_STOCHASTIC) return FP4_ERR_INVALID_ARG;
+  if (sfl_out != FP4_SFLAYOUT_PLAIN && sfl_out != FP4_SFLAYOUT_MMA) return FP4_ERR_INVALID_ARG;
+  if (f == FP4_SF_E1M6 || sweep_fmt((int)f)) return FP4_ERR_UNSUPPORTED;
+  if (Aq == nullptr || As == nullptr || Bq == nullptr || Bs == nullptr || C_codes == nullptr ||
+      C_scales == nullptr || g_out == nullptr)
+    return FP4_ERR_INVALID_ARG;
+  if (f != FP4_SF_E8M0 && (ga == nullptr || gb == nullptr)) return FP4_ERR_INVALID_ARG;
+  if (f == FP4_SF_UE5M3 && (tA == nullptr || tB == nullptr)) return FP4_ERR_INVALID_ARG;
+  if (M <= 0 || N <= 0 || K <= 0 || M % 128 != 0 || N % 256 != 0 || K % 256 != 0) return FP4_ERR_SHAPE;
+  if (M % 256 != 0) return FP4_ERR_UNSUPPORTED;  // the quantizing epilogue runs on CTA pairs
+  if (!aligned16(Aq) || !aligned16(As) || !aligned16(Bq) || !aligned16(Bs) || !aligned16(C_codes) ||
+      !aligned16(C_scales))
+    return FP4_ERR_ALIGNMENT;
+  cudaStream_t st = (cudaStream_t)stream;
+  if (C_amax_out != nullptr) {
+    fp4_status s = cuda_status(cudaMemsetAsync(C_amax_out, 0, sizeof(float), st));
+    if (s != FP4_OK) return s;
+  }
+  fp4lib::GemmArgs a{};
+  a.Aq = Aq;
+  a.As = As;
+  a.Bq = Bq;
+  a.Bs = Bs;
+  a.ga = ga;
+  a.gb = gb;
+  a.tA = f == FP4_SF_UE5M3 ? tA : nullptr;
+  a.tB = f == FP4_SF_UE5M3 ? tB : nullptr;
+  a.M = M;
+  a.N = N;
+  a.K = K;
+  a.ldc = N;
+  a.fmt = (int)f;
+  a.bf16_out = true;
+  a.status = dev_status;
+  a.qout = true;
+  a.q_codes = C_codes;
+  a.q_scales = C_scales;
+  a.q_g = g_out;
+  a.q_amax_out = C_amax_out;
+  a.q_seed = seed_out;
+  a.q_sr = r_out == FP4_ROUND_STOCHASTIC;
+  a.q_mma = sfl_out == FP4_SFLAYOUT_MMA;
+  return cuda_status(fp4lib::launch_gemm(a, st));
+}
+
 fp4_status fp4_gemv_w4a16(const uint8_t* Wq, const uint8_t* Ws, const float* gw, const void* x_bf16,
                           int64_t batch, int64_t N, int64_t K, fp4_out_dtype od, void* y, fp4_stream_t stream) {
   if (od != FP4_OUT_F32 && od != FP4_OUT_BF16) return FP4_ERR_INVALID_ARG;

@@ -350,6 +350,13 @@ struct Params {
   const int32_t* tB;
   int M, N, K;
   int32_t* status;
+  // quantized output (pair kernel with QOUT): see fp4lib::GemmArgs
+  uint8_t* q_codes;
+  uint8_t* q_scales;
+  const float* q_g;
+  float* q_amax_out;
+  uint64_t q_seed;
+  int q_sr, q_mma;
 };
 
 // Epilogue of one warp: 32 accumulator rows (row0.., one per lane) x 64
@@ -399,6 +406,45 @@ __device__ __forceinline__ void store_block(const uint32_t (&r)[2][32], float al
       bulk_commit();
     }
   }
+}
+
+// Quantizing epilogue of one warp: row `row` (this lane) x 64 columns from
+// col0, exactly what fp4_quantize (E4M3 scales, 16-element blocks along N)
+// makes of the bf16 output the other epilogue would store: bf16(acc * alpha),
+// block amax, scale, RNE or Philox SR at output-layout indices row * N + col,
+// 32 code bytes and 4 scale bytes per lane.
+__device__ __forceinline__ void quant_epilogue(const uint32_t (&r)[2][32], float alpha, const Params& p, int row,
+                                               int col0, float s_enc_out, float& amax_local) {
+  uint32_t w[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    const int c = 2 * i;
+    const float x0 = __fmul_rn(__uint_as_float(r[c >> 5][c & 31]), alpha);
+    const float x1 = __fmul_rn(__uint_as_float(r[c >> 5][(c & 31) + 1]), alpha);
+    const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
+    w[i] = *reinterpret_cast<const uint32_t*>(&h);
+  }
+  uint32_t q[8];
+  uint32_t sc = 0;
+#pragma unroll
+  for (int blk = 0; blk < 4; ++blk) {
+    const uint32_t* wb = w + 8 * blk;
+    const float a = fp4dev::absmax_words(wb, 8);
+    amax_local = fmaxf(amax_local, a);
+    const fp4dev::BlockScale bs = fp4dev::block_scale<fp4dev::SF_E4M3>(a, s_enc_out);
+    const uint64_t idx0 = (uint64_t)row * (uint64_t)p.N + (uint64_t)(col0 + 16 * blk);
+    const uint2 qq = p.q_sr ? fp4dev::quant16<true>(wb, bs.r, p.q_seed, idx0)
+                            : fp4dev::quant16<false>(wb, bs.r, p.q_seed, idx0);
+    q[2 * blk] = qq.x;
+    q[2 * blk + 1] = qq.y;
+    sc |= bs.code << (8 * blk);
+  }
+  uint4* dst = reinterpret_cast<uint4*>(p.q_codes + (int64_t)row * (p.N / 2) + col0 / 2);
+  dst[0] = make_uint4(q[0], q[1], q[2], q[3]);
+  dst[1] = make_uint4(q[4], q[5], q[6], q[7]);
+  const int64_t nb = p.N / 16, b = col0 / 16;
+  const int64_t off = p.q_mma ? fp4dev::mma_sf_offset(row, b, nb) : (int64_t)row * nb + b;
+  *reinterpret_cast<uint32_t*>(p.q_scales + off) = sc;
 }
 
 // Epilogue scale of the accumulator: alpha = 1 / (s_encA * s_encB), times
@@ -709,7 +755,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 //     the whole tile to its half of the product);
 //   * both CTAs' epilogue warps drain their own accumulator rows and release
 //     them on the even CTA's acc_empty.
-template <int FMT, bool BF16, class PL>
+template <int FMT, bool BF16, class PL, bool QOUT = false>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     k_gemm_fp4_pair(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                     const __grid_constant__ CUtensorMap tmap_c, Params p) {
@@ -972,6 +1018,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const float alpha = epilogue_alpha<FMT>(p);
     uint8_t* stage_buf = smem + SMEM_OUT + ew * STAGE_BYTES;
     const uint32_t stage_addr = smem_u32(stage_buf);
+    float s_enc_out = 1.0f, amax_local = 0.0f;
+    if constexpr (QOUT) s_enc_out = fp4dev::global_encode_scale<fp4dev::SF_E4M3>(__ldg(p.q_g), p.status);
     uint32_t acc_phase = 0;
     for (int u = cluster_id; u < num_units && run; u += num_clusters) {
       const int mp = u / n_tiles, nt = u % n_tiles;
@@ -986,8 +1034,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(lead_acc_empty);
-      store_block<BF16, PL>(r, alpha, stage_buf, stage_addr, &tmap_c, mp * PM + BM * (int)crank + 32 * quarter,
-                            nt * BN + EPI_COLS * cblk, lane);
+      if constexpr (QOUT) {
+        quant_epilogue(r, alpha, p, mp * PM + BM * (int)crank + 32 * quarter + lane, nt * BN + EPI_COLS * cblk,
+                       s_enc_out, amax_local);
+      } else {
+        store_block<BF16, PL>(r, alpha, stage_buf, stage_addr, &tmap_c, mp * PM + BM * (int)crank + 32 * quarter,
+                              nt * BN + EPI_COLS * cblk, lane);
+      }
+    }
+    if constexpr (QOUT) {
+      if (p.q_amax_out != nullptr) {
+        // non-negative floats order like their bit patterns
+        const unsigned int am = __reduce_max_sync(0xFFFFFFFFu, __float_as_uint(amax_local));
+        if (lane == 0) atomicMax(reinterpret_cast<unsigned int*>(p.q_amax_out), am);
+      }
     }
     if (lane == 0) bulk_wait0();
     __syncwarp();
@@ -1076,7 +1136,7 @@ cudaError_t launch_t(const fp4lib::GemmArgs& a, cudaStream_t st) {
   if (!make_code_map(&ma, a.Aq, a.M, a.K / 2, BM) || !make_code_map(&mb, a.Bq, a.N, a.K / 2, BN) ||
       !make_out_map(&mc, a.C, a.M, a.N, a.ldc, BF16, PL::OUT_ROW_BYTES))
     return cudaErrorInvalidValue;
-  Params p;
+  Params p{};
   p.As = a.As;
   p.Bs = a.Bs;
   p.ga = a.ga;
@@ -1095,10 +1155,10 @@ cudaError_t launch_t(const fp4lib::GemmArgs& a, cudaStream_t st) {
 
 // CTA-pair launch: clusters of 2 CTAs, one 256 x 256 output tile per cluster
 // and round.
-template <int FMT, bool BF16>
+template <int FMT, bool BF16, bool QOUT = false>
 cudaError_t launch_pair(const fp4lib::GemmArgs& a, cudaStream_t st) {
   using PL = PlanPair;
-  auto kern = k_gemm_fp4_pair<FMT, BF16, PL>;
+  auto kern = k_gemm_fp4_pair<FMT, BF16, PL, QOUT>;
   constexpr int SMEM_LAUNCH = PL::SMEM_LAUNCH;
   static bool attr_set = false;
   static int max_clusters = 0;
@@ -1123,10 +1183,13 @@ cudaError_t launch_pair(const fp4lib::GemmArgs& a, cudaStream_t st) {
     attr_set = true;
   }
   CUtensorMap ma, mb, mc;
+  // with a quantized output the C map is never used; it is built over the code buffer
+  void* cbase = QOUT ? static_cast<void*>(a.q_codes) : a.C;
+  const int64_t cn = QOUT ? a.N / 4 : a.N, cld = QOUT ? a.N / 4 : a.ldc;
   if (!make_code_map(&ma, a.Aq, a.M, a.K / 2, BM) || !make_code_map(&mb, a.Bq, a.N, a.K / 2, BN / 2) ||
-      !make_out_map(&mc, a.C, a.M, a.N, a.ldc, BF16, PL::OUT_ROW_BYTES))
+      !make_out_map(&mc, cbase, a.M, cn, cld, QOUT ? true : BF16, PL::OUT_ROW_BYTES))
     return cudaErrorInvalidValue;
-  Params p;
+  Params p{};
   p.As = a.As;
   p.Bs = a.Bs;
   p.ga = a.ga;
@@ -1137,6 +1200,13 @@ cudaError_t launch_pair(const fp4lib::GemmArgs& a, cudaStream_t st) {
   p.N = (int)a.N;
   p.K = (int)a.K;
   p.status = a.status;
+  p.q_codes = a.q_codes;
+  p.q_scales = a.q_scales;
+  p.q_g = a.q_g;
+  p.q_amax_out = a.q_amax_out;
+  p.q_seed = a.q_seed;
+  p.q_sr = a.q_sr ? 1 : 0;
+  p.q_mma = a.q_mma ? 1 : 0;
   const int units = (int)((a.M / (2 * BM)) * (a.N / BN));
   const int clusters = units < max_clusters ? units : max_clusters;
   cfg.gridDim = dim3((unsigned)(2 * clusters), 1, 1);
@@ -1157,6 +1227,16 @@ namespace fp4lib {
 
 cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t st) {
   if (a.N % BN != 0) return cudaErrorNotSupported;
+  if (a.qout) {
+    // quantizing epilogue: CTA-pair kernel only (M a multiple of 256)
+    if (a.M % (2 * BM) != 0) return cudaErrorNotSupported;
+    switch (a.fmt) {
+      case FP4_SF_E4M3: return launch_pair<fp4dev::SF_E4M3, true, true>(a, st);
+      case FP4_SF_UE5M3: return launch_pair<fp4dev::SF_UE5M3, true, true>(a, st);
+      case FP4_SF_E8M0: return launch_pair<fp4dev::SF_E8M0, true, true>(a, st);
+      default: return cudaErrorInvalidValue;
+    }
+  }
   switch (a.fmt) {
     case FP4_SF_E4M3: return a.bf16_out ? launch_cm<fp4dev::SF_E4M3, true>(a, st) : launch_cm<fp4dev::SF_E4M3, false>(a, st);
     case FP4_SF_UE5M3: return a.bf16_out ? launch_cm<fp4dev::SF_UE5M3, true>(a, st) : launch_cm<fp4dev::SF_UE5M3, false>(a, st);

@@ -42,6 +42,14 @@ struct GemmArgs {
   bool bf16_out;
   void* C;
   int32_t* status;
+  // quantized output instead of C (fp4_gemm_quantize): NVFP4 codes and scales
+  // of bf16(C) under the stored global amax q_g
+  bool qout;
+  uint8_t *q_codes, *q_scales;
+  const float* q_g;
+  float* q_amax_out;  // nullable: max |bf16(C)|
+  uint64_t q_seed;
+  bool q_sr, q_mma;
 };
 cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t st);
 

@@ -67,6 +67,8 @@ _SIGS = {
     "fp4_ue5m3_to_e4m3": (_I32, [_VP, _I64, _VP, _VP, _VP, _VP]),
     "fp4_gemm": (_I32, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _I64, _I64, _I64, _I32, _I32, _I32, _VP, _I64,
                         _VP, _VP]),
+    "fp4_gemm_quantize": (_I32, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _I64, _I64, _I64, _I32, _I32, _VP, _I32,
+                                 _U64, _I32, _VP, _VP, _VP, _VP, _VP]),
     "fp4_gemv_w4a16": (_I32, [_VP, _VP, _VP, _VP, _I64, _I64, _I64, _I32, _VP, _VP]),
     "fp4_encode_scales": (_I32, [_VP, _I64, _I32, _VP, _VP, _VP]),
     "fp4_philox_bits16": (_I32, [_U64, _U64, _I64, _VP, _VP]),
@@ -182,6 +184,14 @@ def fp4_gemm(Aq, As, Bq, Bs, ga, gb, tA, tB, M, N, K, fmt, out_dtype, C, ldc=Non
     _check(_lib().fp4_gemm(_ptr(Aq), _ptr(As), _ptr(Bq), _ptr(Bs), _ptr(ga), _ptr(gb), _ptr(tA), _ptr(tB),
                            M, N, K, _fmt(fmt), FP4_LAYOUT_TN, int(out_dtype), _ptr(C),
                            N if ldc is None else ldc, _ptr(dev_status), _stream(stream)), "fp4_gemm")
+
+
+def fp4_gemm_quantize(Aq, As, Bq, Bs, ga, gb, tA, tB, M, N, K, fmt, g_out, rounding, seed, sf_layout, C_codes,
+                      C_scales, C_amax_out=None, dev_status=None, stream=None):
+    _check(_lib().fp4_gemm_quantize(_ptr(Aq), _ptr(As), _ptr(Bq), _ptr(Bs), _ptr(ga), _ptr(gb), _ptr(tA), _ptr(tB),
+                                    M, N, K, _fmt(fmt), FP4_LAYOUT_TN, _ptr(g_out), int(rounding), int(seed),
+                                    int(sf_layout), _ptr(C_codes), _ptr(C_scales), _ptr(C_amax_out),
+                                    _ptr(dev_status), _stream(stream)), "fp4_gemm_quantize")
 
 
 def fp4_gemv_w4a16(Wq, Ws, gw, x, batch, N, K, out_dtype, y, stream=None):

@@ -220,6 +220,25 @@ fp4_status fp4_gemm(const uint8_t* Aq, const uint8_t* As, const uint8_t* Bq, con
                     fp4_out_dtype od, void* C, int64_t ldc, int32_t* dev_status,
                     fp4_stream_t stream);
 
+/* fp4_gemm with its output quantized in the epilogue instead of stored:
+ * writes exactly what fp4_quantize(bf16(C), FP4_SF_E4M3, r_out, seed_out,
+ * g_out, transpose = 0, sfl_out) would make of the bf16 result of fp4_gemm
+ * with the same operands, i.e. NVFP4 codes [M, N/2] and E4M3 scales of
+ * 16-element blocks along N (Philox indices row * N + col), without the
+ * bf16 C in memory.  Quantizing the next layer's input where it is produced
+ * needs the stored global amax of C (g_out, device float), the recipe of
+ * [UE5M3] "Что сделали" (tensor maximum refreshed every 50 steps, the stored
+ * value used in between); C_amax_out (nullable device float) receives
+ * max |bf16(C)| for the next refresh.  Requirements as fp4_gemm, and M % 256
+ * == 0 (the epilogue runs on the CTA-pair kernel; FP4_ERR_UNSUPPORTED
+ * otherwise). */
+fp4_status fp4_gemm_quantize(const uint8_t* Aq, const uint8_t* As, const uint8_t* Bq, const uint8_t* Bs,
+                             const float* ga, const float* gb, const int32_t* tA, const int32_t* tB,
+                             int64_t M, int64_t N, int64_t K, fp4_scale_fmt f, fp4_gemm_layout layout,
+                             const float* g_out, fp4_rounding r_out, uint64_t seed_out,
+                             fp4_sf_layout sfl_out, uint8_t* C_codes, uint8_t* C_scales,
+                             float* C_amax_out, int32_t* dev_status, fp4_stream_t stream);
+
 /* Weight-only NVFP4 linear ([W4A16] "Метод"): y[b, n] = sum_k deq(W)[n, k] * x[b, k],
  * deq(W) = e2m1 * s_b / s_enc(*gw) (E4M3 scales, G = 16, FP4_SFLAYOUT_PLAIN),
  * x bf16 [batch, K] (row stride K), float32 accumulation, y [batch, N] float32
