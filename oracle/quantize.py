@@ -214,14 +214,14 @@ def quantize(x: np.ndarray, fmt: str = "E4M3", rounding: str = "rne", seed: int 
     global_amax None -> the fresh amax of x.  transpose=True quantizes x^T
     (blocks along the original rows; output layout [K, M], Philox indices in
     that layout).  rht_mask: apply the 16 x 16 random Hadamard transform with
-    this sign mask to every 16-element block along K first (rows only); the
-    amax is then the transformed tensor's.  Returns dict(codes, scales, amax, s_enc).
+    this sign mask to every 16-element block along the blocked dimension first
+    (K for rows, M for transpose=True); the amax is then the transformed
+    tensor's.  Returns dict(codes, scales, amax, s_enc).
     """
     x = np.asarray(x, dtype=np.float32)
     if rht_mask is not None:
-        if transpose:
-            raise ValueError("the Hadamard transform runs along rows only")
-        x = rht16(x, rht_mask)
+        # transform along the blocked dimension: K for rows, M for the transposed output
+        x = rht16(x.T, rht_mask).T if transpose else rht16(x, rht_mask)
     amax = np.float32(np.max(np.abs(x))) if x.size else np.float32(0)
     g = amax if global_amax is None else np.float32(global_amax)
     src = x.T if transpose else x

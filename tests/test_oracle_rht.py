@@ -107,3 +107,23 @@ def test_gemm_on_transformed_operands_approximates_the_product():
     C, _ = Gm.gemm_ref(qa["codes"], qa["scales"], qa["amax"], qb["codes"], qb["scales"], qb["amax"], "E4M3")
     exact = X.astype(np.float64) @ W.T.astype(np.float64)
     assert np.linalg.norm(C - exact) / np.linalg.norm(exact) < 0.2
+
+
+def test_transposed_transform_runs_along_m():
+    rng = np.random.default_rng(7)
+    x = bf16(rng.standard_normal((64, 32)))
+    q = Q.quantize(x, "E4M3", transpose=True, rht_mask=MASK)
+    q2 = Q.quantize(R.rht16(x.T, MASK), "E4M3")
+    assert np.array_equal(q["codes"], q2["codes"]) and np.array_equal(q["scales"], q2["scales"])
+    assert q["amax"] == np.float32(np.max(np.abs(R.rht16(x.T, MASK))))
+
+
+def test_wgrad_product_preserved_with_transposed_transforms():
+    # dW = dY^T X: both operands transformed along M (the reduction dimension)
+    rng = np.random.default_rng(8)
+    dY = bf16(rng.standard_normal((256, 48)))
+    X = bf16(rng.standard_normal((256, 64)))
+    exact = dY.T.astype(np.float64) @ X.astype(np.float64)
+    got = R.rht16(dY.T, MASK).astype(np.float64) @ R.rht16(X.T, MASK).T.astype(np.float64)
+    S = np.abs(dY.T).astype(np.float64) @ np.abs(X).astype(np.float64)
+    assert np.all(np.abs(got - exact) <= 1e-5 * S)
