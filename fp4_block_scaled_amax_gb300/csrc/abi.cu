@@ -171,6 +171,67 @@ fp4_status fp4_quantize_rht(const void* x_bf16, int64_t M, int64_t K, int64_t ld
   return cuda_status(fp4lib::launch_quantize_rht(a, rht_mask, st));
 }
 
+fp4_status fp4_quantize_dual_rht(const void* x_bf16, int64_t M, int64_t K, int64_t ldx, fp4_scale_fmt f,
+                                 fp4_rounding r_row, uint64_t seed_row, fp4_rounding r_col, uint64_t seed_col,
+                                 uint32_t rht_mask, const float* g_row, const float* g_col, fp4_sf_layout sfl,
+                                 uint8_t* codes_row, uint8_t* scales_row, uint8_t* codes_col, uint8_t* scales_col,
+                                 float* amax_row_out, float* amax_col_out, int32_t* dev_status,
+                                 fp4_stream_t stream) {
+  if ((r_row != FP4_ROUND_RNE && r_row != FP4_ROUND_STOCHASTIC) ||
+      (r_col != FP4_ROUND_RNE && r_col != FP4_ROUND_STOCHASTIC) || rht_mask > 0xFFFFu)
+    return FP4_ERR_INVALID_ARG;
+  if ((g_row == nullptr) != (g_col == nullptr)) return FP4_ERR_INVALID_ARG;
+  if ((amax_row_out == nullptr) != (amax_col_out == nullptr)) return FP4_ERR_INVALID_ARG;
+  fp4_status s = check_quant_common(x_bf16, M, K, ldx, (int)f, (int)sfl, M, K);
+  if (s != FP4_OK) return s;
+  if ((s = check_quant_common(x_bf16, M, K, ldx, (int)f, (int)sfl, K, M)) != FP4_OK) return s;
+  if (f != FP4_SF_E4M3 && f != FP4_SF_UE5M3 && f != FP4_SF_E8M0) return FP4_ERR_UNSUPPORTED;
+  if (M % 32 != 0 || K % 32 != 0) return FP4_ERR_SHAPE;
+  if (M * K > 0) {
+    if ((s = check_out(codes_row, scales_row)) != FP4_OK) return s;
+    if ((s = check_out(codes_col, scales_col)) != FP4_OK) return s;
+  }
+  cudaStream_t st = (cudaStream_t)stream;
+  fp4lib::DualRhtArgs a{};
+  a.fmt = (int)f;
+  a.x = x_bf16;
+  a.M = M;
+  a.K = K;
+  a.ldx = ldx;
+  a.mask = rht_mask;
+  a.row_sr = r_row == FP4_ROUND_STOCHASTIC;
+  a.col_sr = r_col == FP4_ROUND_STOCHASTIC;
+  a.mma = sfl == FP4_SFLAYOUT_MMA;
+  a.seed_row = seed_row;
+  a.seed_col = seed_col;
+  a.codes_row = codes_row;
+  a.scales_row = scales_row;
+  a.codes_col = codes_col;
+  a.scales_col = scales_col;
+  a.amax_row_out = amax_row_out;
+  a.amax_col_out = amax_col_out;
+  a.status = dev_status;
+  if (g_row == nullptr) {
+    // fresh: both transformed amaxes first
+    if (amax_row_out == nullptr) return FP4_ERR_INVALID_ARG;
+    if ((s = cuda_status(fp4lib::launch_amax_rht(x_bf16, M, K, ldx, rht_mask, amax_row_out, st))) != FP4_OK) return s;
+    if ((s = cuda_status(fp4lib::launch_amax_rht_cols(x_bf16, M, K, ldx, rht_mask, amax_col_out, st))) != FP4_OK)
+      return s;
+    a.g_row = amax_row_out;
+    a.g_col = amax_col_out;
+    a.amax_by_product = false;
+  } else {
+    a.g_row = g_row;
+    a.g_col = g_col;
+    a.amax_by_product = amax_row_out != nullptr;
+    if (a.amax_by_product) {
+      if ((s = cuda_status(cudaMemsetAsync(amax_row_out, 0, sizeof(float), st))) != FP4_OK) return s;
+      if ((s = cuda_status(cudaMemsetAsync(amax_col_out, 0, sizeof(float), st))) != FP4_OK) return s;
+    }
+  }
+  return cuda_status(fp4lib::launch_quantize_dual_rht(a, st));
+}
+
 fp4_status fp4_quantize_dual(const void* x_bf16, int64_t M, int64_t K, int64_t ldx, fp4_scale_fmt f,
                              fp4_rounding r_row, uint64_t seed_row, fp4_rounding r_col, uint64_t seed_col,
                              const float* global_amax, fp4_sf_layout sfl, uint8_t* codes_row, uint8_t* scales_row,

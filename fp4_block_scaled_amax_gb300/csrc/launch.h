@@ -32,6 +32,21 @@ cudaError_t launch_philox_bits16(uint64_t seed, uint64_t start, int64_t n, uint1
 cudaError_t launch_amax_rht(const void* x, int64_t M, int64_t K, int64_t ldx, uint32_t mask, float* out,
                             cudaStream_t st);
 cudaError_t launch_quantize_rht(const QuantArgs& a, uint32_t mask, cudaStream_t st);
+struct DualRhtArgs {
+  int fmt;
+  const void* x;
+  int64_t M, K, ldx;
+  uint32_t mask;
+  const float *g_row, *g_col;  // device: stored global amaxes of the two transformed layouts
+  bool row_sr, col_sr, mma, amax_by_product;
+  uint64_t seed_row, seed_col;
+  uint8_t *codes_row, *scales_row, *codes_col, *scales_col;
+  float *amax_row_out, *amax_col_out;
+  int32_t* status;
+};
+cudaError_t launch_amax_rht_cols(const void* x, int64_t M, int64_t K, int64_t ldx, uint32_t mask, float* out,
+                                 cudaStream_t st);
+cudaError_t launch_quantize_dual_rht(const DualRhtArgs& a, cudaStream_t st);
 
 struct GemmArgs {
   const uint8_t *Aq, *As, *Bq, *Bs;

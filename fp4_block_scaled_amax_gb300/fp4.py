@@ -61,6 +61,8 @@ _SIGS = {
     "fp4_quantize": (_I32, [_VP, _I64, _I64, _I64, _I32, _I32, _U64, _VP, _I32, _I32, _VP, _VP, _VP, _VP, _VP]),
     "fp4_quantize_rht": (_I32, [_VP, _I64, _I64, _I64, _I32, _I32, _U64, ctypes.c_uint32, _VP, _I32, _VP, _VP, _VP,
                                 _VP, _VP]),
+    "fp4_quantize_dual_rht": (_I32, [_VP, _I64, _I64, _I64, _I32, _I32, _U64, _I32, _U64, ctypes.c_uint32, _VP, _VP,
+                                     _I32, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
     "fp4_quantize_dual": (_I32, [_VP, _I64, _I64, _I64, _I32, _I32, _U64, _I32, _U64, _VP, _I32,
                                  _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
     "fp4_dequantize": (_I32, [_VP, _VP, _I32, _I64, _I64, _I32, _VP, _I32, _VP, _VP]),
@@ -158,6 +160,17 @@ def fp4_quantize_rht(x, fmt, rounding, seed, rht_mask, global_amax, sf_layout, c
     _check(_lib().fp4_quantize_rht(_ptr(x), M, K, x.stride(0), _fmt(fmt), int(rounding), int(seed), int(rht_mask),
                                    _ptr(global_amax), int(sf_layout), _ptr(codes), _ptr(scales), _ptr(amax_out),
                                    _ptr(dev_status), _stream(stream)), "fp4_quantize_rht")
+
+
+def fp4_quantize_dual_rht(x, fmt, r_row, seed_row, r_col, seed_col, rht_mask, g_row, g_col, sf_layout, codes_row,
+                          scales_row, codes_col, scales_col, amax_row_out=None, amax_col_out=None, dev_status=None,
+                          stream=None):
+    M, K = x.shape
+    _check(_lib().fp4_quantize_dual_rht(_ptr(x), M, K, x.stride(0), _fmt(fmt), int(r_row), int(seed_row), int(r_col),
+                                        int(seed_col), int(rht_mask), _ptr(g_row), _ptr(g_col), int(sf_layout),
+                                        _ptr(codes_row), _ptr(scales_row), _ptr(codes_col), _ptr(scales_col),
+                                        _ptr(amax_row_out), _ptr(amax_col_out), _ptr(dev_status), _stream(stream)),
+           "fp4_quantize_dual_rht")
 
 
 def fp4_quantize_dual(x, fmt, r_row, seed_row, r_col, seed_col, global_amax, sfl, codes_row, scales_row,

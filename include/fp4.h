@@ -173,6 +173,25 @@ fp4_status fp4_quantize_rht(const void* x_bf16, int64_t M, int64_t K, int64_t ld
                             uint8_t* codes, uint8_t* scales, float* amax_out,
                             int32_t* dev_status, fp4_stream_t stream);
 
+/* Row and transposed quantization with the 16 x 16 random Hadamard transform
+ * of fp4_quantize_rht, from one read: the row output transforms 16-element
+ * blocks along K, the transposed output (blocks along the original rows)
+ * 16-row blocks along M, so fwd, dgrad and wgrad operands all see the
+ * transform along their reduction dimension.  The two transformed tensors
+ * have their own global amax: g_row / g_col (device floats, both or neither;
+ * NULL computes both fresh, which then requires amax_row_out / amax_col_out),
+ * and amax_row_out / amax_col_out (both or neither) receive this call's
+ * max |x'| of each.  Formats E4M3, UE5M3, E8M0.  Needs M % 32 == 0 and
+ * K % 32 == 0 besides fp4_quantize_dual's requirements. */
+fp4_status fp4_quantize_dual_rht(const void* x_bf16, int64_t M, int64_t K, int64_t ldx,
+                                 fp4_scale_fmt f, fp4_rounding r_row, uint64_t seed_row,
+                                 fp4_rounding r_col, uint64_t seed_col, uint32_t rht_mask,
+                                 const float* g_row, const float* g_col, fp4_sf_layout sfl,
+                                 uint8_t* codes_row, uint8_t* scales_row,
+                                 uint8_t* codes_col, uint8_t* scales_col,
+                                 float* amax_row_out, float* amax_col_out,
+                                 int32_t* dev_status, fp4_stream_t stream);
+
 /* Row and transposed quantization of one bf16 [M, K] matrix from a single
  * read: writes exactly what fp4_quantize(transpose=0, r_row, seed_row) and
  * fp4_quantize(transpose=1, r_col, seed_col) would, with the same global amax.
