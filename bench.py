@@ -359,8 +359,9 @@ RHT_MASK = 0xB38D  # sign mask of the 16 x 16 random Hadamard transform (any 16-
 
 def hadamard_study(step, fp4, flush, device, reps=5):
     """16 x 16 random Hadamard transform before quantization, outside the timed
-    step: (1) its cost on the given-amax E4M3 row quantizer of dY (GB/s with and
-    without the transform, 2.5625 B/elem); (2) relative RMS error of NVFP4 /
+    step: (1) its cost on the given-amax E4M3 quantizers of dY (GB/s with and
+    without the transform: the row quantizer, 2.5625 B/elem, and the dual
+    row + transposed SR quantizer, 3.125 B/elem); (2) relative RMS error of NVFP4 /
     NVINT4 / MXFP4 / MXINT4 on the 350M MLP input X 8192x1024 with and without
     the transform (fresh amax; with it, measured against the transformed
     tensor, whose norm the orthogonal transform keeps)."""
@@ -387,9 +388,18 @@ def hadamard_study(step, fp4, flush, device, reps=5):
     RNE, MMA = fp4.FP4_ROUND_RNE, fp4.FP4_SFLAYOUT_MMA
     us_plain = timed(lambda: fp4.fp4_quantize(x, "E4M3", RNE, 0, g, False, MMA, cr, srs, None))
     us_rht = timed(lambda: fp4.fp4_quantize_rht(x, "E4M3", RNE, 0, RHT_MASK, g, MMA, cr, srs, None))
+    _, _, cc, scs = step.q["dY"]
+    SR = fp4.FP4_ROUND_STOCHASTIC
+    us_dual = timed(lambda: fp4.fp4_quantize_dual(x, "E4M3", SR, 1234, SR, 1235, g, MMA, cr, srs, cc, scs))
+    us_dual_rht = timed(lambda: fp4.fp4_quantize_dual_rht(x, "E4M3", SR, 1234, SR, 1235, RHT_MASK, g, g, MMA,
+                                                           cr, srs, cc, scs))
     out = {"cost": {"tensor": f"dY {x.shape[0]}x{x.shape[1]}, E4M3 RNE rows, given amax", "unit": "GB/s",
                     "plain": round(n * 2.5625 / us_plain / 1e3, 1), "with_rht": round(n * 2.5625 / us_rht / 1e3, 1),
-                    "us_plain": round(us_plain, 2), "us_rht": round(us_rht, 2), "peak": hbm}}
+                    "us_plain": round(us_plain, 2), "us_rht": round(us_rht, 2), "peak": hbm},
+           "cost_dual": {"tensor": f"dY {x.shape[0]}x{x.shape[1]}, E4M3 SR rows + SR transposed, given amax",
+                         "unit": "GB/s", "plain": round(n * 3.125 / us_dual / 1e3, 1),
+                         "with_rht": round(n * 3.125 / us_dual_rht / 1e3, 1), "us_plain": round(us_dual, 2),
+                         "us_rht": round(us_dual_rht, 2), "peak": hbm}}
     X = synth.config2()["X"].to(device)
     M, K = X.shape
     Xf = X.float()

@@ -382,7 +382,8 @@ fp4_status fp4_gemm_quantize(const uint8_t* Aq, const uint8_t* As, const uint8_t
 }
 
 fp4_status fp4_gemv_w4a16(const uint8_t* Wq, const uint8_t* Ws, const float* gw, const void* x_bf16,
-                          int64_t batch, int64_t N, int64_t K, fp4_out_dtype od, void* y, fp4_stream_t stream) {
+                          int64_t batch, int64_t N, int64_t K, fp4_out_dtype od, void* y, int32_t* dev_status,
+                          fp4_stream_t stream) {
   if (od != FP4_OUT_F32 && od != FP4_OUT_BF16) return FP4_ERR_INVALID_ARG;
   if (Wq == nullptr || Ws == nullptr || gw == nullptr || x_bf16 == nullptr || y == nullptr)
     return FP4_ERR_INVALID_ARG;
@@ -398,6 +399,7 @@ fp4_status fp4_gemv_w4a16(const uint8_t* Wq, const uint8_t* Ws, const float* gw,
   a.K = K;
   a.bf16_out = od == FP4_OUT_BF16;
   a.y = y;
+  a.status = dev_status;
   return cuda_status(fp4lib::launch_gemv(a, (cudaStream_t)stream));
 }
 

@@ -12,7 +12,12 @@
 // them with the bf16 activations on the tensor cores (mma.sync m16n8k16,
 // float32 accumulation).  The batch is the MMA's N dimension (8 per tile).
 //
-// k permutation: inside a 128-wide k chunk, lane q of a quad (q = lane % 4)
+// Two forms.  Decode batches (batch <= 8, K % 256 == 0) take the TMA-fed
+// kernel further down: weights, scales and activations stream through a
+// shared-memory ring and are shared by all warps of a CTA.  Larger batches
+// and other K take the register-fed kernel right below.
+//
+// Register-fed form.  k permutation: inside a 128-wide k chunk, lane q of a quad (q = lane % 4)
 // supplies at MMA step s the fragment positions {2q, 2q+1, 2q+8, 2q+9} from
 // the actual columns 32q + 4s + {0, 1, 2, 3}.  A and B use the same map, so the
 // sum over positions is the sum over k, while each lane reads 16 contiguous
@@ -21,9 +26,12 @@
 // CTA = 16 weight rows x WARPS warps splitting K; partial sums meet in shared
 // memory.
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 
+#include "async_sm103.cuh"
 #include "fp4_device.cuh"
 #include "launch.h"
 
@@ -207,12 +215,316 @@ __global__ void __launch_bounds__(NT <= 2 ? 512 : 256) k_gemv_w4a16(const uint8_
   }
 }
 
+
+// ---------------------------------------------------------------------------
+// TMA-fed form: batch <= 8 and K % 256 == 0
+// ---------------------------------------------------------------------------
+// One CTA per group of T 16-row tiles (T chosen so the groups cover the SMs
+// in about one wave).  Warp 0 streams stages of SC = 128 * WPT columns into a
+// shared-memory ring with cp.async.bulk.tensor: the T*16 code rows (128-byte
+// boxes, 128-byte swizzle), their SC/16 scale bytes per row, and the eight
+// activation rows of the same columns (64-column boxes, 128-byte swizzle; rows
+// >= batch, code rows >= N and columns >= K arrive as zeros).  Each 16-row
+// tile has WPT consumer warps, one per 128-column slice of the stage; a lane
+// reads one code word (8 columns) of each of its two rows per pair of MMAs.
+//
+// Pairing: the code word's nibbles n0..n7 become four bf16x2 registers
+// (n_i, n_{i+4}).  Bits (e1 e0 m) of a nibble at bf16 bits 8..6 are the E2M1
+// value times 2^-126 exactly (e = 0 lands on a bf16 subnormal), with the sign
+// at bit 15: isolating nibbles i and i+4 and multiplying by 2^6 + 2^12 puts
+// both fields in place at once (the two shifted copies do not overlap), and
+// one AND clears the rest.  One bf16x2 multiply by the block scale times
+// 2^118 gives e2m1 * s_b * 2^-8, exact (<= 6 significant bits, normal).  The
+// activations are paired the same way, (x_i, x_{i+4}), with one PRMT per
+// register, so each MMA's k positions are the same columns on both sides.
+// Word order: lane q takes its four words starting at word q (mod 4), which
+// keeps the 16-byte activation loads and the code loads free of bank
+// conflicts.  The 2^-8 folds into the final division by s_enc.
+
+constexpr int TV_MAX_TILES = 8;  // 16-row tiles per CTA
+constexpr int TV_MAX_STAGES = 32;
+constexpr int TV_RING_BUDGET = 200 * 1024;
+
+template <int WPT>
+struct TvLayout {
+  static constexpr int SC = 128 * WPT;     // columns per stage
+  static constexpr int SB = SC / 16;       // scale bytes per row per stage
+  static constexpr int CODE_BOXES = SC / 256;
+  static constexpr int X_BOXES = SC / 64;
+  __host__ __device__ static constexpr uint32_t code_box_bytes(int T) { return 2048u * T; }
+  __host__ __device__ static constexpr uint32_t code_bytes(int T) { return CODE_BOXES * code_box_bytes(T); }
+  __host__ __device__ static constexpr uint32_t x_bytes() { return 1024u * X_BOXES; }
+  __host__ __device__ static constexpr uint32_t stage_bytes(int T) {
+    return code_bytes(T) + x_bytes() + ((16u * SB * T + 1023u) & ~1023u);
+  }
+};
+
+// Code word (nibbles n0..n7, n0 lowest) -> bf16x2 (n_i, n_{i+4}) * 2^-126.
+__device__ __forceinline__ void e2m1x8_pairs(uint32_t v, uint32_t (&r)[4]) {
+  constexpr uint32_t M = 0x81C081C0u;  // bf16 bits 8..6 and 15 of both halves
+  const uint32_t v2 = v >> 8;
+  r[0] = ((v & 0x000F000Fu) * 4160u) & M;
+  r[1] = ((v & 0x00F000F0u) * 260u) & M;
+  r[2] = ((v2 & 0x000F000Fu) * 4160u) & M;
+  r[3] = ((v2 & 0x00F000F0u) * 260u) & M;
+}
+
+__device__ __forceinline__ uint32_t mul_bf16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+
+// Two E4M3 scale codes per row (sa: row A, sb: row B; low byte = block 2j)
+// -> bf16x2 of (value * 2^118) for each row and block, in both halves.  A
+// code shifted to bf16 bits 11..4 is value * 2^-120 exactly (E4M3 subnormals
+// land on bf16 subnormals); two exact multiplies by 2^119.
+__device__ __forceinline__ void e4m3_scales_bf16x2(uint32_t sa, uint32_t sb, uint32_t (&sA)[2],
+                                                   uint32_t (&sB)[2]) {
+  const uint32_t both = sa | (sb << 16);
+  constexpr uint32_t TWO119 = 0x7B007B00u;  // bf16x2 (2^119, 2^119)
+  const uint32_t lo = mul_bf16x2(mul_bf16x2((both & 0x00FF00FFu) << 4, TWO119), TWO119);
+  const uint32_t hi = mul_bf16x2(mul_bf16x2((both >> 4) & 0x0FF00FF0u, TWO119), TWO119);
+  sA[0] = prmt(lo, lo, 0x1010u);
+  sB[0] = prmt(lo, lo, 0x3232u);
+  sA[1] = prmt(hi, hi, 0x1010u);
+  sB[1] = prmt(hi, hi, 0x3232u);
+}
+
+// MMA without side effects, so the compiler may schedule the next step's
+// shared-memory loads ahead of it.
+__device__ __forceinline__ void mma_bf16_16816_pure(float* d, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                                    uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Every lane waits; the warp proceeds only if all lanes saw the phase.
+__device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                          int32_t* status) {
+  const bool ok = fp4async::wait_bounded(bar, parity, abort_flag, status);
+  return __all_sync(0xFFFFFFFFu, ok);
+}
+
+// Wait, without recording an error, for a phase that should already be
+// complete (copies issued before an abort); gives up after DRAIN_CYCLES.
+__device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity) {
+  const long long t0 = clock64();
+  while (!fp4async::mbar_try_wait(bar, parity)) {
+    if (clock64() - t0 > fp4async::DRAIN_CYCLES) return;
+  }
+}
+
+template <int WPT>
+__global__ void __launch_bounds__(32 * (1 + 4 * 6))
+    k_gemv_w4a16_tma(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant__ CUtensorMap tm_scales,
+                     const __grid_constant__ CUtensorMap tm_x, const float* __restrict__ gw, int batch, int N, int nk,
+                     int T, int S, bool bf16_out, void* __restrict__ y, int32_t* status) {
+  using namespace fp4async;
+  using L = TvLayout<WPT>;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ int abort_flag;
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* const base_ptr = smem_raw + (base - raw);
+  const uint32_t stage_bytes = L::stage_bytes(T);
+  const uint32_t code_bytes = L::code_bytes(T);
+  const uint32_t code_box = L::code_box_bytes(T);
+  const int nwarps = WPT * T;
+  float* const red = reinterpret_cast<float*>(base_ptr + S * stage_bytes);  // [WPT*T][16][8]
+  const uint32_t bars = base + S * stage_bytes + (uint32_t)nwarps * 16 * 8 * 4;  // full[S], empty[S]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n0 = blockIdx.x * 16 * T;
+
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    for (int s = 0; s < S; ++s) {
+      mbar_init(bars + 8 * s, 1);
+      mbar_init(bars + 8 * (S + s), nwarps);
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  __syncthreads();
+
+  if (warp == 0) {
+    if (lane == 0) {
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_codes)) : "memory");
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_scales)) : "memory");
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_x)) : "memory");
+      const uint32_t tx = code_bytes + L::x_bytes() + 16u * L::SB * T;
+      int issued = 0;
+      for (int it = 0, s = 0, ph = 0; it < nk; ++it) {
+        if (it >= S && !wait_bounded(bars + 8 * (S + s), ph ^ 1, &abort_flag, status)) break;
+        const uint32_t full = bars + 8 * s;
+        const uint32_t st = base + s * stage_bytes;
+        mbar_expect_tx(full, tx);
+#pragma unroll
+        for (int i = 0; i < L::CODE_BOXES; ++i)
+          tma_load_2d(st + code_box * i, &tm_codes, full, it * (L::SC / 2) + 128 * i, n0);
+#pragma unroll
+        for (int i = 0; i < L::X_BOXES; ++i) tma_load_2d(st + code_bytes + 1024u * i, &tm_x, full, it * L::SC + 64 * i, 0);
+        tma_load_2d(st + code_bytes + L::x_bytes(), &tm_scales, full, it * L::SB, n0);
+        issued = it + 1;
+        if (++s == S) {
+          s = 0;
+          ph ^= 1;
+        }
+      }
+      // no copy may still be landing when the CTA exits
+      for (int it = issued > S ? issued - S : 0; it < issued; ++it) wait_drain(bars + 8 * (it % S), (it / S) & 1);
+    }
+  } else {
+    const int cw = warp - 1, t = cw / WPT, qt = cw % WPT;
+    const int g = lane >> 2, q = lane & 3;
+    const int j = 4 * qt + q;  // the lane's 32-column chunk of the stage
+    const uint32_t rowA = 16u * t + g;
+    uint32_t code_off[4], x_off[4];
+    bool upper[4];
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {
+      const int w = (s + q) & 3;
+      code_off[s] = (uint32_t)(j >> 3) * code_box + rowA * 128u + ((uint32_t)((j & 7) ^ g) << 4) + 4u * w;
+      x_off[s] = code_bytes + (uint32_t)(j >> 1) * 1024u + g * 128u + ((uint32_t)((4 * (j & 1) + w) ^ g) << 4);
+      upper[s] = (w >> 1) != 0;
+    }
+    const uint32_t sc_off = code_bytes + L::x_bytes() + rowA * L::SB + 2u * j;
+    float acc0[4] = {0.f, 0.f, 0.f, 0.f}, acc1[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int it = 0, s = 0, ph = 0; it < nk; ++it) {
+      if (!wait_warp(bars + 8 * s, ph, &abort_flag, status)) break;
+      const uint8_t* st = base_ptr + s * stage_bytes;
+      uint32_t scA[2], scB[2];
+      e4m3_scales_bf16x2(*reinterpret_cast<const uint16_t*>(st + sc_off),
+                         *reinterpret_cast<const uint16_t*>(st + sc_off + 8 * L::SB), scA, scB);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const uint32_t va = *reinterpret_cast<const uint32_t*>(st + code_off[k]);
+        const uint32_t vb = *reinterpret_cast<const uint32_t*>(st + code_off[k] + 8 * 128);
+        const uint4 xv = *reinterpret_cast<const uint4*>(st + x_off[k]);
+        uint32_t ra[4], rb[4];
+        e2m1x8_pairs(va, ra);
+        e2m1x8_pairs(vb, rb);
+        const uint32_t sA = upper[k] ? scA[1] : scA[0], sB = upper[k] ? scB[1] : scB[0];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          ra[i] = mul_bf16x2(ra[i], sA);
+          rb[i] = mul_bf16x2(rb[i], sB);
+        }
+        mma_bf16_16816_pure(acc0, ra[0], rb[0], ra[1], rb[1], prmt(xv.x, xv.z, 0x5410u), prmt(xv.x, xv.z, 0x7632u));
+        mma_bf16_16816_pure(acc1, ra[2], rb[2], ra[3], rb[3], prmt(xv.y, xv.w, 0x5410u), prmt(xv.y, xv.w, 0x7632u));
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bars + 8 * (S + s));
+      if (++s == S) {
+        s = 0;
+        ph ^= 1;
+      }
+    }
+    float* rw = red + (size_t)cw * 16 * 8;
+    rw[g * 8 + 2 * q] = acc0[0] + acc1[0];
+    rw[g * 8 + 2 * q + 1] = acc0[1] + acc1[1];
+    rw[(g + 8) * 8 + 2 * q] = acc0[2] + acc1[2];
+    rw[(g + 8) * 8 + 2 * q + 1] = acc0[3] + acc1[3];
+  }
+  __syncthreads();
+  const float s_enc = fp4dev::global_encode_scale<fp4dev::SF_E4M3>(__ldg(gw), nullptr);
+  const int rows = 16 * T;
+  for (int i = threadIdx.x; i < rows * 8; i += blockDim.x) {
+    const int b = i / rows, r = i % rows;
+    const int n = n0 + r;
+    if (n >= N || b >= batch) continue;
+    const int t = r >> 4, rr = r & 15;
+    const float* p = red + ((size_t)(WPT * t) * 16 + rr) * 8 + b;
+    float v = 0.0f;
+#pragma unroll
+    for (int k = 0; k < WPT; ++k) v = __fadd_rn(v, p[k * 16 * 8]);
+    v = __fdiv_rn(__fmul_rn(v, 256.0f), s_enc);
+    if (bf16_out) static_cast<__nv_bfloat16*>(y)[(int64_t)b * N + n] = __float2bfloat16_rn(v);
+    else static_cast<float*>(y)[(int64_t)b * N + n] = v;
+  }
+}
+
+bool make_map(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t outer,
+              uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swz,
+              CUtensorMapL2promotion l2) {
+  auto fn = fp4async::encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)outer};
+  cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1u, 1u};
+  return fn(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz, l2,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int sm_count() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 148;
+  }
+  return n;
+}
+
+template <int WPT>
+cudaError_t launch_tma_t(const fp4lib::GemvArgs& a, int T, cudaStream_t st) {
+  using L = TvLayout<WPT>;
+  const int64_t tiles = (a.N + 15) / 16;
+  const int64_t ctas = (tiles + T - 1) / T;
+  const int nk = (int)((a.K + L::SC - 1) / L::SC);
+  int S = (int)(TV_RING_BUDGET / L::stage_bytes(T));
+  if (S > TV_MAX_STAGES) S = TV_MAX_STAGES;
+  if (S > nk) S = nk;
+  const size_t smem = 1024 + (size_t)S * L::stage_bytes(T) + (size_t)WPT * T * 16 * 8 * 4 + 16u * S;
+  CUtensorMap mc, ms, mx;
+  if (!make_map(&mc, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.Wq, a.K / 2, a.N, a.K / 2, 128, 16 * T,
+                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B) ||
+      !make_map(&ms, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.Ws, a.K / 16, a.N, a.K / 16, L::SB, 16 * T,
+                CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE) ||
+      !make_map(&mx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.x, a.K, a.batch, a.K * 2, 64, 8,
+                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B))
+    return cudaErrorNotSupported;
+  static size_t smem_set = 0;
+  if (smem > smem_set) {
+    cudaError_t e = cudaFuncSetAttribute(k_gemv_w4a16_tma<WPT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    smem_set = smem;
+  }
+  k_gemv_w4a16_tma<WPT><<<(unsigned)ctas, 32 * (1 + WPT * T), smem, st>>>(mc, ms, mx, a.gw, (int)a.batch, (int)a.N, nk,
+                                                                         T, S, a.bf16_out, a.y, a.status);
+  return cudaGetLastError();
+}
+
+// Returns cudaErrorNotSupported (before launching anything) when the shape or
+// the driver rules the TMA-fed form out.  Four warps per tile (512-column
+// stages) up to six tiles per CTA, two beyond.
+cudaError_t launch_gemv_tma(const fp4lib::GemvArgs& a, cudaStream_t st) {
+  if (a.batch > 8 || a.K % 256 != 0 || a.N > (int64_t)1 << 30 || a.K > (int64_t)1 << 30)
+    return cudaErrorNotSupported;
+  const int64_t tiles = (a.N + 15) / 16;
+  const int sms = sm_count();
+  int T = (int)((tiles + sms - 1) / sms);
+  T = T < 1 ? 1 : (T > TV_MAX_TILES ? TV_MAX_TILES : T);
+  return T <= 6 ? launch_tma_t<4>(a, T, st) : launch_tma_t<2>(a, T, st);
+}
+
 }  // namespace
 
 namespace fp4lib {
 
 cudaError_t launch_gemv(const GemvArgs& a, cudaStream_t st) {
-  // 16 weight rows per CTA; enough warps per CTA (split K) to put about 16
+  const cudaError_t e = launch_gemv_tma(a, st);
+  if (e != cudaErrorNotSupported) return e;
+  // register-fed form: 16 weight rows per CTA; enough warps per CTA (split K) to put about 16
   // warps on each of the GPU's SMs in a single wave
   const int64_t ctas = (a.N + 15) / 16;
   int dev = 0, sms = 148;

@@ -75,6 +75,7 @@ struct GemvArgs {
   int64_t batch, N, K;
   bool bf16_out;
   void* y;
+  int32_t* status;
 };
 cudaError_t launch_gemv(const GemvArgs& a, cudaStream_t st);
 

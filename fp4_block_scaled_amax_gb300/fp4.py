@@ -71,7 +71,7 @@ _SIGS = {
                         _VP, _VP]),
     "fp4_gemm_quantize": (_I32, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _I64, _I64, _I64, _I32, _I32, _VP, _I32,
                                  _U64, _I32, _VP, _VP, _VP, _VP, _VP]),
-    "fp4_gemv_w4a16": (_I32, [_VP, _VP, _VP, _VP, _I64, _I64, _I64, _I32, _VP, _VP]),
+    "fp4_gemv_w4a16": (_I32, [_VP, _VP, _VP, _VP, _I64, _I64, _I64, _I32, _VP, _VP, _VP]),
     "fp4_encode_scales": (_I32, [_VP, _I64, _I32, _VP, _VP, _VP]),
     "fp4_philox_bits16": (_I32, [_U64, _U64, _I64, _VP, _VP]),
     "fp4_status_string": (ctypes.c_char_p, [_I32]),
@@ -207,9 +207,9 @@ def fp4_gemm_quantize(Aq, As, Bq, Bs, ga, gb, tA, tB, M, N, K, fmt, g_out, round
                                     _ptr(dev_status), _stream(stream)), "fp4_gemm_quantize")
 
 
-def fp4_gemv_w4a16(Wq, Ws, gw, x, batch, N, K, out_dtype, y, stream=None):
+def fp4_gemv_w4a16(Wq, Ws, gw, x, batch, N, K, out_dtype, y, dev_status=None, stream=None):
     _check(_lib().fp4_gemv_w4a16(_ptr(Wq), _ptr(Ws), _ptr(gw), _ptr(x), batch, N, K, int(out_dtype), _ptr(y),
-                                 _stream(stream)), "fp4_gemv_w4a16")
+                                 _ptr(dev_status), _stream(stream)), "fp4_gemv_w4a16")
 
 
 def fp4_encode_scales(s, fmt, codes, decoded, stream=None):

@@ -109,10 +109,10 @@ def test_gemm_argument_errors():
 
 def test_gemv_and_misc_argument_errors():
     lib = _need_lib()
-    assert lib.fp4_gemv_w4a16(P, P, P, P, 0, 128, 256, 0, P, None) == fp4.FP4_ERR_SHAPE
-    assert lib.fp4_gemv_w4a16(P, P, P, P, 65, 128, 256, 0, P, None) == fp4.FP4_ERR_SHAPE
-    assert lib.fp4_gemv_w4a16(P, P, P, P, 1, 128, 48, 0, P, None) == fp4.FP4_ERR_SHAPE
-    assert lib.fp4_gemv_w4a16(P, P, None, P, 1, 128, 256, 0, P, None) == fp4.FP4_ERR_INVALID_ARG
+    assert lib.fp4_gemv_w4a16(P, P, P, P, 0, 128, 256, 0, P, None, None) == fp4.FP4_ERR_SHAPE
+    assert lib.fp4_gemv_w4a16(P, P, P, P, 65, 128, 256, 0, P, None, None) == fp4.FP4_ERR_SHAPE
+    assert lib.fp4_gemv_w4a16(P, P, P, P, 1, 128, 48, 0, P, None, None) == fp4.FP4_ERR_SHAPE
+    assert lib.fp4_gemv_w4a16(P, P, None, P, 1, 128, 256, 0, P, None, None) == fp4.FP4_ERR_INVALID_ARG
     assert lib.fp4_amax(P, 4, 12, 12, P, None) == fp4.FP4_ERR_SHAPE
     assert lib.fp4_amax(P, 4, 16, 16, None, None) == fp4.FP4_ERR_INVALID_ARG
     assert lib.fp4_dequantize(P, P, 0, 4, 24, 0, P, 0, P, None) == fp4.FP4_ERR_SHAPE

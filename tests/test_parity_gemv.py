@@ -39,3 +39,43 @@ def test_gemv_ragged_rows_and_k():
     W = synth.normal((1000, 1056), 30, 0, std=0.02)  # N not a multiple of 16, K % 128 = 32
     x = synth.normal((5, 1056), 30, 1)
     run(W, x)
+
+
+def test_gemv_ragged_rows_tma_form():
+    # batch <= 8 and K % 256 == 0 take the shared-memory (TMA) form; N = 1000
+    # leaves the last CTA's tiles partly past the end of W
+    W = synth.normal((1000, 1024), 31, 0, std=0.02)
+    for b in (1, 5, 8):
+        run(W, synth.normal((b, 1024), 31, b))
+
+
+def test_gemv_wide_scale_range():
+    # block amaxes spread over 2^-20 .. 1 of the tensor amax: E4M3 block scales
+    # down to the subnormal codes, and every E2M1 code, including +-0.5
+    rng = np.random.default_rng(32)
+    N, K = 512, 2048
+    mag = 2.0 ** rng.uniform(-20, 0, (N, K // 16))
+    W = rng.standard_normal((N, K)) * np.repeat(mag, 16, axis=1)
+    W = torch.from_numpy(W.astype(np.float32)).to(torch.bfloat16)
+    qw = Q.quantize(f32(W), "E4M3")
+    assert (qw["scales"] < 8).any() and (qw["scales"] > 0).any()  # subnormal scale codes occur
+    nib = np.concatenate([qw["codes"] & 15, qw["codes"] >> 4])
+    assert np.isin(np.arange(16), nib).all()
+    for b in (2, 8):
+        run(W, synth.normal((b, K), 32, b), "bf16")
+
+
+def test_gemv_status_word_stays_clear():
+    fp4 = lib()
+    W = synth.normal((4608, 768), 33, 0, std=0.02)
+    x = synth.normal((8, 768), 33, 1)
+    qw = Q.quantize(f32(W), "E4M3")
+    y = torch.empty((8, 4608), dtype=torch.float32, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    gw = torch.tensor([qw["amax"]], dtype=torch.float32, device="cuda")
+    for _ in range(3):
+        fp4.fp4_gemv_w4a16(dev(qw["codes"]), dev(qw["scales"]), gw, dev(x), 8, 4608, 768, fp4.FP4_OUT_F32, y,
+                           dev_status=st)
+    assert int(host(st)[0]) == 0
+    yr, S = Gm.gemv_ref(qw["codes"], qw["scales"], qw["amax"], f32(x))
+    assert (np.abs(host(y) - yr) <= Gm.gemm_bound(S)).all()
