@@ -51,13 +51,18 @@ STEP_FLOPS = 3 * 2 * M_TOK * N_FFN * K_HID
 WORKLOAD = "llama2-7b-mlp-linear-fwd-bwd"
 METRIC = "NVFP4 GEMM TFLOPS & quantize GB/s at 7B shapes, % of FP4-MMA/HBM peak"
 FP4_PER_BF16 = 6.0  # nominal dense FP4 / bf16 tensor ratio on GB300 (13.5 / 2.25 PFLOP/s)
-# DRAM bytes (read + write) from one ncu capture, valid only while the kernel
-# sources still hash to the recorded value.  quant_dual: the step's three dual
-# quantizations, captured at 8192 tokens and scaled by the rows processed
-# (streaming kernel: X and dY scale with tokens, W does not).  The GEMM's
-# traffic does not scale in proportion with tokens and is reported as null.
-NCU_TRAFFIC = {"quant_dual": {"bytes": 698.0e6, "src": "2fa66c14db1d343f",
-                              "files": ["quantize.cu", "fp4_device.cuh"]}}
+# DRAM bytes (read + write) per launch from one ncu capture of the full-size
+# step (`ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum`, one pass),
+# valid only while the kernel sources still hash to the recorded value.
+# gemm: mean over the fwd, dgrad and wgrad launches; quant_dual: the step's
+# three dual quantizations together; gemv: one launch.  Writes still held in
+# L2 when a kernel ends do not appear in its DRAM bytes.
+NCU_TRAFFIC = {"gemm": {"bytes": 290.8e6, "src": "92954cfdc17a7e4b",
+                        "files": ["gemm_sm103.cu", "async_sm103.cuh", "fp4_device.cuh"]},
+               "quant_dual": {"bytes": 757.8e6, "src": "3b5bfecadef66cf0",
+                              "files": ["quantize.cu", "fp4_device.cuh"]},
+               "gemv": {"bytes": 25.45e6, "src": "17b46c52569c69be",
+                        "files": ["gemv.cu", "async_sm103.cuh", "fp4_device.cuh"]}}
 
 
 def parse():
@@ -68,6 +73,8 @@ def parse():
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-studies", action="store_true",
+                   help="skip the side measurements after the timed steps (for ncu launch lists)")
     p.add_argument("--tokens", type=int, default=16384,
                    help="token count M (default: the workload's 16384; smaller only for ncu captures)")
     return p.parse_args()
@@ -547,11 +554,14 @@ def run_ours(args, rank, world, local):
         return t["bytes"] if t and t["src"] == src_hash(t["files"]) and M_TOK == 16384 else None
     traffic_v = traffic_of("gemm")
     qtraffic_v = traffic_of("quant_dual")
+    gvtraffic_v = traffic_of("gemv")
 
-    qmodes = quantizer_modes(step, flush)
-    sweep = scale_format_sweep(step.fp4, flush, device)
-    hadamard = hadamard_study(step, step.fp4, flush, device)
-    fused_ep = fused_epilogue_study(step, flush)
+    qmodes = sweep = hadamard = fused_ep = None
+    if not args.no_studies:
+        qmodes = quantizer_modes(step, flush)
+        sweep = scale_format_sweep(step.fp4, flush, device)
+        hadamard = hadamard_study(step, step.fp4, flush, device)
+        fused_ep = fused_epilogue_study(step, flush)
     e2e = None
     if not args.no_e2e:
         e2e = run_e2e(step, d, args, world, device)
@@ -587,7 +597,7 @@ def run_ours(args, rank, world, local):
         "fused_epilogue_quantize": fused_ep,
         "amax_gbs": round(a_gbs, 1),
         "gemv_w4a16": {"batch": GEMV_BATCH, "N": N_FFN, "K": K_HID, "us": round(statistics.mean(gemv_ms) * 1e3, 2),
-                       "GB/s": round(gv_gbs, 1), "frac": round(gv_gbs / hbm, 4)},
+                       "GB/s": round(gv_gbs, 1), "frac": round(gv_gbs / hbm, 4), "traffic": gvtraffic_v},
         "kernel_ms": {"fwd_gemm": round(statistics.mean(fwd_ms), 4),
                       "gemm_mean": round(statistics.mean(gemm_ms), 4),
                       "quant_dual_total": round(sum(quant_ms) / args.steps, 4),
