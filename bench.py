@@ -440,6 +440,83 @@ def hadamard_study(step, fp4, flush, device, reps=5):
     return out
 
 
+def step_variants_study(step, flush, reps=5):
+    """The linear layer's forward + backward (three quantizations, three
+    GEMMs; no GEMV) in four forms, each timed end to end with CUDA events
+    after an L2 flush: bf16 cuBLAS GEMMs (torch.matmul, the BF16 baseline the
+    UE5M3 blog compares against), FP4 with a fresh amax per tensor (the timed
+    step), FP4 with the stored amax (the UE5M3 recipe between refreshes, no
+    amax pass), and FP4 with the 16 x 16 random Hadamard transform and fresh
+    amaxes of the transformed tensors (the variant the recipe removes).
+    Outside the timed step."""
+    fp4 = step.fp4
+    M, K, N = M_TOK, K_HID, N_FFN
+    RNE, SR, MMA, BF = fp4.FP4_ROUND_RNE, fp4.FP4_ROUND_STOCHASTIC, fp4.FP4_SFLAYOUT_MMA, fp4.FP4_OUT_BF16
+    dev = step.Y.device
+    plan = [("X", RNE, 0, SR, 1236), ("W", RNE, 0, RNE, 0), ("dY", SR, 1234, SR, 1235)]
+    rht_amax = torch.zeros(6, dtype=torch.float32, device=dev)
+    qX, qW, qd = step.q["X"], step.q["W"], step.q["dY"]
+    st = torch.cuda.current_stream()
+
+    def gemms(a):
+        aX, aW, ad = a[0:1], a[1:2], a[2:3]
+        fp4.fp4_gemm(qX[0], qX[1], qW[0], qW[1], aX, aW, None, None, M, N, K, "E4M3", BF, step.Y)
+        fp4.fp4_gemm(qd[0], qd[1], qW[2], qW[3], ad, aW, None, None, M, K, N, "E4M3", BF, step.dX)
+        fp4.fp4_gemm(qd[2], qd[3], qX[2], qX[3], ad, aX, None, None, N, K, M, "E4M3", BF, step.dW)
+
+    def bf16_step():
+        torch.matmul(step.X, step.W.t(), out=step.Y)
+        torch.matmul(step.dY, step.W, out=step.dX)
+        torch.matmul(step.dY.t(), step.X, out=step.dW)
+
+    def fp4_step(fresh):
+        for j, (name, rr, sr, rc, sc) in enumerate(plan):
+            x, a = getattr(step, name), step.amax[j:j + 1]
+            if fresh:
+                fp4.fp4_amax(x, a)
+            cr, srs, cc, scs = step.q[name]
+            fp4.fp4_quantize_dual(x, "E4M3", rr, sr, rc, sc, a, MMA, cr, srs, cc, scs)
+        gemms(step.amax)
+
+    def rht_step():
+        for j, (name, rr, sr, rc, sc) in enumerate(plan):
+            cr, srs, cc, scs = step.q[name]
+            fp4.fp4_quantize_dual_rht(getattr(step, name), "E4M3", rr, sr, rc, sc, RHT_MASK, None, None, MMA,
+                                      cr, srs, cc, scs, rht_amax[2 * j:2 * j + 1], rht_amax[2 * j + 1:2 * j + 2])
+        # rows of X, W, dY carry their row-transform amax; the transposed operands their column one
+        fp4.fp4_gemm(qX[0], qX[1], qW[0], qW[1], rht_amax[0:1], rht_amax[2:3], None, None, M, N, K, "E4M3", BF,
+                     step.Y)
+        fp4.fp4_gemm(qd[0], qd[1], qW[2], qW[3], rht_amax[4:5], rht_amax[3:4], None, None, M, K, N, "E4M3", BF,
+                     step.dX)
+        fp4.fp4_gemm(qd[2], qd[3], qX[2], qX[3], rht_amax[5:6], rht_amax[1:2], None, None, N, K, M, "E4M3", BF,
+                     step.dW)
+
+    variants = [("bf16_cublas", bf16_step), ("fp4_fresh_amax", lambda: fp4_step(True)),
+                ("fp4_stored_amax", lambda: fp4_step(False)), ("fp4_rht16_fresh_amax", rht_step)]
+    flops = 3 * 2 * M * N * K
+    res = {"linear": f"fwd + dgrad + wgrad, {M} tokens x {K} -> {N}", "unit": "ms"}
+    for name, fn in variants:
+        fn()
+        ts = []
+        for _ in range(reps):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(st)
+            fn()
+            e1.record(st)
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        ms = statistics.median(ts)
+        res[name] = {"ms": round(ms, 4), "TFLOP/s": round(flops / (ms * 1e-3) / 1e12, 1)}
+    base = res["bf16_cublas"]["ms"]
+    for name in ("fp4_fresh_amax", "fp4_stored_amax", "fp4_rht16_fresh_amax"):
+        res[name]["speedup_vs_bf16"] = round(base / res[name]["ms"], 3)
+    res["rht_removal_gain"] = round(res["fp4_rht16_fresh_amax"]["ms"] / res["fp4_fresh_amax"]["ms"] - 1, 4)
+    torch.cuda.synchronize()
+    assert int(step.status.item()) == 0
+    return res
+
+
 def fused_epilogue_study(step, flush, reps=5):
     """The forward GEMM Y = X W^T with Y quantized for the next layer (NVFP4,
     RNE rows, the stored amax of Y): the GEMM writing bf16 Y followed by the
@@ -556,8 +633,9 @@ def run_ours(args, rank, world, local):
     qtraffic_v = traffic_of("quant_dual")
     gvtraffic_v = traffic_of("gemv")
 
-    qmodes = sweep = hadamard = fused_ep = None
+    qmodes = sweep = hadamard = fused_ep = variants = None
     if not args.no_studies:
+        variants = step_variants_study(step, flush)
         qmodes = quantizer_modes(step, flush)
         sweep = scale_format_sweep(step.fp4, flush, device)
         hadamard = hadamard_study(step, step.fp4, flush, device)
@@ -595,6 +673,7 @@ def run_ours(args, rank, world, local):
         "scale_format_sweep": sweep,
         "hadamard_16x16": hadamard,
         "fused_epilogue_quantize": fused_ep,
+        "step_variants": variants,
         "amax_gbs": round(a_gbs, 1),
         "gemv_w4a16": {"batch": GEMV_BATCH, "N": N_FFN, "K": K_HID, "us": round(statistics.mean(gemv_ms) * 1e3, 2),
                        "GB/s": round(gv_gbs, 1), "frac": round(gv_gbs / hbm, 4), "traffic": gvtraffic_v},
