@@ -305,3 +305,41 @@ def ue5m3_reencode_e4m3(scales: np.ndarray, t: int):
     code = codec.encode(v)
     exact = bool(np.all(codec.decode(code) == v))
     return code, exact
+
+
+# ---------------------------------------------------------------------------
+# UE5M3 scales wider than one E4M3 window ("UE5M3 ..." blog, section
+# "Ограничения", the same software emulation).  Reading fixed here: with
+# e(s) = floor(log2 s) for every nonzero scale value and e_max the largest,
+# scale s belongs to window w = floor((e_max - e(s)) / 14), and window w is
+# re-encoded as E4M3 with the shift t_w = e_max - 7 - 14 w (window 0 is the
+# single shift above).  Inside a window e(s) - t_w lies in [-6, 7], the normal
+# E4M3 exponents, and a UE5M3 value has at most 4 significant bits, so every
+# re-encode is exact.  UE5M3 values span 2^-17 .. 1.75 * 2^16, so three
+# windows always suffice.  A GEMM over UE5M3 operands is then the sum, over
+# window pairs (wa, wb), of the E4M3 GEMMs with every other window's scales
+# set to zero, each multiplied by 2^(t_wa + t_wb).
+# ---------------------------------------------------------------------------
+
+UE5M3_WINDOW_BINADES = 14
+UE5M3_MAX_WINDOWS = 3
+
+
+def ue5m3_windows(scales: np.ndarray):
+    """(shifts t_w for w = 0..2, E4M3 codes per window [3, *scales.shape],
+    number of windows in use)."""
+    v = scale_values(scales, "UE5M3")
+    nz = v > 0
+    t0 = ue5m3_shift(scales)
+    e_max = t0 + 7
+    e = np.zeros(v.shape, dtype=np.int64)
+    e[nz] = np.frexp(v[nz])[1].astype(np.int64) - 1
+    w = np.where(nz, (e_max - e) // UE5M3_WINDOW_BINADES, -1)
+    shifts = [e_max - 7 - UE5M3_WINDOW_BINADES * k for k in range(UE5M3_MAX_WINDOWS)]
+    codec = F.CODECS["E4M3"]
+    out = np.zeros((UE5M3_MAX_WINDOWS,) + v.shape, dtype=np.uint8)
+    for k in range(UE5M3_MAX_WINDOWS):
+        sel = w == k
+        out[k][sel] = codec.encode(v[sel] * (2.0 ** -shifts[k]))
+    n_windows = int(w.max()) + 1 if nz.any() else 1
+    return shifts, out, n_windows

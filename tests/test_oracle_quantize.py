@@ -357,3 +357,67 @@ def test_int4_sr_unbiased_4sigma(y):
     sigma = np.sqrt(p * (1 - p) / n)
     assert abs(v.mean() - y) < 4 * sigma + 1e-12
     assert set(np.unique(v)) <= {lo, lo + 1}
+
+
+# ---------------------------------------------------------------------------
+# UE5M3 scales split into E4M3 windows (the multi-pass UE5M3 GEMM)
+# ---------------------------------------------------------------------------
+
+def _ue5m3_codes_of(values):
+    c = F.CODECS["UE5M3"].encode(np.asarray(values, dtype=np.float64))
+    assert np.array_equal(F.CODECS["UE5M3"].decode(c), values)
+    return c
+
+
+def test_ue5m3_windows_reconstruct_every_code():
+    rng = np.random.default_rng(40)
+    for top in (0xFE, 0xC3, 0x80, 0x41):  # different largest scales
+        codes = np.arange(top + 1, dtype=np.uint8)
+        rng.shuffle(codes)
+        t, out, n = Q.ue5m3_windows(codes)
+        v = F.CODECS["UE5M3"].decode(codes)
+        rec = sum(F.CODECS["E4M3"].decode(out[k]) * 2.0 ** t[k] for k in range(3))
+        assert np.array_equal(rec, v)
+        assert np.array_equal((out > 0).sum(axis=0), (v > 0).astype(int))  # one window per nonzero scale
+        assert t == [t[0], t[0] - 14, t[0] - 28] and t[0] == Q.ue5m3_shift(codes)
+        # every window's E4M3 values are normal (or zero): exponents -6 .. 7
+        for k in range(3):
+            d = F.CODECS["E4M3"].decode(out[k])
+            nz = d[d > 0]
+            assert nz.size == 0 or (nz.min() >= 2.0 ** -6 and nz.max() < 2.0 ** 8)
+
+
+def test_ue5m3_windows_single_window_is_the_single_shift():
+    rng = np.random.default_rng(41)
+    v = 2.0 ** rng.integers(-5, 9, 500) * rng.choice([1, 1.125, 1.5, 1.875], 500)  # 13 binades
+    codes = _ue5m3_codes_of(v)
+    t, out, n = Q.ue5m3_windows(codes)
+    ref, exact = Q.ue5m3_reencode_e4m3(codes, Q.ue5m3_shift(codes))
+    assert n == 1 and exact and np.array_equal(out[0], ref) and not out[1:].any()
+
+
+@pytest.mark.parametrize("low,n", [(-13, 1), (-14, 2), (-27, 2), (-28, 3), (-33, 3)])
+def test_ue5m3_window_count_closed_form(low, n):
+    # largest scale 2^16, smallest 2^(16 + low): window of the smallest = floor(-low / 14)
+    v = np.array([2.0 ** 16, 2.0 ** (16 + low), 0.0, 2.0 ** 16])
+    t, out, nw = Q.ue5m3_windows(_ue5m3_codes_of(v))
+    assert nw == n and t[0] == 16 - 7
+    assert out[n - 1][1] != 0 and out[0][2] == 0
+
+
+def test_windowed_gemm_equals_the_ue5m3_gemm():
+    from oracle import gemm as Gm
+    rng = np.random.default_rng(42)
+    M, N, K = 24, 40, 128
+    Aq = rng.integers(0, 256, (M, K // 2), dtype=np.uint8)
+    Bq = rng.integers(0, 256, (N, K // 2), dtype=np.uint8)
+    As = _ue5m3_codes_of(2.0 ** rng.integers(-17, 17, (M, K // 16)) * 1.0)
+    Bs = _ue5m3_codes_of(2.0 ** rng.integers(-10, 17, (N, K // 16)) * 1.5 / 1.5)
+    ga, gb = 3.0, 0.25
+    C, S = Gm.gemm_ref(Aq, As, ga, Bq, Bs, gb, "UE5M3")
+    ta, wa, na = Q.ue5m3_windows(As)
+    tb, wb, nb = Q.ue5m3_windows(Bs)
+    assert na == 3 and nb == 2
+    Cw = sum(Gm.gemm_ref(Aq, wa[i], ga, Bq, wb[j], gb, "E4M3")[0] * 2.0 ** (ta[i] + tb[j])
+             for i in range(na) for j in range(nb))
+    assert np.allclose(Cw, C, rtol=1e-12, atol=1e-12 * S.max())
