@@ -57,9 +57,9 @@ FP4_PER_BF16 = 6.0  # nominal dense FP4 / bf16 tensor ratio on GB300 (13.5 / 2.2
 # gemm: mean over the fwd, dgrad and wgrad launches; quant_dual: the step's
 # three dual quantizations together; gemv: one launch.  Writes still held in
 # L2 when a kernel ends do not appear in its DRAM bytes.
-NCU_TRAFFIC = {"gemm": {"bytes": 290.8e6, "src": "92954cfdc17a7e4b",
+NCU_TRAFFIC = {"gemm": {"bytes": 291.0e6, "src": "7caa10f11717ccc4",
                         "files": ["gemm_sm103.cu", "async_sm103.cuh", "fp4_device.cuh"]},
-               "quant_dual": {"bytes": 757.8e6, "src": "3b5bfecadef66cf0",
+               "quant_dual": {"bytes": 758.0e6, "src": "4e39ab39f16f087e",
                               "files": ["quantize.cu", "fp4_device.cuh"]},
                "gemv": {"bytes": 25.45e6, "src": "17b46c52569c69be",
                         "files": ["gemv.cu", "async_sm103.cuh", "fp4_device.cuh"]}}
@@ -517,6 +517,78 @@ def step_variants_study(step, flush, reps=5):
     return res
 
 
+def ue5m3_windows_study(step, flush, reps=3):
+    """The forward GEMM 16384 x 11008 x 4096 on UE5M3 operands (float32 out):
+    the single-shift path (fp4_ue5m3_to_e4m3 + fp4_gemm) against the
+    window path (fp4_ue5m3_windows + fp4_gemm_ue5m3_windows), A = X with a
+    fresh amax (one window: the window path only adds launches), and A = a
+    seeded 16384 x 4096 tensor whose 16-element blocks are scaled by
+    2^U(-30, 0), with a stored amax 256x below its maximum (scales from
+    UE5M3's top to its bottom: three windows, where the single shift is not
+    exact).  B = W, fresh amax.  Scale preparation included in both.
+    Outside the timed step."""
+    fp4 = step.fp4
+    M, N, K = M_TOK, N_FFN, K_HID
+    dev = step.Y.device
+    RNE, MMA = fp4.FP4_ROUND_RNE, fp4.FP4_SFLAYOUT_MMA
+    u8 = dict(dtype=torch.uint8, device=dev)
+    i32 = dict(dtype=torch.int32, device=dev)
+    C = torch.empty((M, N), dtype=torch.float32, device=dev)
+    st = torch.cuda.current_stream()
+    res = {"gemm": f"fwd {M}x{N}x{K}, UE5M3 scales, float32 out", "unit": "ms"}
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(60)
+    wide = torch.randn(M, K, device=dev, generator=gen)
+    wide = (wide * torch.exp2(-30.0 * torch.rand(M, K // 16, device=dev, generator=gen)).repeat_interleave(16, 1))
+    wide = wide.to(torch.bfloat16)
+    wide_amax = (wide.float().abs().max() / 256.0).reshape(1)
+    for label, a_in, a_amax in (("X_fresh_amax", step.X, step.amax[0:1]),
+                                ("wide_blocks_stored_amax", wide, wide_amax)):
+        ops = {}
+        for name, x, amax in (("X", a_in, a_amax), ("W", step.W, step.amax[1:2])):
+            R = x.shape[0]
+            codes, scales = torch.empty((R, K // 2), **u8), torch.empty(R * K // 16, **u8)
+            amax = amax.contiguous().clone()
+            fp4.fp4_quantize(x, "UE5M3", RNE, 0, amax, False, MMA, codes, scales, None)
+            ops[name] = (codes, scales, amax, torch.empty_like(scales), torch.zeros(1, **i32),
+                         torch.empty(3 * scales.numel(), **u8), torch.zeros(3, **i32), torch.zeros(1, **i32))
+        (xc, xs, xa, xe, xt, xw, xwt, xn), (wc, ws, wa, we, wt, ww, wwt, wn) = ops["X"], ops["W"]
+
+        def single():
+            fp4.fp4_ue5m3_to_e4m3(xs, xt, xe)
+            fp4.fp4_ue5m3_to_e4m3(ws, wt, we)
+            fp4.fp4_gemm(xc, xe, wc, we, xa, wa, xt, wt, M, N, K, "UE5M3", fp4.FP4_OUT_F32, C)
+
+        def windows():
+            fp4.fp4_ue5m3_windows(xs, xwt, xn, xw)
+            fp4.fp4_ue5m3_windows(ws, wwt, wn, ww)
+            fp4.fp4_gemm_ue5m3_windows(xc, xw, xwt, xn, wc, ww, wwt, wn, xa, wa, M, N, K, C)
+
+        out = {}
+        for name, fn in (("single_shift", single), ("windows", windows)):
+            fn()
+            ts = []
+            for _ in range(reps):
+                flush.zero_()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(st)
+                fn()
+                e1.record(st)
+                torch.cuda.synchronize()
+                ts.append(e0.elapsed_time(e1))
+            out[name] = round(statistics.median(ts), 4)
+        out["windows_in_use"] = [int(xn.item()), int(wn.item())]
+        # how far the single shift's result (inexact scales rounded) is from the exact window sum
+        windows()
+        ref = C.clone()
+        single()
+        out["single_shift_rel_err"] = float((C - ref).norm() / ref.norm())
+        del ref
+        res[label] = out
+    del wide
+    return res
+
+
 def fused_epilogue_study(step, flush, reps=5):
     """The forward GEMM Y = X W^T with Y quantized for the next layer (NVFP4,
     RNE rows, the stored amax of Y): the GEMM writing bf16 Y followed by the
@@ -633,9 +705,10 @@ def run_ours(args, rank, world, local):
     qtraffic_v = traffic_of("quant_dual")
     gvtraffic_v = traffic_of("gemv")
 
-    qmodes = sweep = hadamard = fused_ep = variants = None
+    qmodes = sweep = hadamard = fused_ep = variants = windows = None
     if not args.no_studies:
         variants = step_variants_study(step, flush)
+        windows = ue5m3_windows_study(step, flush)
         qmodes = quantizer_modes(step, flush)
         sweep = scale_format_sweep(step.fp4, flush, device)
         hadamard = hadamard_study(step, step.fp4, flush, device)
@@ -674,6 +747,7 @@ def run_ours(args, rank, world, local):
         "hadamard_16x16": hadamard,
         "fused_epilogue_quantize": fused_ep,
         "step_variants": variants,
+        "ue5m3_windows": windows,
         "amax_gbs": round(a_gbs, 1),
         "gemv_w4a16": {"batch": GEMV_BATCH, "N": N_FFN, "K": K_HID, "us": round(statistics.mean(gemv_ms) * 1e3, 2),
                        "GB/s": round(gv_gbs, 1), "frac": round(gv_gbs / hbm, 4), "traffic": gvtraffic_v},

@@ -295,6 +295,60 @@ fp4_status fp4_ue5m3_to_e4m3(const uint8_t* ue5m3_scales, int64_t n, int32_t* t_
                                                   (cudaStream_t)stream));
 }
 
+fp4_status fp4_ue5m3_windows(const uint8_t* ue5m3_scales, int64_t n, int32_t* t_out, int32_t* n_windows_out,
+                             uint8_t* e4m3_out, int32_t* dev_status, fp4_stream_t stream) {
+  if (n < 0) return FP4_ERR_SHAPE;
+  if (t_out == nullptr || n_windows_out == nullptr) return FP4_ERR_INVALID_ARG;
+  if (n > 0 && (ue5m3_scales == nullptr || e4m3_out == nullptr)) return FP4_ERR_INVALID_ARG;
+  return cuda_status(fp4lib::launch_ue5m3_windows(ue5m3_scales, n, t_out, n_windows_out, e4m3_out, dev_status,
+                                                  (cudaStream_t)stream));
+}
+
+fp4_status fp4_gemm_ue5m3_windows(const uint8_t* Aq, const uint8_t* As_windows, const int32_t* tA,
+                                  const int32_t* nA, const uint8_t* Bq, const uint8_t* Bs_windows,
+                                  const int32_t* tB, const int32_t* nB, const float* ga, const float* gb,
+                                  int64_t M, int64_t N, int64_t K, float* C, int64_t ldc, int32_t* dev_status,
+                                  fp4_stream_t stream) {
+  if (Aq == nullptr || As_windows == nullptr || tA == nullptr || nA == nullptr || Bq == nullptr ||
+      Bs_windows == nullptr || tB == nullptr || nB == nullptr || ga == nullptr || gb == nullptr || C == nullptr)
+    return FP4_ERR_INVALID_ARG;
+  if (M <= 0 || N <= 0 || K <= 0 || M % 128 != 0 || N % 256 != 0 || K % 256 != 0 || ldc < N) return FP4_ERR_SHAPE;
+  if (!aligned16(Aq) || !aligned16(As_windows) || !aligned16(Bq) || !aligned16(Bs_windows) || !aligned16(C) ||
+      (ldc * 4) % 16 != 0)
+    return FP4_ERR_ALIGNMENT;
+  // one window's scale array: M*K/16 (A) or N*K/16 (B) bytes, a multiple of 16
+  const int64_t a_win = M * K / 16, b_win = N * K / 16;
+  fp4lib::GemmArgs a{};
+  a.Aq = Aq;
+  a.Bq = Bq;
+  a.ga = ga;
+  a.gb = gb;
+  a.M = M;
+  a.N = N;
+  a.K = K;
+  a.ldc = ldc;
+  a.fmt = (int)FP4_SF_UE5M3;
+  a.bf16_out = false;
+  a.C = C;
+  a.status = dev_status;
+  a.wcount_a = nA;
+  a.wcount_b = nB;
+  for (int wa = 0; wa < 3; ++wa) {
+    for (int wb = 0; wb < 3; ++wb) {
+      a.As = As_windows + wa * a_win;
+      a.Bs = Bs_windows + wb * b_win;
+      a.tA = tA + wa;
+      a.tB = tB + wb;
+      a.wa = wa;
+      a.wb = wb;
+      a.accumulate = wa != 0 || wb != 0;  // window pair (0, 0) always runs and stores C
+      const fp4_status s = cuda_status(fp4lib::launch_gemm(a, (cudaStream_t)stream));
+      if (s != FP4_OK) return s;
+    }
+  }
+  return FP4_OK;
+}
+
 fp4_status fp4_gemm(const uint8_t* Aq, const uint8_t* As, const uint8_t* Bq, const uint8_t* Bs, const float* ga,
                     const float* gb, const int32_t* tA, const int32_t* tB, int64_t M, int64_t N, int64_t K,
                     fp4_scale_fmt f, fp4_gemm_layout layout, fp4_out_dtype od, void* C, int64_t ldc,

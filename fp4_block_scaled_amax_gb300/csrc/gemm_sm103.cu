@@ -125,6 +125,14 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t sr
                "r"(src), "r"(x), "r"(y)
                : "memory");
 }
+// The same store, added element-wise to what the destination holds (float32
+// add for a float32 map): the later passes of a multi-pass GEMM.
+__device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* map, uint32_t src, int x, int y) {
+  asm volatile("cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(src), "r"(x), "r"(y)
+               : "memory");
+}
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
@@ -285,7 +293,18 @@ struct Params {
   float* q_amax_out;
   uint64_t q_seed;
   int q_sr, q_mma;
+  // multi-pass GEMM (UE5M3 scale windows): add to C instead of storing it, and
+  // skip the launch when window wa of A or wb of B is unused (device counts)
+  int accumulate;
+  const int32_t* wcount_a;
+  const int32_t* wcount_b;
+  int wa, wb;
 };
+
+// True when this launch is a multi-pass GEMM pass over an unused window.
+__device__ __forceinline__ bool skip_pass(const Params& p) {
+  return p.wcount_a != nullptr && (p.wa >= __ldg(p.wcount_a) || p.wb >= __ldg(p.wcount_b));
+}
 
 // Epilogue of one warp: 32 accumulator rows (row0.., one per lane) x 64
 // columns held in r, scaled by alpha, converted, staged in shared memory as
@@ -293,7 +312,7 @@ struct Params {
 template <bool BF16, class PL>
 __device__ __forceinline__ void store_block(const uint32_t (&r)[2][32], float alpha, uint8_t* stage_buf,
                                             uint32_t stage_addr, const CUtensorMap* tmap_c, int row0, int col0,
-                                            int lane) {
+                                            int lane, bool accumulate) {
   constexpr int OB = PL::OUT_ROW_BYTES;
   constexpr int BLK_COLS = OB / (BF16 ? 2 : 4);  // columns per staged row
   constexpr int VECS = OB / 16;                  // 16-byte vectors per staged row
@@ -330,7 +349,8 @@ __device__ __forceinline__ void store_block(const uint32_t (&r)[2][32], float al
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     __syncwarp();
     if (lane == 0) {
-      tma_store_2d(tmap_c, stage_addr, col0 + BLK_COLS * b, row0);
+      if (accumulate) tma_reduce_add_2d(tmap_c, stage_addr, col0 + BLK_COLS * b, row0);
+      else tma_store_2d(tmap_c, stage_addr, col0 + BLK_COLS * b, row0);
       bulk_commit();
     }
   }
@@ -404,6 +424,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   constexpr int SMEM_OUT = PL::SMEM_OUT, SMEM_BAR = PL::SMEM_BAR, STAGE_BYTES = PL::STAGE_BYTES;
   constexpr uint32_t TMEM_COLS = PL::TMEM_COLS, TMEM_SFA = PL::TMEM_SFA, TMEM_SFB = PL::TMEM_SFB;
 
+  if (skip_pass(p)) return;  // uniform: before any barrier, cluster sync or tensor memory
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
@@ -650,7 +671,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_acc_empty);
       store_block<BF16, PL>(r, alpha, stage_buf, stage_addr, &tmap_c, mt * BM + 32 * quarter,
-                            nt * BN + EPI_COLS * cblk, lane);
+                            nt * BN + EPI_COLS * cblk, lane, p.accumulate != 0);
     }
     if (lane == 0) bulk_wait0();
     __syncwarp();
@@ -700,6 +721,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   constexpr int SMEM_OUT = PL::SMEM_OUT, SMEM_BAR = PL::SMEM_BAR, STAGE_BYTES = PL::STAGE_BYTES;
   constexpr uint32_t TMEM_COLS = PL::TMEM_COLS, TMEM_SFA = PL::TMEM_SFA, TMEM_SFB = PL::TMEM_SFB;
 
+  if (skip_pass(p)) return;  // uniform: before any barrier, cluster sync or tensor memory
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
@@ -967,7 +989,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                        s_enc_out, amax_local);
       } else {
         store_block<BF16, PL>(r, alpha, stage_buf, stage_addr, &tmap_c, mp * PM + BM * (int)crank + 32 * quarter,
-                              nt * BN + EPI_COLS * cblk, lane);
+                              nt * BN + EPI_COLS * cblk, lane, p.accumulate != 0);
       }
     }
     if constexpr (QOUT) {
@@ -1057,6 +1079,11 @@ cudaError_t launch_t(const fp4lib::GemmArgs& a, cudaStream_t st) {
   p.ga = a.ga;
   p.gb = a.gb;
   p.tA = a.tA;
+  p.accumulate = a.accumulate ? 1 : 0;
+  p.wcount_a = a.wcount_a;
+  p.wcount_b = a.wcount_b;
+  p.wa = a.wa;
+  p.wb = a.wb;
   p.tB = a.tB;
   p.M = (int)a.M;
   p.N = (int)a.N;
@@ -1110,6 +1137,11 @@ cudaError_t launch_pair(const fp4lib::GemmArgs& a, cudaStream_t st) {
   p.ga = a.ga;
   p.gb = a.gb;
   p.tA = a.tA;
+  p.accumulate = a.accumulate ? 1 : 0;
+  p.wcount_a = a.wcount_a;
+  p.wcount_b = a.wcount_b;
+  p.wa = a.wa;
+  p.wb = a.wb;
   p.tB = a.tB;
   p.M = (int)a.M;
   p.N = (int)a.N;

@@ -25,6 +25,10 @@ cudaError_t launch_dequantize(const uint8_t* codes, const uint8_t* scales, bool 
                               int fmt, const float* gptr, bool bf16, void* out, cudaStream_t st);
 cudaError_t launch_ue5m3_to_e4m3(const uint8_t* in, int64_t n, int32_t* t_out, uint8_t* out, int32_t* status,
                                  cudaStream_t st);
+// UE5M3 scale codes -> up to three E4M3 windows (out: 3 arrays of n codes),
+// shifts t_out[3], windows in use n_out[1]
+cudaError_t launch_ue5m3_windows(const uint8_t* in, int64_t n, int32_t* t_out, int32_t* n_out, uint8_t* out,
+                                 int32_t* status, cudaStream_t st);
 cudaError_t launch_encode_scales(const float* s, int64_t n, int fmt, uint8_t* codes, float* decoded,
                                  cudaStream_t st);
 cudaError_t launch_philox_bits16(uint64_t seed, uint64_t start, int64_t n, uint16_t* out, cudaStream_t st);
@@ -65,6 +69,11 @@ struct GemmArgs {
   float* q_amax_out;  // nullable: max |bf16(C)|
   uint64_t q_seed;
   bool q_sr, q_mma;
+  // multi-pass GEMM over UE5M3 scale windows: add into C (float32 output),
+  // and skip the launch if window wa of A or wb of B is unused
+  bool accumulate;
+  const int32_t *wcount_a, *wcount_b;
+  int wa, wb;
 };
 cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t st);
 

@@ -341,6 +341,50 @@ __global__ void k_ue5m3_finalize(int32_t* t_inout) {
   *t_inout = ue5m3_shift_from_maxcode((uint32_t)*t_inout);
 }
 
+// UE5M3 scales wider than one E4M3 window: with e_max the largest exponent
+// (t_0 = e_max - 7), scale s with exponent e goes to window
+// w = (e_max - e) / 14 and is re-encoded as E4M3 of s * 2^-(t_0 - 14 w), which
+// is exact (e - t_w lies in -6..7 and s has at most 4 significant bits).
+// out holds UE5M3_WINDOWS arrays of n codes; other windows get code 0.
+constexpr int UE5M3_WINDOWS = 3;
+constexpr int UE5M3_WINDOW_BINADES = 14;
+
+__global__ void __launch_bounds__(256) k_ue5m3_windows(const uint8_t* __restrict__ s, int64_t n,
+                                                       const int32_t* maxcode, uint8_t* __restrict__ out,
+                                                       int32_t* wmax, int32_t* status) {
+  const int e_max = ue5m3_shift_from_maxcode((uint32_t)__ldg(maxcode)) + 7;
+  int top = 0;
+  bool bad = false;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+    const float v = ScaleFmt<SF_UE5M3>::decode(s[i]);
+    uint8_t c[UE5M3_WINDOWS] = {0, 0, 0};
+    if (v > 0.0f) {
+      const int e = (int)((__float_as_uint(v) >> 23) & 0xFFu) - 127;  // UE5M3 values are normal floats
+      const int w = (e_max - e) / UE5M3_WINDOW_BINADES;
+      const int t = e_max - 7 - UE5M3_WINDOW_BINADES * w;
+      const float u = __fmul_rn(v, __uint_as_float((uint32_t)(127 - t) << 23));  // exact
+      const uint32_t code = ScaleFmt<SF_E4M3>::encode(u);
+      bad |= w >= UE5M3_WINDOWS || ScaleFmt<SF_E4M3>::decode(code) != u;
+      if (w < UE5M3_WINDOWS) c[w] = (uint8_t)code;
+      top = max(top, w + 1);
+    }
+#pragma unroll
+    for (int k = 0; k < UE5M3_WINDOWS; ++k) out[k * n + i] = c[k];
+  }
+  top = __reduce_max_sync(0xFFFFFFFFu, top);
+  if ((threadIdx.x & 31) == 0 && top > 0) atomicMax(wmax, top);
+  if (__any_sync(0xFFFFFFFFu, bad) && (threadIdx.x & 31) == 0) set_status(status, FP4_ERR_UE5M3_RANGE);
+}
+
+// t_out[0] held the largest code; n_out the number of windows in use (0 for
+// an all-zero tensor)
+__global__ void k_ue5m3_windows_finalize(int32_t* t_out, int32_t* n_out) {
+  const int t0 = ue5m3_shift_from_maxcode((uint32_t)t_out[0]);
+#pragma unroll
+  for (int k = 0; k < UE5M3_WINDOWS; ++k) t_out[k] = t0 - UE5M3_WINDOW_BINADES * k;
+  *n_out = max(*n_out, 1);
+}
+
 // ---------------------------------------------------------------------------
 // Conformance helpers
 // ---------------------------------------------------------------------------
@@ -505,6 +549,21 @@ cudaError_t launch_ue5m3_to_e4m3(const uint8_t* in, int64_t n, int32_t* t_out, u
     k_ue5m3_reencode<<<(unsigned)blocks, 256, 0, st>>>(in, n, t_out, out, status);
   }
   k_ue5m3_finalize<<<1, 1, 0, st>>>(t_out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_ue5m3_windows(const uint8_t* in, int64_t n, int32_t* t_out, int32_t* n_out, uint8_t* out,
+                                 int32_t* status, cudaStream_t st) {
+  cudaError_t e = cudaMemsetAsync(t_out, 0, sizeof(int32_t), st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(n_out, 0, sizeof(int32_t), st);
+  if (e != cudaSuccess) return e;
+  if (n > 0) {
+    int64_t blocks = (n + 255) / 256;
+    if (blocks > 152 * 8) blocks = 152 * 8;
+    k_ue5m3_maxcode<<<(unsigned)blocks, 256, 0, st>>>(in, n, t_out);
+    k_ue5m3_windows<<<(unsigned)blocks, 256, 0, st>>>(in, n, t_out, out, n_out, status);
+  }
+  k_ue5m3_windows_finalize<<<1, 1, 0, st>>>(t_out, n_out);
   return cudaGetLastError();
 }
 

@@ -71,6 +71,9 @@ _SIGS = {
                         _VP, _VP]),
     "fp4_gemm_quantize": (_I32, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _I64, _I64, _I64, _I32, _I32, _VP, _I32,
                                  _U64, _I32, _VP, _VP, _VP, _VP, _VP]),
+    "fp4_ue5m3_windows": (_I32, [_VP, _I64, _VP, _VP, _VP, _VP, _VP]),
+    "fp4_gemm_ue5m3_windows": (_I32, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _I64, _I64, _I64, _VP, _I64,
+                                      _VP, _VP]),
     "fp4_gemv_w4a16": (_I32, [_VP, _VP, _VP, _VP, _I64, _I64, _I64, _I32, _VP, _VP, _VP]),
     "fp4_encode_scales": (_I32, [_VP, _I64, _I32, _VP, _VP, _VP]),
     "fp4_philox_bits16": (_I32, [_U64, _U64, _I64, _VP, _VP]),
@@ -205,6 +208,19 @@ def fp4_gemm_quantize(Aq, As, Bq, Bs, ga, gb, tA, tB, M, N, K, fmt, g_out, round
                                     M, N, K, _fmt(fmt), FP4_LAYOUT_TN, _ptr(g_out), int(rounding), int(seed),
                                     int(sf_layout), _ptr(C_codes), _ptr(C_scales), _ptr(C_amax_out),
                                     _ptr(dev_status), _stream(stream)), "fp4_gemm_quantize")
+
+
+def fp4_ue5m3_windows(scales, t_out, n_windows_out, out, dev_status=None, stream=None):
+    _check(_lib().fp4_ue5m3_windows(_ptr(scales), scales.numel(), _ptr(t_out), _ptr(n_windows_out), _ptr(out),
+                                    _ptr(dev_status), _stream(stream)), "fp4_ue5m3_windows")
+
+
+def fp4_gemm_ue5m3_windows(Aq, As_windows, tA, nA, Bq, Bs_windows, tB, nB, ga, gb, M, N, K, C, ldc=None,
+                           dev_status=None, stream=None):
+    _check(_lib().fp4_gemm_ue5m3_windows(_ptr(Aq), _ptr(As_windows), _ptr(tA), _ptr(nA), _ptr(Bq), _ptr(Bs_windows),
+                                         _ptr(tB), _ptr(nB), _ptr(ga), _ptr(gb), M, N, K, _ptr(C),
+                                         N if ldc is None else ldc, _ptr(dev_status), _stream(stream)),
+           "fp4_gemm_ue5m3_windows")
 
 
 def fp4_gemv_w4a16(Wq, Ws, gw, x, batch, N, K, out_dtype, y, dev_status=None, stream=None):

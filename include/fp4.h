@@ -221,6 +221,37 @@ fp4_status fp4_dequantize(const uint8_t* codes, const uint8_t* scales, fp4_sf_la
 fp4_status fp4_ue5m3_to_e4m3(const uint8_t* ue5m3_scales, int64_t n, int32_t* t_out,
                              uint8_t* e4m3_out, int32_t* dev_status, fp4_stream_t stream);
 
+/* UE5M3 scales wider than one E4M3 window (the same emulation, [UE5M3]
+ * "Ограничения").  With e(s) = floor(log2 s) for each nonzero scale value and
+ * e_max the largest: scale s belongs to window w = floor((e_max - e(s)) / 14)
+ * and becomes the E4M3 code of s * 2^-t_w, t_w = e_max - 7 - 14 w, which is
+ * always exact (e(s) - t_w lies in -6..7).  UE5M3 spans 2^-17 .. 1.75 * 2^16,
+ * so three windows suffice.  Writes, for n scale codes (any layout):
+ *   e4m3_out      3 arrays of n codes, window-major (code 0 where a scale
+ *                 belongs to another window), caller-owned device memory;
+ *   t_out         device int32[3], the shifts t_0, t_1, t_2;
+ *   n_windows_out device int32[1], the windows in use (1 if all scales are 0).
+ * Window 0 equals fp4_ue5m3_to_e4m3's output whenever that one is exact. */
+fp4_status fp4_ue5m3_windows(const uint8_t* ue5m3_scales, int64_t n, int32_t* t_out,
+                             int32_t* n_windows_out, uint8_t* e4m3_out, int32_t* dev_status,
+                             fp4_stream_t stream);
+
+/* UE5M3 GEMM over windowed scales: C = sum over window pairs (wa, wb) of the
+ * fp4_gemm (f = UE5M3, float32 out) of A with window wa's scales and B with
+ * window wb's, shifted by tA[wa], tB[wb].  Pair (0, 0) stores C; every other
+ * pair adds its result into C (TMA reduce-add) or, when wa >= *nA or
+ * wb >= *nB (device counts from fp4_ue5m3_windows), exits at once, so the host
+ * never reads the counts.  Nine launches on the stream.  As_windows /
+ * Bs_windows: fp4_ue5m3_windows outputs for A's and B's MMA-layout scales
+ * (3 x M*K/16 and 3 x N*K/16 bytes).  C is float32 [M, N], ldc elements; the
+ * sum of passes adds one float32 rounding per pass in use.  Shape and
+ * alignment rules as fp4_gemm. */
+fp4_status fp4_gemm_ue5m3_windows(const uint8_t* Aq, const uint8_t* As_windows, const int32_t* tA,
+                                  const int32_t* nA, const uint8_t* Bq, const uint8_t* Bs_windows,
+                                  const int32_t* tB, const int32_t* nB, const float* ga,
+                                  const float* gb, int64_t M, int64_t N, int64_t K, float* C,
+                                  int64_t ldc, int32_t* dev_status, fp4_stream_t stream);
+
 /* Block-scaled FP4 GEMM (forward, dgrad and wgrad are all this call in TN form),
  * float32 accumulation on tcgen05 tensor cores:
  *   C[m, n] = alpha * sum_k (qa[m,k] * sa[m, k/G]) * (qb[n,k] * sb[n, k/G]),

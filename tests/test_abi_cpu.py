@@ -117,6 +117,17 @@ def test_gemv_and_misc_argument_errors():
     assert lib.fp4_amax(P, 4, 16, 16, None, None) == fp4.FP4_ERR_INVALID_ARG
     assert lib.fp4_dequantize(P, P, 0, 4, 24, 0, P, 0, P, None) == fp4.FP4_ERR_SHAPE
     assert lib.fp4_ue5m3_to_e4m3(P, 16, None, P, None, None) == fp4.FP4_ERR_INVALID_ARG
+    assert lib.fp4_ue5m3_windows(P, 16, P, None, P, None, None) == fp4.FP4_ERR_INVALID_ARG
+    assert lib.fp4_ue5m3_windows(P, -1, P, P, P, None, None) == fp4.FP4_ERR_SHAPE
+    w = lambda M=256, N=256, K=256, A=P, C=P, ldc=256, nA=P: lib.fp4_gemm_ue5m3_windows(
+        A, P, P, nA, P, P, P, P, P, P, M, N, K, C, ldc, None, None)
+    assert w(nA=None) == fp4.FP4_ERR_INVALID_ARG
+    assert w(C=None) == fp4.FP4_ERR_INVALID_ARG
+    assert w(M=100) == fp4.FP4_ERR_SHAPE
+    assert w(N=128) == fp4.FP4_ERR_SHAPE
+    assert w(ldc=100) == fp4.FP4_ERR_SHAPE
+    assert w(A=P + 1) == fp4.FP4_ERR_ALIGNMENT
+    assert w(ldc=258) == fp4.FP4_ERR_ALIGNMENT           # 1032-byte float32 rows
     assert lib.fp4_encode_scales(P, 4, 11, P, P, None) == fp4.FP4_ERR_INVALID_ARG
     assert lib.fp4_philox_bits16(1, 0, -1, P, None) == fp4.FP4_ERR_SHAPE
     # empty tensors are valid no-ops
