@@ -61,7 +61,7 @@ NCU_TRAFFIC = {"gemm": {"bytes": 291.0e6, "src": "7caa10f11717ccc4",
                         "files": ["gemm_sm103.cu", "async_sm103.cuh", "fp4_device.cuh"]},
                "quant_dual": {"bytes": 758.0e6, "src": "4e39ab39f16f087e",
                               "files": ["quantize.cu", "fp4_device.cuh"]},
-               "gemv": {"bytes": 25.45e6, "src": "17b46c52569c69be",
+               "gemv": {"bytes": 25.45e6, "src": "5cd08efd4b2ec796",
                         "files": ["gemv.cu", "async_sm103.cuh", "fp4_device.cuh"]}}
 
 

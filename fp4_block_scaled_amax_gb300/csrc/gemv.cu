@@ -505,8 +505,8 @@ cudaError_t launch_tma_t(const fp4lib::GemvArgs& a, int T, cudaStream_t st) {
 }
 
 // Returns cudaErrorNotSupported (before launching anything) when the shape or
-// the driver rules the TMA-fed form out.  Four warps per tile (512-column
-// stages) up to six tiles per CTA, two beyond.
+// the tensor-map encoder rules the TMA-fed form out.  Four warps per tile
+// (512-column stages) up to six tiles per CTA, two beyond.
 cudaError_t launch_gemv_tma(const fp4lib::GemvArgs& a, cudaStream_t st) {
   if (a.batch > 8 || a.K % 256 != 0 || a.N > (int64_t)1 << 30 || a.K > (int64_t)1 << 30)
     return cudaErrorNotSupported;
