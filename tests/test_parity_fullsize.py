@@ -187,3 +187,41 @@ def test_config5_fullsize(wname):
         got = host(y.float())
         bound = Gm.gemm_bound(S) + np.abs(yr) * 2.0 ** -8
         assert (np.abs(got - yr) <= bound).all(), (wname, b)
+
+
+# ---------------------------------------------------------------------------
+# 16 x 16 random Hadamard transform on the dual quantizer at full size
+# ---------------------------------------------------------------------------
+
+def test_dual_rht_fullsize_sampled(step):
+    from oracle import rht as R
+    from gpu_util import host
+    bench, d, s = step
+    fp4 = s.fp4
+    mask = bench.RHT_MASK
+    x = d["dY"]
+    M, K = x.shape
+    cr, srs, cc, scs = (torch.empty_like(t) for t in s.q["dY"])
+    amax = torch.zeros(2, dtype=torch.float32, device=s.dY.device)
+    st = torch.zeros(1, dtype=torch.int32, device=s.dY.device)
+    SR = fp4.FP4_ROUND_STOCHASTIC
+    fp4.fp4_quantize_dual_rht(s.dY, "E4M3", SR, 1234, SR, 1235, mask, None, None, fp4.FP4_SFLAYOUT_MMA,
+                              cr, srs, cc, scs, amax[0:1], amax[1:2], st)
+    a = host(amax)
+    assert int(host(st)[0]) == 0
+    xf = x.float().numpy()
+    rows_t = R.rht16(xf, mask)                 # blocks along K
+    g_row = np.float32(np.max(np.abs(rows_t)))
+    assert a[0] == g_row
+    cols_t = R.rht16(np.ascontiguousarray(xf.T), mask)  # blocks along M, one row per column of dY
+    del xf
+    g_col = np.float32(np.max(np.abs(cols_t)))
+    assert a[1] == g_col
+    cr, srs, cc, scs = host(cr), host(srs), host(cc), host(scs)
+    srow, scol = from_mma(srs, M, K // 16), from_mma(scs, K, M // 16)
+    for r in _rows(M, 8, 6):
+        codes, scales = Q.quantize_rows(rows_t[r:r + 1], "E4M3", "sr", 1234, g_row, row0=int(r))
+        assert np.array_equal(cr[r], codes[0]) and np.array_equal(srow[r], scales[0]), ("row", r)
+    for c in _rows(K, 8, 7):
+        codes, scales = Q.quantize_rows(cols_t[c:c + 1], "E4M3", "sr", 1235, g_col, row0=int(c))
+        assert np.array_equal(cc[c], codes[0]) and np.array_equal(scol[c], scales[0]), ("col", c)
