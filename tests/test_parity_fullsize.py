@@ -225,3 +225,63 @@ def test_dual_rht_fullsize_sampled(step):
     for c in _rows(K, 8, 7):
         codes, scales = Q.quantize_rows(cols_t[c:c + 1], "E4M3", "sr", 1235, g_col, row0=int(c))
         assert np.array_equal(cc[c], codes[0]) and np.array_equal(scol[c], scales[0]), ("col", c)
+
+
+# ---------------------------------------------------------------------------
+# Quantizing epilogue and UE5M3 windows at the forward GEMM's full size
+# ---------------------------------------------------------------------------
+
+def test_gemm_quantize_epilogue_fullsize_identical(step):
+    # fp4_gemm_quantize == fp4_gemm (bf16 Y) followed by fp4_quantize of Y's rows,
+    # byte for byte, with Y's stored amax (RNE and SR)
+    bench, d, s = step
+    fp4 = s.fp4
+    M, N, K = bench.M_TOK, bench.N_FFN, bench.K_HID
+    qX, qW = s.q["X"], s.q["W"]
+    aX, aW = s.amax[0:1], s.amax[1:2]
+    dev = s.Y.device
+    Y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    fp4.fp4_gemm(qX[0], qX[1], qW[0], qW[1], aX, aW, None, None, M, N, K, "E4M3", fp4.FP4_OUT_BF16, Y)
+    gY = Y.float().abs().max().reshape(1)
+    for rnd, seed in ((fp4.FP4_ROUND_RNE, 0), (fp4.FP4_ROUND_STOCHASTIC, 77)):
+        c1, s1 = torch.empty((M, N // 2), dtype=torch.uint8, device=dev), torch.empty(M * N // 16, dtype=torch.uint8,
+                                                                                     device=dev)
+        c2, s2 = torch.empty_like(c1), torch.empty_like(s1)
+        fp4.fp4_quantize(Y, "E4M3", rnd, seed, gY, False, fp4.FP4_SFLAYOUT_MMA, c1, s1, None)
+        st = torch.zeros(1, dtype=torch.int32, device=dev)
+        fp4.fp4_gemm_quantize(qX[0], qX[1], qW[0], qW[1], aX, aW, None, None, M, N, K, "E4M3", gY, rnd, seed,
+                              fp4.FP4_SFLAYOUT_MMA, c2, s2, dev_status=st)
+        torch.cuda.synchronize()
+        assert int(st.item()) == 0
+        assert torch.equal(c1, c2) and torch.equal(s1, s2), rnd
+
+
+def test_ue5m3_windows_fullsize_one_window_identical(step):
+    # X and W quantized with UE5M3 scales (fresh amaxes) fit one window: the window
+    # GEMM equals the single-shift GEMM bit for bit at 16384 x 11008 x 4096
+    bench, d, s = step
+    fp4 = s.fp4
+    M, N, K = bench.M_TOK, bench.N_FFN, bench.K_HID
+    dev = s.Y.device
+    i32 = dict(dtype=torch.int32, device=dev)
+    ops = []
+    for x, a in ((s.X, s.amax[0:1]), (s.W, s.amax[1:2])):
+        R = x.shape[0]
+        codes = torch.empty((R, K // 2), dtype=torch.uint8, device=dev)
+        sc = torch.empty(R * K // 16, dtype=torch.uint8, device=dev)
+        fp4.fp4_quantize(x, "UE5M3", fp4.FP4_ROUND_RNE, 0, a, False, fp4.FP4_SFLAYOUT_MMA, codes, sc, None)
+        t, e4 = torch.zeros(1, **i32), torch.empty_like(sc)
+        fp4.fp4_ue5m3_to_e4m3(sc, t, e4)
+        tw, nw, win = torch.zeros(3, **i32), torch.zeros(1, **i32), torch.empty(3 * sc.numel(), dtype=torch.uint8,
+                                                                             device=dev)
+        fp4.fp4_ue5m3_windows(sc, tw, nw, win)
+        ops.append((codes, a, t, e4, tw, nw, win))
+    (xc, xa, xt, xe, xtw, xn, xw), (wc, wa, wt, we, wtw, wn, ww) = ops
+    C1 = torch.empty((M, N), dtype=torch.float32, device=dev)
+    C2 = torch.full((M, N), float("nan"), dtype=torch.float32, device=dev)
+    fp4.fp4_gemm(xc, xe, wc, we, xa, wa, xt, wt, M, N, K, "UE5M3", fp4.FP4_OUT_F32, C1)
+    st = torch.zeros(1, **i32)
+    fp4.fp4_gemm_ue5m3_windows(xc, xw, xtw, xn, wc, ww, wtw, wn, xa, wa, M, N, K, C2, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0 and int(xn.item()) == 1 and int(wn.item()) == 1
+    assert torch.equal(C1, C2)
