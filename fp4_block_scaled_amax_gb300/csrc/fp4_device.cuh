@@ -264,17 +264,22 @@ __device__ __forceinline__ uint32_t e2m1x2_rne(float lo, float hi) {
 //    (or lies in (-1, 0], whose ceiling is 0 either way);
 //  * ceil of t in (-1, 2^22) is (t + 1.5*2^23 rounded up) - 1.5*2^23, both
 //    steps exact; larger t (and +Inf) only ever saturate.
-// The value ceil(.) * 2^(k-1) is a grid value, or 8 and above, which the
+// All of it runs scaled by the step s = 2^(k-1) (exact for these magnitudes):
+// t*s = |y| - rho*s in one fma, then (t*s + 1.5*2^23*s rounded up) -
+// 1.5*2^23*s = ceil(t)*s, the grid value itself, so only the sign remains to
+// be attached.  The value is a grid value, or 8 and above, which the
 // saturating E2M1 conversion maps to 6.  A zero result keeps the sign of x.
-// rbits is the float32 pattern of 1 + r * 2^-16 (0x3F800000 | r << 7).
+// rbits is the float32 pattern of 1 + r * 2^-23 (0x3F800000 | r), so
+// rho * s = (rbits - 1) * 2^(k+6).
 __device__ __forceinline__ float e2m1_sr_value(float x, float r, uint32_t rbits) {
   const float ay = __fmul_rn(fabsf(x), r);
   const uint32_t eb = min(max(__float_as_uint(ay) & 0x7F800000u, 0x3F800000u), 0x40800000u);  // 2^k
-  const float m = __uint_as_float(0x7F800000u - eb);                                              // 2^(1-k)
-  const float rho = __fsub_rn(__uint_as_float(rbits), 1.0f);
-  const float t = __fmaf_rn(ay, m, -rho);
-  const float c = __fsub_rn(__fadd_ru(t, 12582912.0f), 12582912.0f);
-  return __fmul_rn(c, __uint_as_float((eb - 0x00800000u) | (__float_as_uint(x) & 0x80000000u)));
+  const float s7 = __uint_as_float(eb + (6u << 23));                                           // 2^(k+6)
+  const float rho = __fsub_rn(__uint_as_float(rbits), 1.0f);                                   // r * 2^-23
+  const float t = __fmaf_rn(-rho, s7, ay);
+  const float cs = __fmul_rn(s7, 98304.0f);                                                    // 1.5*2^23*s
+  const float c = __fsub_rn(__fadd_ru(t, cs), cs);
+  return __uint_as_float(__float_as_uint(c) | (__float_as_uint(x) & 0x80000000u));
 }
 // INT4 grid (integers -7..7, two's-complement nibble): nearest with ties to
 // even after clamping to [-7, 7]; adding 1.5 * 2^23 rounds to an integer in
@@ -289,16 +294,17 @@ __device__ __forceinline__ uint32_t int4_rne(float y) {
 // ulp(z) >= 2^-21 > ulp(n)/2, and below 1 it is exact.  -0 becomes code 0.
 __device__ __forceinline__ uint32_t int4_sr(float x, float r, uint32_t rbits) {
   const float ay = fminf(__fmul_rn(fabsf(x), r), 7.0f);
-  const float rho = __fsub_rn(__uint_as_float(rbits), 1.0f);
-  const float t = __fsub_rn(ay, rho);
+  const float rho = __fsub_rn(__uint_as_float(rbits), 1.0f);  // r * 2^-23
+  const float t = __fmaf_rn(-rho, 128.0f, ay);                 // ay - r * 2^-16, one rounding
   const float c = __fsub_rn(__fadd_ru(t, 12582912.0f), 12582912.0f);
   const float v = __uint_as_float(__float_as_uint(c) | (__float_as_uint(x) & 0x80000000u));
   return (__float_as_uint(__fadd_rn(v, 12582912.0f)) - 0x4B400000u) & 0xFu;
 }
 
-// 1 + r * 2^-16 for the low and high 16-bit halves of a Philox word.
-__device__ __forceinline__ uint32_t sr_rbits_lo(uint32_t w) { return 0x3F800000u | ((w << 7) & 0x007FFF80u); }
-__device__ __forceinline__ uint32_t sr_rbits_hi(uint32_t w) { return 0x3F800000u | ((w >> 9) & 0x007FFF80u); }
+// 1 + r * 2^-23 (float32 bits 0x3F800000 | r) for the low and high 16-bit
+// halves r of a Philox word: one byte permute each.
+__device__ __forceinline__ uint32_t sr_rbits_lo(uint32_t w) { return __byte_perm(w, 0x3F800000u, 0x7610u); }
+__device__ __forceinline__ uint32_t sr_rbits_hi(uint32_t w) { return __byte_perm(w, 0x3F800000u, 0x7632u); }
 
 // ---------------------------------------------------------------------------
 // Philox4x32-10 (Salmon, Moraes, Dror, Shaw, SC'11): 10 rounds of
