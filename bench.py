@@ -57,11 +57,11 @@ FP4_PER_BF16 = 6.0  # nominal dense FP4 / bf16 tensor ratio on GB300 (13.5 / 2.2
 # gemm: mean over the fwd, dgrad and wgrad launches; quant_dual: the step's
 # three dual quantizations together; gemv: one launch.  Writes still held in
 # L2 when a kernel ends do not appear in its DRAM bytes.
-NCU_TRAFFIC = {"gemm": {"bytes": 291.0e6, "src": "7caa10f11717ccc4",
+NCU_TRAFFIC = {"gemm": {"bytes": 291.3e6, "src": "dd8052b50d94f2a0",
                         "files": ["gemm_sm103.cu", "async_sm103.cuh", "fp4_device.cuh"]},
-               "quant_dual": {"bytes": 758.0e6, "src": "4e39ab39f16f087e",
+               "quant_dual": {"bytes": 754.9e6, "src": "dffdbb1504ea6a3a",
                               "files": ["quantize.cu", "fp4_device.cuh"]},
-               "gemv": {"bytes": 25.45e6, "src": "5cd08efd4b2ec796",
+               "gemv": {"bytes": 25.5e6, "src": "5f703ac380737906",
                         "files": ["gemv.cu", "async_sm103.cuh", "fp4_device.cuh"]}}
 
 
