@@ -59,10 +59,13 @@ __global__ void __launch_bounds__(256) k_amax(const uint16_t* __restrict__ x, in
     const int64_t r = c / per_row;
     return x + r * ldx + (c - r * per_row) * 8;
   };
-  for (; i + 7 * stride < total; i += 8 * stride) {
+  // eight independent 16-byte loads in flight per thread, the last round
+  // guarded, so the tail costs one memory latency rather than one per chunk
+  for (; i < total; i += 8 * stride) {
     uint4 v[8];
 #pragma unroll
-    for (int u = 0; u < 8; ++u) v[u] = ld_stream(addr(i + u * stride));
+    for (int u = 0; u < 8; ++u)
+      v[u] = i + u * stride < total ? ld_stream(addr(i + u * stride)) : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
       m = absmax2(m, v[u].x & 0x7FFF7FFFu);
@@ -70,13 +73,6 @@ __global__ void __launch_bounds__(256) k_amax(const uint16_t* __restrict__ x, in
       m = absmax2(m, v[u].z & 0x7FFF7FFFu);
       m = absmax2(m, v[u].w & 0x7FFF7FFFu);
     }
-  }
-  for (; i < total; i += stride) {
-    const uint4 v = ld_stream(addr(i));
-    m = absmax2(m, v.x & 0x7FFF7FFFu);
-    m = absmax2(m, v.y & 0x7FFF7FFFu);
-    m = absmax2(m, v.z & 0x7FFF7FFFu);
-    m = absmax2(m, v.w & 0x7FFF7FFFu);
   }
   float a = fmaxf(bf16_lo(m), bf16_hi(m));
   unsigned int ab = __reduce_max_sync(0xFFFFFFFFu, __float_as_uint(a));
