@@ -589,6 +589,54 @@ def ue5m3_windows_study(step, flush, reps=3):
     return res
 
 
+def gemv_graph_study(step, reps=5, launches=64, copies=8):
+    """Weight-only GEMV as a decode loop would issue it: `launches` launches
+    back to back over `copies` copies of the 11008 x 4096 NVFP4 weight
+    (8 x 25.6 MB > L2, so each launch streams its weights from HBM), issued
+    one by one on the stream against replayed from one captured CUDA graph.
+    Per-launch time, outside the timed step."""
+    fp4 = step.fp4
+    N, K = N_FFN, K_HID
+    dev = step.Y.device
+    BF = fp4.FP4_OUT_BF16
+    ws = [(step.Wg_codes, step.Wg_scales, step.Wg_amax)]
+    for _ in range(copies - 1):
+        ws.append((step.Wg_codes.clone(), step.Wg_scales.clone(), step.Wg_amax.clone()))
+    y = torch.empty((GEMV_BATCH, N), dtype=torch.bfloat16, device=dev)
+
+    def loop():
+        for i in range(launches):
+            c, sc, a = ws[i % copies]
+            fp4.fp4_gemv_w4a16(c, sc, a, step.xg, GEMV_BATCH, N, K, BF, y)
+
+    loop()
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(graph, stream=side):
+            loop()
+    torch.cuda.current_stream().wait_stream(side)
+    st = torch.cuda.current_stream()
+    res = {"gemv": f"batch {GEMV_BATCH}, {N}x{K}, {launches} launches over {copies} weight copies", "unit": "us/launch"}
+    gv_bytes = N * K * (0.5 + 1 / 16) + 2 * GEMV_BATCH * (N + K)
+    for name, fn in (("stream", loop), ("cuda_graph", graph.replay)):
+        fn()
+        ts = []
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(st)
+            fn()
+            e1.record(st)
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1) * 1e3 / launches)
+        us = statistics.median(ts)
+        res[name] = {"us": round(us, 2), "GB/s": round(gv_bytes / us / 1e3, 1)}
+    del graph
+    return res
+
+
 def fused_epilogue_study(step, flush, reps=5):
     """The forward GEMM Y = X W^T with Y quantized for the next layer (NVFP4,
     RNE rows, the stored amax of Y): the GEMM writing bf16 Y followed by the
@@ -705,8 +753,9 @@ def run_ours(args, rank, world, local):
     qtraffic_v = traffic_of("quant_dual")
     gvtraffic_v = traffic_of("gemv")
 
-    qmodes = sweep = hadamard = fused_ep = variants = windows = None
+    qmodes = sweep = hadamard = fused_ep = variants = windows = gv_graph = None
     if not args.no_studies:
+        gv_graph = gemv_graph_study(step)
         variants = step_variants_study(step, flush)
         windows = ue5m3_windows_study(step, flush)
         qmodes = quantizer_modes(step, flush)
@@ -748,6 +797,7 @@ def run_ours(args, rank, world, local):
         "fused_epilogue_quantize": fused_ep,
         "step_variants": variants,
         "ue5m3_windows": windows,
+        "gemv_decode_loop": gv_graph,
         "amax_gbs": round(a_gbs, 1),
         "gemv_w4a16": {"batch": GEMV_BATCH, "N": N_FFN, "K": K_HID, "us": round(statistics.mean(gemv_ms) * 1e3, 2),
                        "GB/s": round(gv_gbs, 1), "frac": round(gv_gbs / hbm, 4), "traffic": gvtraffic_v},
