@@ -637,6 +637,40 @@ def gemv_graph_study(step, reps=5, launches=64, copies=8):
     return res
 
 
+def step_graph_study(step, flush, reps=5):
+    """The timed step (10 launches) replayed from one captured CUDA graph
+    against the same step launched one kernel at a time, each timed with
+    CUDA events after an L2 flush.  Outside the timed step."""
+    st = torch.cuda.current_stream()
+    step.run()
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream()
+    side.wait_stream(st)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(graph, stream=side):
+            step.run()
+    st.wait_stream(side)
+    res = {"step": "the timed step: 3 amax, 3 dual quantizations, 3 GEMMs, GEMV", "unit": "ms"}
+    for name, fn in (("eager", step.run), ("cuda_graph", graph.replay)):
+        fn()
+        ts = []
+        for _ in range(reps):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(st)
+            fn()
+            e1.record(st)
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        ms = statistics.median(ts)
+        res[name] = {"ms": round(ms, 4), "TFLOP/s": round(STEP_FLOPS / (ms * 1e-3) / 1e12, 1)}
+    torch.cuda.synchronize()
+    assert int(step.status.item()) == 0
+    del graph
+    return res
+
+
 def fused_epilogue_study(step, flush, reps=5):
     """The forward GEMM Y = X W^T with Y quantized for the next layer (NVFP4,
     RNE rows, the stored amax of Y): the GEMM writing bf16 Y followed by the
@@ -753,8 +787,9 @@ def run_ours(args, rank, world, local):
     qtraffic_v = traffic_of("quant_dual")
     gvtraffic_v = traffic_of("gemv")
 
-    qmodes = sweep = hadamard = fused_ep = variants = windows = gv_graph = None
+    qmodes = sweep = hadamard = fused_ep = variants = windows = gv_graph = step_graph = None
     if not args.no_studies:
+        step_graph = step_graph_study(step, flush)
         gv_graph = gemv_graph_study(step)
         variants = step_variants_study(step, flush)
         windows = ue5m3_windows_study(step, flush)
@@ -798,6 +833,7 @@ def run_ours(args, rank, world, local):
         "step_variants": variants,
         "ue5m3_windows": windows,
         "gemv_decode_loop": gv_graph,
+        "step_cuda_graph": step_graph,
         "amax_gbs": round(a_gbs, 1),
         "gemv_w4a16": {"batch": GEMV_BATCH, "N": N_FFN, "K": K_HID, "us": round(statistics.mean(gemv_ms) * 1e3, 2),
                        "GB/s": round(gv_gbs, 1), "frac": round(gv_gbs / hbm, 4), "traffic": gvtraffic_v},
