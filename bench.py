@@ -61,7 +61,7 @@ NCU_TRAFFIC = {"gemm": {"bytes": 291.5e6, "src": "dd8052b50d94f2a0",
                         "files": ["gemm_sm103.cu", "async_sm103.cuh", "fp4_device.cuh"]},
                "quant_dual": {"bytes": 751.9e6, "src": "ee5a8ae16859e27f",
                               "files": ["quantize.cu", "fp4_device.cuh"]},
-               "gemv": {"bytes": 25.5e6, "src": "5f703ac380737906",
+               "gemv": {"bytes": 25.45e6, "src": "6e6c84997c1e2aac",
                         "files": ["gemv.cu", "async_sm103.cuh", "fp4_device.cuh"]}}
 
 
@@ -671,6 +671,57 @@ def step_graph_study(step, flush, reps=5):
     return res
 
 
+def gemv_shapes_study(step, reps=5, launches=32):
+    """The weight-only GEMV on the Qwen2.5-7B-like MLP shapes, W_up 18944 x
+    3584 and W_down 3584 x 18944 (NVFP4, quantized once), at batch 1, 8 and
+    64: per-launch time over `launches` back-to-back launches that rotate over
+    enough weight copies to exceed L2 (each launch streams its weights from
+    HBM).  Batch <= 8 runs the shared-memory (TMA) form, batch 64 the
+    register-fed one.  Outside the timed step."""
+    from fp4_block_scaled_amax_gb300 import synth
+    fp4 = step.fp4
+    dev = step.Y.device
+    BF, RNE, PLAIN = fp4.FP4_OUT_BF16, fp4.FP4_ROUND_RNE, fp4.FP4_SFLAYOUT_PLAIN
+    st = torch.cuda.current_stream()
+    res = {"unit": "us/launch"}
+    for wname, xname in (("W_up", "x_up"), ("W_down", "x_down")):
+        W = synth.config5(1)[wname].to(dev)
+        N, K = W.shape
+        codes = torch.empty((N, K // 2), dtype=torch.uint8, device=dev)
+        scales = torch.empty(N * K // 16, dtype=torch.uint8, device=dev)
+        amax = torch.zeros(1, dtype=torch.float32, device=dev)
+        fp4.fp4_quantize(W, "E4M3", RNE, 0, None, False, PLAIN, codes, scales, amax)
+        del W
+        wbytes = N * K * (0.5 + 1 / 16)
+        copies = max(2, int(300e6 // wbytes) + 1)
+        ws = [(codes, scales)] + [(codes.clone(), scales.clone()) for _ in range(copies - 1)]
+        out = {}
+        for b in (1, 8, 64):
+            x = synth.config5(b)[xname].to(dev)
+            y = torch.empty((b, N), dtype=torch.bfloat16, device=dev)
+
+            def loop():
+                for i in range(launches):
+                    c, sc = ws[i % copies]
+                    fp4.fp4_gemv_w4a16(c, sc, amax, x, b, N, K, BF, y)
+
+            loop()
+            ts = []
+            for _ in range(reps):
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(st)
+                loop()
+                e1.record(st)
+                torch.cuda.synchronize()
+                ts.append(e0.elapsed_time(e1) * 1e3 / launches)
+            us = statistics.median(ts)
+            gbs = (wbytes + 2 * b * (N + K)) / us / 1e3
+            out[f"batch_{b}"] = {"us": round(us, 2), "GB/s": round(gbs, 1)}
+        res[f"{wname} {N}x{K}"] = out
+        del ws
+    return res
+
+
 def fused_epilogue_study(step, flush, reps=5):
     """The forward GEMM Y = X W^T with Y quantized for the next layer (NVFP4,
     RNE rows, the stored amax of Y): the GEMM writing bf16 Y followed by the
@@ -787,8 +838,9 @@ def run_ours(args, rank, world, local):
     qtraffic_v = traffic_of("quant_dual")
     gvtraffic_v = traffic_of("gemv")
 
-    qmodes = sweep = hadamard = fused_ep = variants = windows = gv_graph = step_graph = None
+    qmodes = sweep = hadamard = fused_ep = variants = windows = gv_graph = step_graph = gv_shapes = None
     if not args.no_studies:
+        gv_shapes = gemv_shapes_study(step)
         step_graph = step_graph_study(step, flush)
         gv_graph = gemv_graph_study(step)
         variants = step_variants_study(step, flush)
@@ -833,6 +885,7 @@ def run_ours(args, rank, world, local):
         "step_variants": variants,
         "ue5m3_windows": windows,
         "gemv_decode_loop": gv_graph,
+        "gemv_qwen_mlp_shapes": gv_shapes,
         "step_cuda_graph": step_graph,
         "amax_gbs": round(a_gbs, 1),
         "gemv_w4a16": {"batch": GEMV_BATCH, "N": N_FFN, "K": K_HID, "us": round(statistics.mean(gemv_ms) * 1e3, 2),

@@ -12,10 +12,10 @@
 // them with the bf16 activations on the tensor cores (mma.sync m16n8k16,
 // float32 accumulation).  The batch is the MMA's N dimension (8 per tile).
 //
-// Two forms.  Decode batches (batch <= 8, K % 256 == 0) take the TMA-fed
-// kernel further down: weights, scales and activations stream through a
-// shared-memory ring and are shared by all warps of a CTA.  Larger batches
-// and other K take the register-fed kernel right below.
+// Two forms.  K % 256 == 0 (any batch up to 64) takes the TMA-fed kernel
+// further down: weights, scales and activations stream through a shared-memory
+// ring and are shared by all warps of a CTA.  Other K take the register-fed
+// kernel right below.
 //
 // Register-fed form.  k permutation: inside a 128-wide k chunk, lane q of a quad (q = lane % 4)
 // supplies at MMA step s the fragment positions {2q, 2q+1, 2q+8, 2q+9} from
@@ -217,7 +217,7 @@ __global__ void __launch_bounds__(NT <= 2 ? 512 : 256) k_gemv_w4a16(const uint8_
 
 
 // ---------------------------------------------------------------------------
-// TMA-fed form: batch <= 8 and K % 256 == 0
+// TMA-fed form: K % 256 == 0, batch up to 64 (NT tiles of 8 rows)
 // ---------------------------------------------------------------------------
 // One CTA per group of T 16-row tiles (T chosen so the groups cover the SMs
 // in about one wave).  Warp 0 streams stages of SC = 128 * WPT columns into a
@@ -244,16 +244,19 @@ __global__ void __launch_bounds__(NT <= 2 ? 512 : 256) k_gemv_w4a16(const uint8_
 constexpr int TV_MAX_TILES = 8;  // 16-row tiles per CTA
 constexpr int TV_MAX_STAGES = 32;
 constexpr int TV_RING_BUDGET = 200 * 1024;
+constexpr int TV_SMEM_MAX = 227 * 1024;  // dynamic shared memory per CTA on sm_103a
 
-template <int WPT>
+// WPT consumer warps per 16-row tile; NT batch tiles of 8 rows (the MMA's N)
+template <int WPT, int NT>
 struct TvLayout {
   static constexpr int SC = 128 * WPT;     // columns per stage
   static constexpr int SB = SC / 16;       // scale bytes per row per stage
   static constexpr int CODE_BOXES = SC / 256;
-  static constexpr int X_BOXES = SC / 64;
+  static constexpr int X_BOXES = SC / 64;  // 64-column activation boxes of 8 * NT rows
+  static constexpr uint32_t X_BOX_BYTES = 1024u * NT;
   __host__ __device__ static constexpr uint32_t code_box_bytes(int T) { return 2048u * T; }
   __host__ __device__ static constexpr uint32_t code_bytes(int T) { return CODE_BOXES * code_box_bytes(T); }
-  __host__ __device__ static constexpr uint32_t x_bytes() { return 1024u * X_BOXES; }
+  __host__ __device__ static constexpr uint32_t x_bytes() { return X_BOX_BYTES * X_BOXES; }
   __host__ __device__ static constexpr uint32_t stage_bytes(int T) {
     return code_bytes(T) + x_bytes() + ((16u * SB * T + 1023u) & ~1023u);
   }
@@ -322,13 +325,14 @@ __device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity) {
   }
 }
 
-template <int WPT>
-__global__ void __launch_bounds__(32 * (1 + 4 * 6))
+template <int WPT, int NT>
+__global__ void __launch_bounds__(NT == 1 ? 32 * (1 + 4 * 6) : 32 * (1 + 2 * 8))
     k_gemv_w4a16_tma(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant__ CUtensorMap tm_scales,
                      const __grid_constant__ CUtensorMap tm_x, const float* __restrict__ gw, int batch, int N, int nk,
                      int T, int S, bool bf16_out, void* __restrict__ y, int32_t* status) {
   using namespace fp4async;
-  using L = TvLayout<WPT>;
+  using L = TvLayout<WPT, NT>;
+  constexpr int BW = 8 * NT;  // batch columns per tile
   extern __shared__ uint8_t smem_raw[];
   __shared__ int abort_flag;
   const uint32_t raw = smem_u32(smem_raw);
@@ -338,8 +342,8 @@ __global__ void __launch_bounds__(32 * (1 + 4 * 6))
   const uint32_t code_bytes = L::code_bytes(T);
   const uint32_t code_box = L::code_box_bytes(T);
   const int nwarps = WPT * T;
-  float* const red = reinterpret_cast<float*>(base_ptr + S * stage_bytes);  // [WPT*T][16][8]
-  const uint32_t bars = base + S * stage_bytes + (uint32_t)nwarps * 16 * 8 * 4;  // full[S], empty[S]
+  float* const red = reinterpret_cast<float*>(base_ptr + S * stage_bytes);  // [WPT*T][16][BW]
+  const uint32_t bars = base + S * stage_bytes + (uint32_t)nwarps * 16 * BW * 4;  // full[S], empty[S]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n0 = blockIdx.x * 16 * T;
 
@@ -370,7 +374,8 @@ __global__ void __launch_bounds__(32 * (1 + 4 * 6))
         for (int i = 0; i < L::CODE_BOXES; ++i)
           tma_load_2d(st + code_box * i, &tm_codes, full, it * (L::SC / 2) + 128 * i, n0);
 #pragma unroll
-        for (int i = 0; i < L::X_BOXES; ++i) tma_load_2d(st + code_bytes + 1024u * i, &tm_x, full, it * L::SC + 64 * i, 0);
+        for (int i = 0; i < L::X_BOXES; ++i)
+          tma_load_2d(st + code_bytes + L::X_BOX_BYTES * i, &tm_x, full, it * L::SC + 64 * i, 0);
         tma_load_2d(st + code_bytes + L::x_bytes(), &tm_scales, full, it * L::SB, n0);
         issued = it + 1;
         if (++s == S) {
@@ -392,11 +397,15 @@ __global__ void __launch_bounds__(32 * (1 + 4 * 6))
     for (int s = 0; s < 4; ++s) {
       const int w = (s + q) & 3;
       code_off[s] = (uint32_t)(j >> 3) * code_box + rowA * 128u + ((uint32_t)((j & 7) ^ g) << 4) + 4u * w;
-      x_off[s] = code_bytes + (uint32_t)(j >> 1) * 1024u + g * 128u + ((uint32_t)((4 * (j & 1) + w) ^ g) << 4);
+      x_off[s] = code_bytes + (uint32_t)(j >> 1) * L::X_BOX_BYTES + g * 128u + ((uint32_t)((4 * (j & 1) + w) ^ g) << 4);
       upper[s] = (w >> 1) != 0;
     }
     const uint32_t sc_off = code_bytes + L::x_bytes() + rowA * L::SB + 2u * j;
+    // NT == 1: two accumulator chains (even and odd MMAs); NT > 1: one chain per batch tile
     float acc0[4] = {0.f, 0.f, 0.f, 0.f}, acc1[4] = {0.f, 0.f, 0.f, 0.f};
+    float acc[NT][4];
+#pragma unroll
+    for (int t8 = 0; t8 < NT; ++t8) acc[t8][0] = acc[t8][1] = acc[t8][2] = acc[t8][3] = 0.f;
     for (int it = 0, s = 0, ph = 0; it < nk; ++it) {
       if (!wait_warp(bars + 8 * s, ph, &abort_flag, status)) break;
       const uint8_t* st = base_ptr + s * stage_bytes;
@@ -407,7 +416,6 @@ __global__ void __launch_bounds__(32 * (1 + 4 * 6))
       for (int k = 0; k < 4; ++k) {
         const uint32_t va = *reinterpret_cast<const uint32_t*>(st + code_off[k]);
         const uint32_t vb = *reinterpret_cast<const uint32_t*>(st + code_off[k] + 8 * 128);
-        const uint4 xv = *reinterpret_cast<const uint4*>(st + x_off[k]);
         uint32_t ra[4], rb[4];
         e2m1x8_pairs(va, ra);
         e2m1x8_pairs(vb, rb);
@@ -417,8 +425,21 @@ __global__ void __launch_bounds__(32 * (1 + 4 * 6))
           ra[i] = mul_bf16x2(ra[i], sA);
           rb[i] = mul_bf16x2(rb[i], sB);
         }
-        mma_bf16_16816_pure(acc0, ra[0], rb[0], ra[1], rb[1], prmt(xv.x, xv.z, 0x5410u), prmt(xv.x, xv.z, 0x7632u));
-        mma_bf16_16816_pure(acc1, ra[2], rb[2], ra[3], rb[3], prmt(xv.y, xv.w, 0x5410u), prmt(xv.y, xv.w, 0x7632u));
+        if constexpr (NT == 1) {
+          const uint4 xv = *reinterpret_cast<const uint4*>(st + x_off[k]);
+          mma_bf16_16816_pure(acc0, ra[0], rb[0], ra[1], rb[1], prmt(xv.x, xv.z, 0x5410u), prmt(xv.x, xv.z, 0x7632u));
+          mma_bf16_16816_pure(acc1, ra[2], rb[2], ra[3], rb[3], prmt(xv.y, xv.w, 0x5410u), prmt(xv.y, xv.w, 0x7632u));
+        } else {
+          // batch tile t8 is activation rows 8*t8 + g: 8 rows (1 KB) further into the box
+#pragma unroll
+          for (int t8 = 0; t8 < NT; ++t8) {
+            const uint4 xv = *reinterpret_cast<const uint4*>(st + x_off[k] + 1024u * t8);
+            mma_bf16_16816_pure(acc[t8], ra[0], rb[0], ra[1], rb[1], prmt(xv.x, xv.z, 0x5410u),
+                                prmt(xv.x, xv.z, 0x7632u));
+            mma_bf16_16816_pure(acc[t8], ra[2], rb[2], ra[3], rb[3], prmt(xv.y, xv.w, 0x5410u),
+                                prmt(xv.y, xv.w, 0x7632u));
+          }
+        }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(bars + 8 * (S + s));
@@ -427,24 +448,34 @@ __global__ void __launch_bounds__(32 * (1 + 4 * 6))
         ph ^= 1;
       }
     }
-    float* rw = red + (size_t)cw * 16 * 8;
-    rw[g * 8 + 2 * q] = acc0[0] + acc1[0];
-    rw[g * 8 + 2 * q + 1] = acc0[1] + acc1[1];
-    rw[(g + 8) * 8 + 2 * q] = acc0[2] + acc1[2];
-    rw[(g + 8) * 8 + 2 * q + 1] = acc0[3] + acc1[3];
+    float* rw = red + (size_t)cw * 16 * BW;
+    if constexpr (NT == 1) {
+      rw[g * 8 + 2 * q] = acc0[0] + acc1[0];
+      rw[g * 8 + 2 * q + 1] = acc0[1] + acc1[1];
+      rw[(g + 8) * 8 + 2 * q] = acc0[2] + acc1[2];
+      rw[(g + 8) * 8 + 2 * q + 1] = acc0[3] + acc1[3];
+    } else {
+#pragma unroll
+      for (int t8 = 0; t8 < NT; ++t8) {
+        rw[g * BW + 8 * t8 + 2 * q] = acc[t8][0];
+        rw[g * BW + 8 * t8 + 2 * q + 1] = acc[t8][1];
+        rw[(g + 8) * BW + 8 * t8 + 2 * q] = acc[t8][2];
+        rw[(g + 8) * BW + 8 * t8 + 2 * q + 1] = acc[t8][3];
+      }
+    }
   }
   __syncthreads();
   const float s_enc = fp4dev::global_encode_scale<fp4dev::SF_E4M3>(__ldg(gw), nullptr);
   const int rows = 16 * T;
-  for (int i = threadIdx.x; i < rows * 8; i += blockDim.x) {
+  for (int i = threadIdx.x; i < rows * BW; i += blockDim.x) {
     const int b = i / rows, r = i % rows;
     const int n = n0 + r;
     if (n >= N || b >= batch) continue;
     const int t = r >> 4, rr = r & 15;
-    const float* p = red + ((size_t)(WPT * t) * 16 + rr) * 8 + b;
+    const float* p = red + ((size_t)(WPT * t) * 16 + rr) * BW + b;
     float v = 0.0f;
 #pragma unroll
-    for (int k = 0; k < WPT; ++k) v = __fadd_rn(v, p[k * 16 * 8]);
+    for (int k = 0; k < WPT; ++k) v = __fadd_rn(v, p[k * 16 * BW]);
     v = __fdiv_rn(__fmul_rn(v, 256.0f), s_enc);
     if (bf16_out) static_cast<__nv_bfloat16*>(y)[(int64_t)b * N + n] = __float2bfloat16_rn(v);
     else static_cast<float*>(y)[(int64_t)b * N + n] = v;
@@ -475,31 +506,37 @@ int sm_count() {
   return n;
 }
 
-template <int WPT>
+template <int WPT, int NT>
 cudaError_t launch_tma_t(const fp4lib::GemvArgs& a, int T, cudaStream_t st) {
-  using L = TvLayout<WPT>;
+  using L = TvLayout<WPT, NT>;
   const int64_t tiles = (a.N + 15) / 16;
   const int64_t ctas = (tiles + T - 1) / T;
   const int nk = (int)((a.K + L::SC - 1) / L::SC);
-  int S = (int)(TV_RING_BUDGET / L::stage_bytes(T));
+  const size_t red_bytes = (size_t)WPT * T * 16 * 8 * NT * 4;
+  // batch <= 8: a 200 KB ring; larger batches: what fits beside the reduction buffer
+  const size_t budget =
+      NT == 1 ? (size_t)TV_RING_BUDGET : (size_t)TV_SMEM_MAX - 1024 - red_bytes - 16 * TV_MAX_STAGES;
+  int S = (int)(budget / L::stage_bytes(T));
   if (S > TV_MAX_STAGES) S = TV_MAX_STAGES;
   if (S > nk) S = nk;
-  const size_t smem = 1024 + (size_t)S * L::stage_bytes(T) + (size_t)WPT * T * 16 * 8 * 4 + 16u * S;
+  if (S < 1) return cudaErrorNotSupported;
+  const size_t smem = 1024 + (size_t)S * L::stage_bytes(T) + red_bytes + 16u * S;
   CUtensorMap mc, ms, mx;
   if (!make_map(&mc, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.Wq, a.K / 2, a.N, a.K / 2, 128, 16 * T,
                 CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B) ||
       !make_map(&ms, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.Ws, a.K / 16, a.N, a.K / 16, L::SB, 16 * T,
                 CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE) ||
-      !make_map(&mx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.x, a.K, a.batch, a.K * 2, 64, 8,
+      !make_map(&mx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.x, a.K, a.batch, a.K * 2, 64, 8 * NT,
                 CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B))
     return cudaErrorNotSupported;
   static size_t smem_set = 0;
   if (smem > smem_set) {
-    cudaError_t e = cudaFuncSetAttribute(k_gemv_w4a16_tma<WPT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e =
+        cudaFuncSetAttribute(k_gemv_w4a16_tma<WPT, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     smem_set = smem;
   }
-  k_gemv_w4a16_tma<WPT><<<(unsigned)ctas, 32 * (1 + WPT * T), smem, st>>>(mc, ms, mx, a.gw, (int)a.batch, (int)a.N, nk,
+  k_gemv_w4a16_tma<WPT, NT><<<(unsigned)ctas, 32 * (1 + WPT * T), smem, st>>>(mc, ms, mx, a.gw, (int)a.batch, (int)a.N, nk,
                                                                          T, S, a.bf16_out, a.y, a.status);
   return cudaGetLastError();
 }
@@ -508,13 +545,16 @@ cudaError_t launch_tma_t(const fp4lib::GemvArgs& a, int T, cudaStream_t st) {
 // the tensor-map encoder rules the TMA-fed form out.  Four warps per tile
 // (512-column stages) up to six tiles per CTA, two beyond.
 cudaError_t launch_gemv_tma(const fp4lib::GemvArgs& a, cudaStream_t st) {
-  if (a.batch > 8 || a.K % 256 != 0 || a.N > (int64_t)1 << 30 || a.K > (int64_t)1 << 30)
+  if (a.batch > 64 || a.K % 256 != 0 || a.N > (int64_t)1 << 30 || a.K > (int64_t)1 << 30)
     return cudaErrorNotSupported;
   const int64_t tiles = (a.N + 15) / 16;
   const int sms = sm_count();
   int T = (int)((tiles + sms - 1) / sms);
   T = T < 1 ? 1 : (T > TV_MAX_TILES ? TV_MAX_TILES : T);
-  return T <= 6 ? launch_tma_t<4>(a, T, st) : launch_tma_t<2>(a, T, st);
+  // eight batch tiles of 8 rows: 512-column stages (four warps per tile) when a CTA holds few tiles,
+  // 256-column stages (two warps per tile) otherwise
+  if (a.batch > 8) return T <= 3 ? launch_tma_t<4, 8>(a, T, st) : launch_tma_t<2, 8>(a, T, st);
+  return T <= 6 ? launch_tma_t<4, 1>(a, T, st) : launch_tma_t<2, 1>(a, T, st);
 }
 
 }  // namespace

@@ -293,8 +293,8 @@ fp4_status fp4_gemm_quantize(const uint8_t* Aq, const uint8_t* As, const uint8_t
  * deq(W) = e2m1 * s_b / s_enc(*gw) (E4M3 scales, G = 16, FP4_SFLAYOUT_PLAIN),
  * x bf16 [batch, K] (row stride K), float32 accumulation, y [batch, N] float32
  * or bf16 (row stride N).  Requirements: 1 <= batch <= 64, N > 0, K % 32 == 0,
- * pointers 16-byte aligned.  batch <= 8 with K % 256 == 0 streams W through
- * shared memory with TMA; its waits are bounded and a wait that expires
+ * pointers 16-byte aligned.  K % 256 == 0 streams W through shared memory
+ * with TMA (any batch up to 64); its waits are bounded and a wait that expires
  * records FP4_ERR_TIMEOUT in *dev_status (optional int32 device word, first
  * error wins). */
 fp4_status fp4_gemv_w4a16(const uint8_t* Wq, const uint8_t* Ws, const float* gw,
