@@ -73,6 +73,8 @@ def parse():
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--studies", default="all",
+                   help="comma-separated side studies to run (default: all), e.g. formats,stack")
     p.add_argument("--no-studies", action="store_true",
                    help="skip the side measurements after the timed steps (for ncu launch lists)")
     p.add_argument("--tokens", type=int, default=16384,
@@ -280,6 +282,169 @@ class LinearStep:
         mark(10)
 
 
+# ---------------------------------------------------------------------------
+# Nemotron-H-8B-like linear stack with UE5M3 scales (the UE5M3 recipe)
+# ---------------------------------------------------------------------------
+C4_M, C4_H, C4_F = 32768, 4096, 21504
+C4_STEPS, C4_PERIOD = 100, 50
+C4_NAMES = ("X", "W1", "H", "W2", "dY", "dH")
+
+
+class StackStep:
+    """One training step of the two-linear stack H = X W1^T, Y = H W2^T with
+    UE5M3 block scales ("UE5M3 FP4 Block Scaling ..." blog, "Что сделали"):
+    every tensor keeps a stored global amax refreshed every 50 steps (fresh
+    amax passes on refresh steps only), forward operands nearest-rounded,
+    the gradients dY and dH stochastically rounded (Philox seeds
+    1234 + 8 t + role, roles 0/1 dY rows/columns, 2/3 dH rows/columns), each
+    tensor quantized once in both layouts; the UE5M3 scales reach the E4M3
+    tensor-core path by the per-tensor shift the quantizer reports and one
+    re-encode pass; six FP4 GEMMs with bf16 outputs:
+      L1 fwd   H   = X W1^T     M x F x H      L2 fwd   Y   = H W2^T     M x H x F
+      L2 dgrad dH  = dY W2      M x F x H      L2 wgrad dW2 = dY^T H     H x F x M
+      L1 dgrad dX  = dH W1      M x H x F      L1 wgrad dW1 = dH^T X     F x H x M
+    """
+
+    def __init__(self, device, M=C4_M, Hd=C4_H, F=C4_F, weights=None):
+        from fp4_block_scaled_amax_gb300 import fp4, synth
+        self.fp4 = fp4
+        self.dev = device
+        self.M, self.Hd, self.F = M, Hd, F
+        u8 = dict(dtype=torch.uint8, device=device)
+        bf = dict(dtype=torch.bfloat16, device=device)
+        if weights is None:
+            scale = C4_M // M
+            weights = synth.config4_weights(scale)
+        self.W1 = weights["W1"].to(device)
+        self.W2 = weights["W2"].to(device)
+        self.H = torch.empty((M, F), **bf)
+        self.dH = torch.empty((M, F), **bf)
+        self.Y = torch.empty((M, Hd), **bf)
+        self.dX = torch.empty((M, Hd), **bf)
+        self.dW2 = torch.empty((Hd, F), **bf)
+        self.dW1 = torch.empty((F, Hd), **bf)
+        shapes = {"X": (M, Hd), "W1": (F, Hd), "H": (M, F), "W2": (Hd, F), "dY": (M, Hd), "dH": (M, F)}
+        # per tensor: row codes, row scales (UE5M3, tiled), transposed codes and
+        # scales, their E4M3 re-encodes, and the two shifts
+        self.q = {}
+        for n, (R, C) in shapes.items():
+            self.q[n] = {"cr": torch.empty((R, C // 2), **u8), "sr": torch.empty(R * C // 16, **u8),
+                         "cc": torch.empty((C, R // 2), **u8), "sc": torch.empty(R * C // 16, **u8),
+                         "er": torch.empty(R * C // 16, **u8), "ec": torch.empty(R * C // 16, **u8),
+                         "t": torch.zeros(2, dtype=torch.int32, device=device)}
+        self.stored = torch.zeros(len(C4_NAMES), dtype=torch.float32, device=device)  # stored amaxes
+        self.current = torch.zeros(len(C4_NAMES), dtype=torch.float32, device=device)  # max|x| by-products
+        self.status = torch.zeros(1, dtype=torch.int32, device=device)
+        self.flops = 6 * 2 * M * Hd * F
+
+    def _g(self, name):
+        j = C4_NAMES.index(name)
+        return self.stored[j:j + 1], self.current[j:j + 1]
+
+    def _quant(self, name, x, refresh, r_row, seed_row, r_col, seed_col):
+        fp4 = self.fp4
+        q = self.q[name]
+        g, cur = self._g(name)
+        if refresh:
+            fp4.fp4_amax(x, g)  # the refresh: this step's max |x| becomes the stored amax
+        fp4.fp4_quantize_dual(x, "UE5M3", r_row, seed_row, r_col, seed_col, g, fp4.FP4_SFLAYOUT_MMA, q["cr"], q["sr"],
+                              q["cc"], q["sc"], None if refresh else cur, self.status, ue5m3_shift_out=q["t"])
+        fp4.fp4_ue5m3_reencode(q["sr"], q["t"][0:1], q["er"], self.status)
+        fp4.fp4_ue5m3_reencode(q["sc"], q["t"][1:2], q["ec"], self.status)
+
+    def _gemm(self, a, a_col, b, b_col, M, N, K, out):
+        fp4 = self.fp4
+        qa, qb = self.q[a], self.q[b]
+        ga, gb = self._g(a)[0], self._g(b)[0]
+        ca, ea, ta = (qa["cc"], qa["ec"], qa["t"][1:2]) if a_col else (qa["cr"], qa["er"], qa["t"][0:1])
+        cb, eb, tb = (qb["cc"], qb["ec"], qb["t"][1:2]) if b_col else (qb["cr"], qb["er"], qb["t"][0:1])
+        fp4.fp4_gemm(ca, ea, cb, eb, ga, gb, ta, tb, M, N, K, "UE5M3", fp4.FP4_OUT_BF16, out, dev_status=self.status)
+
+    def run(self, t, X, dY, ev=None):
+        """Step t on inputs X [M, H], dY [M, H]; ev: optional list of 13 CUDA
+        events (quantization and GEMM phases alternate)."""
+        fp4 = self.fp4
+        RNE, SR = fp4.FP4_ROUND_RNE, fp4.FP4_ROUND_STOCHASTIC
+        M, Hd, F = self.M, self.Hd, self.F
+        refresh = t % C4_PERIOD == 0
+        seed = 1234 + 8 * t
+        st = torch.cuda.current_stream()
+
+        def mark(i):
+            if ev is not None:
+                ev[i].record(st)
+
+        mark(0)
+        self._quant("X", X, refresh, RNE, 0, RNE, 0)
+        self._quant("W1", self.W1, refresh, RNE, 0, RNE, 0)
+        mark(1)
+        self._gemm("X", False, "W1", False, M, F, Hd, self.H)                 # L1 fwd
+        mark(2)
+        self._quant("H", self.H, refresh, RNE, 0, RNE, 0)
+        self._quant("W2", self.W2, refresh, RNE, 0, RNE, 0)
+        mark(3)
+        self._gemm("H", False, "W2", False, M, Hd, F, self.Y)                 # L2 fwd
+        mark(4)
+        self._quant("dY", dY, refresh, SR, seed + 0, SR, seed + 1)
+        mark(5)
+        self._gemm("dY", False, "W2", True, M, F, Hd, self.dH)                # L2 dgrad
+        mark(6)
+        self._gemm("dY", True, "H", True, Hd, F, M, self.dW2)                 # L2 wgrad
+        mark(7)
+        self._quant("dH", self.dH, refresh, SR, seed + 2, SR, seed + 3)
+        mark(8)
+        self._gemm("dH", False, "W1", True, M, Hd, F, self.dX)                # L1 dgrad
+        mark(9)
+        self._gemm("dH", True, "X", True, F, Hd, M, self.dW1)                 # L1 wgrad
+        mark(10)
+
+    def launches(self, refresh):
+        # 6 x (dual quantizer + shift finalize + 2 re-encodes) + 6 GEMMs (+ 6 amax on refresh steps)
+        return 6 * 4 + 6 + (6 if refresh else 0)
+
+
+def stack_study(device, reps=3):
+    """The UE5M3 stack at full size: per step (a refresh step and a stale one,
+    each timed alone after an L2 flush) and the whole 100-step sequence with
+    refreshes at t = 0 and 50 (inputs drawn on the device between steps,
+    outside the events; every step's kernels inside)."""
+    from fp4_block_scaled_amax_gb300 import synth
+    s = StackStep(device)
+    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=device)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(11)]
+    per_phase = {"quant": 0.0, "gemm": 0.0}
+    step_ms = []
+    seq_ms = []
+    for t in range(C4_STEPS):
+        d = synth.config4_step_device(t, device)
+        flush.zero_()
+        torch.cuda.synchronize()
+        s.run(t, d["X"], d["dY"], ev)
+        torch.cuda.synchronize()
+        ms = ev[0].elapsed_time(ev[10])
+        seq_ms.append(ms)
+        if t in (1, 2, 3):  # stale steps: the breakdown of the usual step
+            step_ms.append(ms)
+            for i in range(10):
+                per_phase["gemm" if i in (1, 3, 5, 6, 8, 9) else "quant"] += ev[i].elapsed_time(ev[i + 1])
+    if int(s.status.item()) != 0:
+        raise RuntimeError(f"stack: device status {int(s.status.item())}")
+    stale = statistics.median(seq_ms[1:C4_PERIOD])
+    refresh = statistics.mean([seq_ms[0], seq_ms[C4_PERIOD]])
+    total = sum(seq_ms)
+    gemm_ms = per_phase["gemm"] / len(step_ms)
+    return {"workload": f"nemotron-h-8b-like stack {C4_M} tokens x {C4_H} -> {C4_F} -> {C4_H}, UE5M3 g16, "
+                        "fwd RNE, dY/dH SR, amax refreshed at t % 50 == 0",
+            "unit": "ms", "step_refresh_ms": round(refresh, 4), "step_stale_ms": round(stale, 4),
+            "step_stale_tflops": round(s.flops / (stale * 1e-3) / 1e12, 1),
+            "gemm_ms_per_step": round(gemm_ms, 4),
+            "gemm_tflops": round(s.flops / (gemm_ms * 1e-3) / 1e12, 1),
+            "quant_reencode_amax_ms_per_step": round(per_phase["quant"] / len(step_ms), 4),
+            "sequence_100_steps_ms": round(total, 2),
+            "sequence_tflops": round(C4_STEPS * s.flops / (total * 1e-3) / 1e12, 1),
+            "launches_per_step": {"refresh": s.launches(True), "stale": s.launches(False)}}
+
+
 def quantizer_modes(step, flush, reps=5):
     """Given-amax quantizer of dY (the step's largest tensor) in each mode, timed
     alone with CUDA events after an L2 flush: row or transposed layout at
@@ -358,6 +523,188 @@ def scale_format_sweep(fp4, flush, device, reps=5):
         rel_rmse = float((deq - xf).pow(2).mean().sqrt()) / ref_norm
         out[f] = {"us": round(us, 2), "achieved": round(gbs, 1), "frac": round(gbs / hbm, 4),
                   "rel_rmse": round(rel_rmse, 5)}
+    return out
+
+
+def _time_ms(fn, flush, reps):
+    """Median of reps CUDA-event timings of fn(), each after an L2 flush."""
+    st = torch.cuda.current_stream()
+    fn()
+    ts = []
+    for _ in range(reps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(st)
+        fn()
+        e1.record(st)
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1))
+    return statistics.median(ts)
+
+
+def _ue5m3_operand(fp4, x, sr, seed, device):
+    """Dual UE5M3 quantization of x with the shifts and E4M3 re-encodes the
+    GEMM takes: ((row codes, row E4M3 scales, t_row), (col codes, col scales,
+    t_col), amax)."""
+    R, C = x.shape
+    u8 = dict(dtype=torch.uint8, device=device)
+    cr, srs, cc, scs = (torch.empty((R, C // 2), **u8), torch.empty(R * C // 16, **u8),
+                        torch.empty((C, R // 2), **u8), torch.empty(R * C // 16, **u8))
+    er, ec = torch.empty_like(srs), torch.empty_like(scs)
+    t = torch.zeros(2, dtype=torch.int32, device=device)
+    g = torch.zeros(1, dtype=torch.float32, device=device)
+    rnd = fp4.FP4_ROUND_STOCHASTIC if sr else fp4.FP4_ROUND_RNE
+    fp4.fp4_quantize_dual(x, "UE5M3", rnd, seed, rnd, seed + 1, None, fp4.FP4_SFLAYOUT_MMA, cr, srs, cc, scs, g,
+                          ue5m3_shift_out=t)
+    fp4.fp4_ue5m3_reencode(srs, t[0:1], er)
+    fp4.fp4_ue5m3_reencode(scs, t[1:2], ec)
+    return (cr, er, t[0:1]), (cc, ec, t[1:2]), g
+
+
+def formats_7b_study(step, flush, reps=5):
+    """Forward, dgrad and wgrad FP4 GEMMs of the 7B step (bf16 out) in each
+    tensor-core scale format: NVFP4 (E4M3, group 16, scale_vec::4X), UE5M3
+    (group 16, shifted onto the E4M3 path) and MXFP4 (E8M0, group 32,
+    scale_vec::2X); operands quantized by the library once, outside the
+    events."""
+    fp4 = step.fp4
+    dev = step.dev
+    M, K, N = M_TOK, K_HID, N_FFN
+    RNE, SR, MMA = fp4.FP4_ROUND_RNE, fp4.FP4_ROUND_STOCHASTIC, fp4.FP4_SFLAYOUT_MMA
+    out = {"shapes": {"fwd": [M, N, K], "dgrad": [M, K, N], "wgrad": [N, K, M]}, "unit": "ms", "out": "bf16"}
+    C = {"fwd": step.Y, "dgrad": step.dX, "wgrad": step.dW}
+    for fmt in ("E4M3", "UE5M3", "E8M0"):
+        if fmt == "UE5M3":
+            xr, xc, gx = _ue5m3_operand(fp4, step.X, False, 0, dev)
+            wr, wc, gw = _ue5m3_operand(fp4, step.W, False, 0, dev)
+            dr, dc, gd = _ue5m3_operand(fp4, step.dY, True, 1234, dev)
+        else:
+            G = 32 if fmt == "E8M0" else 16
+            ops = []
+            for x, sr in ((step.X, False), (step.W, False), (step.dY, True)):
+                R, Cc = x.shape
+                cr = torch.empty((R, Cc // 2), dtype=torch.uint8, device=dev)
+                srs = torch.empty(R * Cc // G, dtype=torch.uint8, device=dev)
+                cc = torch.empty((Cc, R // 2), dtype=torch.uint8, device=dev)
+                scs = torch.empty(R * Cc // G, dtype=torch.uint8, device=dev)
+                g = torch.zeros(1, dtype=torch.float32, device=dev)
+                rnd = SR if sr else RNE
+                fp4.fp4_quantize_dual(x, fmt, rnd, 1234, rnd, 1235, None, MMA, cr, srs, cc, scs, g)
+                ops.append(((cr, srs, None), (cc, scs, None), g))
+            (xr, xc, gx), (wr, wc, gw), (dr, dc, gd) = ops
+        calls = {"fwd": (xr, gx, wr, gw, M, N, K), "dgrad": (dr, gd, wc, gw, M, K, N),
+                 "wgrad": (dc, gd, xc, gx, N, K, M)}
+        res = {}
+        for name, (a, ga, b, gb, m, n, k) in calls.items():
+            def run(a=a, ga=ga, b=b, gb=gb, m=m, n=n, k=k, c=C[name]):
+                fp4.fp4_gemm(a[0], a[1], b[0], b[1], ga, gb, a[2], b[2], m, n, k, fmt, fp4.FP4_OUT_BF16, c,
+                             dev_status=step.status)
+            ms = _time_ms(run, flush, reps)
+            res[name] = {"ms": round(ms, 4), "tflops": round(2 * m * n * k / (ms * 1e-3) / 1e12, 1)}
+        res["mean_tflops"] = round(statistics.mean(v["tflops"] for v in res.values()), 1)
+        out[fmt] = res
+    torch.cuda.synchronize()
+    if int(step.status.item()) != 0:
+        raise RuntimeError(f"formats_7b: device status {int(step.status.item())}")
+    return out
+
+
+def cublaslt_nvfp4_study(step, flush, reps=5):
+    """cuBLASLt's NVFP4 GEMM (torch._scaled_mm on the library's own E4M3
+    codes and tiled scales, the blocked layout cuBLASLt reads; bf16 out,
+    without the per-tensor alpha) on the step's three shapes, timed like the
+    library's kernel: the vendor GEMM beside ours, outside the timed step."""
+    fp4_dt = getattr(torch, "float4_e2m1fn_x2", None)
+    if fp4_dt is None or not hasattr(torch, "_scaled_mm"):
+        return {"unavailable": "this torch has no float4_e2m1fn_x2 / _scaled_mm"}
+    M, K, N = M_TOK, K_HID, N_FFN
+    qX, qW, qd = step.q["X"], step.q["W"], step.q["dY"]
+    e4 = torch.float8_e4m3fn
+    calls = {"fwd": (qX[0], qX[1], qW[0], qW[1], M, N, K), "dgrad": (qd[0], qd[1], qW[2], qW[3], M, K, N),
+             "wgrad": (qd[2], qd[3], qX[2], qX[3], N, K, M)}
+    out = {"unit": "ms", "out": "bf16", "api": "torch._scaled_mm (NVFP4, 1x16 E4M3 block scales)"}
+    try:
+        for name, (a, sa, b, sb, m, n, k) in calls.items():
+            A = a.view(fp4_dt)
+            B = b.view(fp4_dt).t()
+            SA = sa.view(e4).reshape(m, k // 16)
+            SB = sb.view(e4).reshape(n, k // 16)
+            ms = _time_ms(lambda: torch._scaled_mm(A, B, SA, SB, out_dtype=torch.bfloat16), flush, reps)
+            out[name] = {"ms": round(ms, 4), "tflops": round(2 * m * n * k / (ms * 1e-3) / 1e12, 1)}
+        out["mean_tflops"] = round(statistics.mean(out[n]["tflops"] for n in calls), 1)
+    except Exception as exc:  # noqa: BLE001 - reported, not fatal
+        out["unavailable"] = f"{type(exc).__name__}: {str(exc).splitlines()[0][:200]}"
+    return out
+
+
+def config2_study(fp4, flush, device, reps=5):
+    """The 350M-parameter MLP linear Y = X W^T, 8192 x 4096 x 1024, with X's
+    per-channel sigma log-uniform in [0.1, 10]: the forward FP4 GEMM (bf16
+    out) in E4M3, UE5M3 and E8M0; and the range study of the review of Intel's
+    FP4 paper ("Форматы FP4": only E1M6, the narrowest scale format, fails):
+    per format the fraction of nonzero blocks whose scale flushes to zero or
+    saturates, along rows (the forward operand) and along columns (the wgrad
+    operand X^T), and the relative Frobenius error of the product of the
+    dequantized operands (X_q W_q^T against X W^T, float64 on 512 sampled
+    rows; E1M6 has no tensor-core path, so its product uses the library's
+    codes dequantized by the library)."""
+    from fp4_block_scaled_amax_gb300 import synth
+    d = synth.config2()
+    X, W = d["X"].to(device), d["W"].to(device)
+    M, K = X.shape
+    N = W.shape[0]
+    MMA = fp4.FP4_SFLAYOUT_MMA
+    out = {"shape": [M, N, K], "unit": "ms", "out": "bf16"}
+    Y = torch.empty((M, N), dtype=torch.bfloat16, device=device)
+    rows = torch.arange(0, M, M // 512, device=device)
+    ref = (X[rows].double() @ W.double().t())
+    ref_norm = float(ref.norm())
+    for fmt in ("E4M3", "UE5M3", "E8M0", "E1M6"):
+        G = 32 if fmt == "E8M0" else 16
+        res = {}
+        ops = []
+        for x in (X, W):
+            R, C = x.shape
+            cr = torch.empty((R, C // 2), dtype=torch.uint8, device=device)
+            srs = torch.empty(R * C // G, dtype=torch.uint8, device=device)
+            cc = torch.empty((C, R // 2), dtype=torch.uint8, device=device)
+            scs = torch.empty(R * C // G, dtype=torch.uint8, device=device)
+            g = torch.zeros(1, dtype=torch.float32, device=device)
+            t = torch.zeros(2, dtype=torch.int32, device=device) if fmt == "UE5M3" else None
+            fp4.fp4_quantize_dual(x, fmt, fp4.FP4_ROUND_RNE, 0, fp4.FP4_ROUND_RNE, 0, None, MMA, cr, srs, cc, scs, g,
+                                  ue5m3_shift_out=t)
+            ops.append((cr, srs, cc, scs, g, t))
+        # blocks of X holding a nonzero element whose scale code is 0 (E4M3, UE5M3, E1M6: the
+        # scale and every element flush to zero; E8M0 has no zero, code 0 is 2^-127), along rows
+        # and along columns
+        (cr, srs, cc, scs, g, _), _ = ops
+        for tag, scales, R, C in (("rows", srs, M, K), ("cols", scs, K, M)):
+            sc = scales.view(R // 128, (C // G) // 4, 32, 4, 4).permute(0, 3, 2, 1, 4).reshape(-1)  # tiled -> plain
+            xr = X if tag == "rows" else X.t()
+            blk_nz = xr.reshape(R, C // G, G).ne(0).any(dim=2).reshape(-1)
+            res[f"flushed_{tag}"] = round(float((blk_nz & (sc == 0)).sum()) / float(blk_nz.sum()), 6)
+        # error of the product of the dequantized operands
+        dq = []
+        for (cr, srs, cc, scs, g, t), x in zip(ops, (X, W)):
+            R, C = x.shape
+            o = torch.empty((R, C), dtype=torch.float32, device=device)
+            fp4.fp4_dequantize(cr, srs, MMA, R, C, fmt, g, fp4.FP4_OUT_F32, o)
+            dq.append(o)
+        prod = dq[0][rows].double() @ dq[1].double().t()
+        res["product_rel_err"] = round(float((prod - ref).norm()) / ref_norm, 6)
+        if fmt != "E1M6":
+            (ac, as_, _, _, ga, ta), (bc, bs, _, _, gb, tb) = ops
+            if fmt == "UE5M3":
+                ea, eb = torch.empty_like(as_), torch.empty_like(bs)
+                fp4.fp4_ue5m3_reencode(as_, ta[0:1], ea)
+                fp4.fp4_ue5m3_reencode(bs, tb[0:1], eb)
+                as_, bs, ta, tb = ea, eb, ta[0:1], tb[0:1]
+            ms = _time_ms(lambda: fp4.fp4_gemm(ac, as_, bc, bs, ga, gb, ta, tb, M, N, K, fmt, fp4.FP4_OUT_BF16, Y),
+                          flush, reps)
+            res["gemm_ms"] = round(ms, 4)
+            res["gemm_tflops"] = round(2 * M * N * K / (ms * 1e-3) / 1e12, 1)
+            res["gemm_rel_err"] = round(float((Y[rows].double() - prod).norm()) / float(prod.norm()), 6)
+        out[fmt] = res
     return out
 
 
@@ -781,6 +1128,10 @@ def src_hash(names):
     return h.hexdigest()[:16]
 
 
+STUDIES = ("formats", "cublaslt", "config2", "stack", "gemv_shapes", "step_graph", "gemv_graph", "variants",
+           "windows", "qmodes", "sweep", "hadamard", "fused")
+
+
 def run_ours(args, rank, world, local):
     from fp4_block_scaled_amax_gb300 import build as b
     if rank == 0:
@@ -839,15 +1190,37 @@ def run_ours(args, rank, world, local):
     gvtraffic_v = traffic_of("gemv")
 
     qmodes = sweep = hadamard = fused_ep = variants = windows = gv_graph = step_graph = gv_shapes = None
-    if not args.no_studies:
+    formats = cublas = cfg2 = stack = None
+    chosen = set() if args.no_studies else (
+        set(STUDIES) if args.studies == "all" else set(x.strip() for x in args.studies.split(",")))
+    unknown = chosen - set(STUDIES)
+    if unknown:
+        raise SystemExit(f"unknown studies {sorted(unknown)}; known: {', '.join(STUDIES)}")
+    if "formats" in chosen:
+        formats = formats_7b_study(step, flush)
+    if "cublaslt" in chosen:
+        cublas = cublaslt_nvfp4_study(step, flush)
+    if "config2" in chosen:
+        cfg2 = config2_study(step.fp4, flush, device)
+    if "stack" in chosen and M_TOK == 16384:
+        stack = stack_study(device)
+    if "gemv_shapes" in chosen:
         gv_shapes = gemv_shapes_study(step)
+    if "step_graph" in chosen:
         step_graph = step_graph_study(step, flush)
+    if "gemv_graph" in chosen:
         gv_graph = gemv_graph_study(step)
+    if "variants" in chosen:
         variants = step_variants_study(step, flush)
+    if "windows" in chosen:
         windows = ue5m3_windows_study(step, flush)
+    if "qmodes" in chosen:
         qmodes = quantizer_modes(step, flush)
+    if "sweep" in chosen:
         sweep = scale_format_sweep(step.fp4, flush, device)
+    if "hadamard" in chosen:
         hadamard = hadamard_study(step, step.fp4, flush, device)
+    if "fused" in chosen:
         fused_ep = fused_epilogue_study(step, flush)
     e2e = None
     if not args.no_e2e:
@@ -879,6 +1252,10 @@ def run_ours(args, rank, world, local):
                               "achieved": round(q_gbs, 1), "peak": hbm, "unit": "GB/s",
                               "frac": round(q_gbs / hbm, 4), "traffic": qtraffic_v, "peak_source": src},
         "quantize_modes": qmodes,
+        "formats_7b_gemm": formats,
+        "cublaslt_nvfp4": cublas,
+        "config2_350m_mlp": cfg2,
+        "stack_ue5m3": stack,
         "scale_format_sweep": sweep,
         "hadamard_16x16": hadamard,
         "fused_epilogue_quantize": fused_ep,

@@ -13,6 +13,9 @@ thread_local int g_last_cuda_error = 0;
 fp4_status cuda_status(cudaError_t e) {
   if (e == cudaSuccess) return FP4_OK;
   g_last_cuda_error = (int)e;
+  // clear the runtime's per-thread last error (a non-sticky one), so that a
+  // later call's launch check does not report this failure again
+  (void)cudaGetLastError();
   return FP4_ERR_CUDA;
 }
 
@@ -69,6 +72,14 @@ fp4_status prepare_amax(fp4lib::QuantArgs& a, const float* global_amax, float* a
   return FP4_OK;
 }
 
+// UE5M3 shift by-product: zero the word(s) the quantizer maxes its scale
+// codes into (n = 1 or 2 consecutive int32), before the launch.
+fp4_status prepare_shift(int f, int32_t* shift_out, int n, cudaStream_t st) {
+  if (shift_out == nullptr) return FP4_OK;
+  if (f != FP4_SF_UE5M3) return FP4_ERR_UNSUPPORTED;
+  return cuda_status(cudaMemsetAsync(shift_out, 0, n * sizeof(int32_t), st));
+}
+
 }  // namespace
 
 extern "C" {
@@ -96,7 +107,8 @@ fp4_status fp4_amax(const void* x_bf16, int64_t M, int64_t K, int64_t ldx, float
 
 fp4_status fp4_quantize(const void* x_bf16, int64_t M, int64_t K, int64_t ldx, fp4_scale_fmt f, fp4_rounding r,
                         uint64_t seed, const float* global_amax, int transpose, fp4_sf_layout sfl, uint8_t* codes,
-                        uint8_t* scales, float* amax_out, int32_t* dev_status, fp4_stream_t stream) {
+                        uint8_t* scales, float* amax_out, int32_t* ue5m3_shift_out, int32_t* dev_status,
+                        fp4_stream_t stream) {
   if (r != FP4_ROUND_RNE && r != FP4_ROUND_STOCHASTIC) return FP4_ERR_INVALID_ARG;
   if (transpose != 0 && transpose != 1) return FP4_ERR_INVALID_ARG;
   const int64_t out_rows = transpose ? K : M, out_cols = transpose ? M : K;
@@ -116,19 +128,25 @@ fp4_status fp4_quantize(const void* x_bf16, int64_t M, int64_t K, int64_t ldx, f
   a.mma = sfl == FP4_SFLAYOUT_MMA;
   a.status = dev_status;
   const bool sr = r == FP4_ROUND_STOCHASTIC;
+  uint32_t* shift_word = reinterpret_cast<uint32_t*>(ue5m3_shift_out);
   if (transpose) {
     a.col_sr = sr;
     a.seed_col = seed;
     a.codes_col = codes;
     a.scales_col = scales;
+    a.sf_max_col = shift_word;
   } else {
     a.row_sr = sr;
     a.seed_row = seed;
     a.codes_row = codes;
     a.scales_row = scales;
+    a.sf_max_row = shift_word;
   }
+  if ((s = prepare_shift((int)f, ue5m3_shift_out, 1, st)) != FP4_OK) return s;
   if ((s = prepare_amax(a, global_amax, amax_out, st)) != FP4_OK) return s;
-  return cuda_status(fp4lib::launch_quantize(a, st));
+  if ((s = cuda_status(fp4lib::launch_quantize(a, st))) != FP4_OK) return s;
+  if (ue5m3_shift_out != nullptr) return cuda_status(fp4lib::launch_ue5m3_finalize(ue5m3_shift_out, 1, st));
+  return FP4_OK;
 }
 
 fp4_status fp4_quantize_rht(const void* x_bf16, int64_t M, int64_t K, int64_t ldx, fp4_scale_fmt f, fp4_rounding r,
@@ -235,8 +253,8 @@ fp4_status fp4_quantize_dual_rht(const void* x_bf16, int64_t M, int64_t K, int64
 fp4_status fp4_quantize_dual(const void* x_bf16, int64_t M, int64_t K, int64_t ldx, fp4_scale_fmt f,
                              fp4_rounding r_row, uint64_t seed_row, fp4_rounding r_col, uint64_t seed_col,
                              const float* global_amax, fp4_sf_layout sfl, uint8_t* codes_row, uint8_t* scales_row,
-                             uint8_t* codes_col, uint8_t* scales_col, float* amax_out, int32_t* dev_status,
-                             fp4_stream_t stream) {
+                             uint8_t* codes_col, uint8_t* scales_col, float* amax_out, int32_t* ue5m3_shift_out,
+                             int32_t* dev_status, fp4_stream_t stream) {
   if ((r_row != FP4_ROUND_RNE && r_row != FP4_ROUND_STOCHASTIC) ||
       (r_col != FP4_ROUND_RNE && r_col != FP4_ROUND_STOCHASTIC))
     return FP4_ERR_INVALID_ARG;
@@ -267,8 +285,15 @@ fp4_status fp4_quantize_dual(const void* x_bf16, int64_t M, int64_t K, int64_t l
   a.scales_row = scales_row;
   a.codes_col = codes_col;
   a.scales_col = scales_col;
+  if (ue5m3_shift_out != nullptr) {
+    a.sf_max_row = reinterpret_cast<uint32_t*>(ue5m3_shift_out);
+    a.sf_max_col = reinterpret_cast<uint32_t*>(ue5m3_shift_out + 1);
+  }
+  if ((s = prepare_shift((int)f, ue5m3_shift_out, 2, st)) != FP4_OK) return s;
   if ((s = prepare_amax(a, global_amax, amax_out, st)) != FP4_OK) return s;
-  return cuda_status(fp4lib::launch_quantize(a, st));
+  if ((s = cuda_status(fp4lib::launch_quantize(a, st))) != FP4_OK) return s;
+  if (ue5m3_shift_out != nullptr) return cuda_status(fp4lib::launch_ue5m3_finalize(ue5m3_shift_out, 2, st));
+  return FP4_OK;
 }
 
 fp4_status fp4_dequantize(const uint8_t* codes, const uint8_t* scales, fp4_sf_layout sfl, int64_t M, int64_t K,
@@ -295,6 +320,13 @@ fp4_status fp4_ue5m3_to_e4m3(const uint8_t* ue5m3_scales, int64_t n, int32_t* t_
                                                   (cudaStream_t)stream));
 }
 
+fp4_status fp4_ue5m3_reencode(const uint8_t* ue5m3_scales, int64_t n, const int32_t* t, uint8_t* e4m3_out,
+                              int32_t* dev_status, fp4_stream_t stream) {
+  if (n < 0) return FP4_ERR_SHAPE;
+  if (t == nullptr || (n > 0 && (ue5m3_scales == nullptr || e4m3_out == nullptr))) return FP4_ERR_INVALID_ARG;
+  return cuda_status(fp4lib::launch_ue5m3_reencode(ue5m3_scales, n, t, e4m3_out, dev_status, (cudaStream_t)stream));
+}
+
 fp4_status fp4_ue5m3_windows(const uint8_t* ue5m3_scales, int64_t n, int32_t* t_out, int32_t* n_windows_out,
                              uint8_t* e4m3_out, int32_t* dev_status, fp4_stream_t stream) {
   if (n < 0) return FP4_ERR_SHAPE;
@@ -312,7 +344,7 @@ fp4_status fp4_gemm_ue5m3_windows(const uint8_t* Aq, const uint8_t* As_windows, 
   if (Aq == nullptr || As_windows == nullptr || tA == nullptr || nA == nullptr || Bq == nullptr ||
       Bs_windows == nullptr || tB == nullptr || nB == nullptr || ga == nullptr || gb == nullptr || C == nullptr)
     return FP4_ERR_INVALID_ARG;
-  if (M <= 0 || N <= 0 || K <= 0 || M % 128 != 0 || N % 256 != 0 || K % 256 != 0 || ldc < N) return FP4_ERR_SHAPE;
+  if (M <= 0 || N <= 0 || K <= 0 || M % 128 != 0 || N % 128 != 0 || K % 256 != 0 || ldc < N) return FP4_ERR_SHAPE;
   if (!aligned16(Aq) || !aligned16(As_windows) || !aligned16(Bq) || !aligned16(Bs_windows) || !aligned16(C) ||
       (ldc * 4) % 16 != 0)
     return FP4_ERR_ALIGNMENT;
@@ -359,7 +391,7 @@ fp4_status fp4_gemm(const uint8_t* Aq, const uint8_t* As, const uint8_t* Bq, con
   if (Aq == nullptr || As == nullptr || Bq == nullptr || Bs == nullptr || C == nullptr) return FP4_ERR_INVALID_ARG;
   if (f != FP4_SF_E8M0 && (ga == nullptr || gb == nullptr)) return FP4_ERR_INVALID_ARG;
   if (f == FP4_SF_UE5M3 && (tA == nullptr || tB == nullptr)) return FP4_ERR_INVALID_ARG;
-  if (M <= 0 || N <= 0 || K <= 0 || M % 128 != 0 || N % 256 != 0 || K % 256 != 0 || ldc < N) return FP4_ERR_SHAPE;
+  if (M <= 0 || N <= 0 || K <= 0 || M % 128 != 0 || N % 128 != 0 || K % 256 != 0 || ldc < N) return FP4_ERR_SHAPE;
   const int64_t esz = od == FP4_OUT_BF16 ? 2 : 4;
   if (!aligned16(Aq) || !aligned16(As) || !aligned16(Bq) || !aligned16(Bs) || !aligned16(C) ||
       (ldc * esz) % 16 != 0)
@@ -398,7 +430,7 @@ fp4_status fp4_gemm_quantize(const uint8_t* Aq, const uint8_t* As, const uint8_t
     return FP4_ERR_INVALID_ARG;
   if (f != FP4_SF_E8M0 && (ga == nullptr || gb == nullptr)) return FP4_ERR_INVALID_ARG;
   if (f == FP4_SF_UE5M3 && (tA == nullptr || tB == nullptr)) return FP4_ERR_INVALID_ARG;
-  if (M <= 0 || N <= 0 || K <= 0 || M % 128 != 0 || N % 256 != 0 || K % 256 != 0) return FP4_ERR_SHAPE;
+  if (M <= 0 || N <= 0 || K <= 0 || M % 128 != 0 || N % 128 != 0 || K % 256 != 0) return FP4_ERR_SHAPE;
   if (M % 256 != 0) return FP4_ERR_UNSUPPORTED;  // the quantizing epilogue runs on CTA pairs
   if (!aligned16(Aq) || !aligned16(As) || !aligned16(Bq) || !aligned16(Bs) || !aligned16(C_codes) ||
       !aligned16(C_scales))

@@ -54,6 +54,7 @@
 #include <cudaTypedefs.h>
 
 #include "async_sm103.cuh"
+#include "device_cache.h"
 #include "fp4_device.cuh"
 #include "launch.h"
 
@@ -444,7 +445,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + SMEM_BAR + BAR_BYTES + 8);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int m_tiles = p.M / BM, n_tiles = p.N / BN;
+  const int m_tiles = p.M / BM, n_tiles = (p.N + BN - 1) / BN;  // N % 128 == 0: the last tile may be half
   const int m_groups = m_tiles;
   const int num_units = m_groups * n_tiles;
   const int cluster_id = blockIdx.x, num_clusters = gridDim.x;
@@ -567,6 +568,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       bool ok = true;
       for (int u = cluster_id; u < num_units && ok; u += num_clusters) {
         const int mt = u % m_groups, nt = u / m_groups;
+        // a half tile past N (N % 256 == 128) reads the first half's scales:
+        // its code rows are zero-filled, so any finite scale gives 0
+        const int b_hi = (2 * nt + 1) * 128 < p.N ? 2 * nt + 1 : 2 * nt;
         for (int ks = 0; ks < k_steps; ++ks) {
           if (!wait_bounded(bar_sfd_empty + 8 * slot, phase ^ 1u, abort_flag, p.status) || *abort_flag) {
             ok = false;
@@ -580,7 +584,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           bulk_load(sbase + SMEM_SFB + slot * SFB_MAX, p.Bs + (2 * nt) * sf_row_stride + (int64_t)ks * SFB_HALF,
                     SFB_HALF, sb);
           bulk_load(sbase + SMEM_SFB + slot * SFB_MAX + SFB_HALF,
-                    p.Bs + (2 * nt + 1) * sf_row_stride + (int64_t)ks * SFB_HALF, SFB_HALF, sb);
+                    p.Bs + b_hi * sf_row_stride + (int64_t)ks * SFB_HALF, SFB_HALF, sb);
           if (++slot == SF_SLOTS) {
             slot = 0;
             phase ^= 1u;
@@ -670,8 +674,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_acc_empty);
-      store_block<BF16, PL>(r, alpha, stage_buf, stage_addr, &tmap_c, mt * BM + 32 * quarter,
-                            nt * BN + EPI_COLS * cblk, lane, p.accumulate != 0);
+      // 64-column slabs at or past N (a half tile) hold no output
+      if (nt * BN + EPI_COLS * cblk < p.N)
+        store_block<BF16, PL>(r, alpha, stage_buf, stage_addr, &tmap_c, mt * BM + 32 * quarter,
+                              nt * BN + EPI_COLS * cblk, lane, p.accumulate != 0);
     }
     if (lane == 0) bulk_wait0();
     __syncwarp();
@@ -740,7 +746,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t crank = cluster_rank();  // 0: issues the MMAs; 1: its peer
   const bool leader = crank == 0;
-  const int m_pairs = p.M / PM, n_tiles = p.N / BN;
+  const int m_pairs = p.M / PM, n_tiles = (p.N + BN - 1) / BN;  // N % 128 == 0: the last tile may be half
   // units walk N fastest: the clusters of one round share a few 256-row
   // blocks of A and sweep B, which keeps a round's operands within L2 even
   // when A alone approaches its size (dgrad, wgrad)
@@ -883,6 +889,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       for (int u = cluster_id; u < num_units && ok; u += num_clusters) {
         const int mp = u / n_tiles, nt = u % n_tiles;
         const int a_slab = 2 * mp + (int)crank;
+        // a half tile past N (N % 256 == 128) reads the first half's scales:
+        // its code rows are zero-filled, so any finite scale gives 0
+        const int b_hi = (2 * nt + 1) * 128 < p.N ? 2 * nt + 1 : 2 * nt;
         for (int ks = 0; ks < k_steps; ++ks) {
           if (!wait_bounded(bar_sfd_empty + 8 * slot, phase ^ 1u, abort_flag, p.status) || *abort_flag) {
             ok = false;
@@ -895,7 +904,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           bulk_load(sbase + SMEM_SFB + slot * SFB_MAX, p.Bs + (2 * nt) * sf_row_stride + (int64_t)ks * SFB_HALF,
                     SFB_HALF, sb);
           bulk_load(sbase + SMEM_SFB + slot * SFB_MAX + SFB_HALF,
-                    p.Bs + (2 * nt + 1) * sf_row_stride + (int64_t)ks * SFB_HALF, SFB_HALF, sb);
+                    p.Bs + b_hi * sf_row_stride + (int64_t)ks * SFB_HALF, SFB_HALF, sb);
           if (++slot == SF_SLOTS) {
             slot = 0;
             phase ^= 1u;
@@ -984,6 +993,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(lead_acc_empty);
+      if (nt * BN + EPI_COLS * cblk >= p.N) continue;  // a slab past N (half tile): no output
       if constexpr (QOUT) {
         quant_epilogue(r, alpha, p, mp * PM + BM * (int)crank + 32 * quarter + lane, nt * BN + EPI_COLS * cblk,
                        s_enc_out, amax_local);
@@ -1048,27 +1058,19 @@ bool make_out_map(CUtensorMap* map, void* base, int64_t M, int64_t N, int64_t ld
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-int sm_count() {
-  static int n = 0;
-  if (n == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    if (n <= 0) n = 148;
-  }
-  return n;
-}
+int sm_count() { return fp4lib::current_sm_count(); }
 
 template <int FMT, bool BF16, class PL>
 cudaError_t launch_t(const fp4lib::GemmArgs& a, cudaStream_t st) {
   auto kern = k_gemm_fp4<FMT, BF16, PL>;
   constexpr int SMEM_LAUNCH = PL::SMEM_LAUNCH;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_LAUNCH);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static fp4lib::DeviceInts attr_set;  // per device: the shared-memory size is set
+  cudaError_t e = cudaSuccess;
+  attr_set.get([&] {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_LAUNCH);
+    return e == cudaSuccess ? 1 : 0;
+  });
+  if (e != cudaSuccess) return e;
   CUtensorMap ma, mb, mc;
   if (!make_code_map(&ma, a.Aq, a.M, a.K / 2, BM) || !make_code_map(&mb, a.Bq, a.N, a.K / 2, BN) ||
       !make_out_map(&mc, a.C, a.M, a.N, a.ldc, BF16, PL::OUT_ROW_BYTES))
@@ -1089,7 +1091,7 @@ cudaError_t launch_t(const fp4lib::GemmArgs& a, cudaStream_t st) {
   p.N = (int)a.N;
   p.K = (int)a.K;
   p.status = a.status;
-  const int units = (int)((a.M / BM) * (a.N / BN));
+  const int units = (int)((a.M / BM) * ((a.N + BN - 1) / BN));
   const int ctas = units < sm_count() ? units : sm_count();
   kern<<<(unsigned)ctas, NUM_THREADS, SMEM_LAUNCH, st>>>(ma, mb, mc, p);
   return cudaGetLastError();
@@ -1102,8 +1104,8 @@ cudaError_t launch_pair(const fp4lib::GemmArgs& a, cudaStream_t st) {
   using PL = PlanPair;
   auto kern = k_gemm_fp4_pair<FMT, BF16, PL, QOUT>;
   constexpr int SMEM_LAUNCH = PL::SMEM_LAUNCH;
-  static bool attr_set = false;
-  static int max_clusters = 0;
+  // per device: the shared-memory size set, then the co-resident clusters
+  static fp4lib::DeviceInts max_clusters_of;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -1115,15 +1117,17 @@ cudaError_t launch_pair(const fp4lib::GemmArgs& a, cudaStream_t st) {
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_LAUNCH);
-    if (e != cudaSuccess) return e;
+  cudaError_t err = cudaSuccess;
+  const int max_clusters = max_clusters_of.get([&] {
+    err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_LAUNCH);
+    if (err != cudaSuccess) return 0;
     cfg.gridDim = dim3(sm_count() & ~1, 1, 1);
-    e = cudaOccupancyMaxActiveClusters(&max_clusters, kern, &cfg);
-    if (e != cudaSuccess) return e;
-    if (max_clusters <= 0) return cudaErrorInvalidConfiguration;
-    attr_set = true;
-  }
+    int n = 0;
+    err = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+    return err == cudaSuccess ? n : 0;
+  });
+  if (err != cudaSuccess) return err;
+  if (max_clusters <= 0) return cudaErrorInvalidConfiguration;
   CUtensorMap ma, mb, mc;
   // with a quantized output the C map is never used; it is built over the code buffer
   void* cbase = QOUT ? static_cast<void*>(a.q_codes) : a.C;
@@ -1154,7 +1158,7 @@ cudaError_t launch_pair(const fp4lib::GemmArgs& a, cudaStream_t st) {
   p.q_seed = a.q_seed;
   p.q_sr = a.q_sr ? 1 : 0;
   p.q_mma = a.q_mma ? 1 : 0;
-  const int units = (int)((a.M / (2 * BM)) * (a.N / BN));
+  const int units = (int)((a.M / (2 * BM)) * ((a.N + BN - 1) / BN));
   const int clusters = units < max_clusters ? units : max_clusters;
   cfg.gridDim = dim3((unsigned)(2 * clusters), 1, 1);
   return cudaLaunchKernelEx(&cfg, kern, ma, mb, mc, p);
@@ -1173,7 +1177,7 @@ cudaError_t launch_cm(const fp4lib::GemmArgs& a, cudaStream_t st) {
 namespace fp4lib {
 
 cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t st) {
-  if (a.N % BN != 0) return cudaErrorNotSupported;
+  if (a.N % 128 != 0) return cudaErrorNotSupported;
   if (a.qout) {
     // quantizing epilogue: CTA-pair kernel only (M a multiple of 256)
     if (a.M % (2 * BM) != 0) return cudaErrorNotSupported;

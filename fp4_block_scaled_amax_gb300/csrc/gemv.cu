@@ -32,6 +32,7 @@
 #include <cudaTypedefs.h>
 
 #include "async_sm103.cuh"
+#include "device_cache.h"
 #include "fp4_device.cuh"
 #include "launch.h"
 
@@ -495,16 +496,7 @@ bool make_map(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-int sm_count() {
-  static int n = 0;
-  if (n == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    if (n <= 0) n = 148;
-  }
-  return n;
-}
+int sm_count() { return fp4lib::current_sm_count(); }
 
 template <int WPT, int NT>
 cudaError_t launch_tma_t(const fp4lib::GemvArgs& a, int T, cudaStream_t st) {
@@ -529,13 +521,23 @@ cudaError_t launch_tma_t(const fp4lib::GemvArgs& a, int T, cudaStream_t st) {
       !make_map(&mx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.x, a.K, a.batch, a.K * 2, 64, 8 * NT,
                 CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B))
     return cudaErrorNotSupported;
-  static size_t smem_set = 0;
-  if (smem > smem_set) {
-    cudaError_t e =
-        cudaFuncSetAttribute(k_gemv_w4a16_tma<WPT, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    smem_set = smem;
-  }
+  // once per device: allow the most dynamic shared memory this instance can
+  // have there (the opt-in limit less its static shared memory)
+  static fp4lib::DeviceInts smem_allowed;
+  cudaError_t e = cudaSuccess;
+  const int allowed = smem_allowed.get([&] {
+    int dev = 0, optin = 0;
+    cudaFuncAttributes fa{};
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) != cudaSuccess ||
+        (e = cudaFuncGetAttributes(&fa, k_gemv_w4a16_tma<WPT, NT>)) != cudaSuccess)
+      return 0;
+    const int n = optin - (int)fa.sharedSizeBytes;
+    e = cudaFuncSetAttribute(k_gemv_w4a16_tma<WPT, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, n);
+    return e == cudaSuccess ? n : 0;
+  });
+  if (e != cudaSuccess) return e;
+  if (allowed <= 0 || smem > (size_t)allowed) return cudaErrorNotSupported;
   k_gemv_w4a16_tma<WPT, NT><<<(unsigned)ctas, 32 * (1 + WPT * T), smem, st>>>(mc, ms, mx, a.gw, (int)a.batch, (int)a.N, nk,
                                                                          T, S, a.bf16_out, a.y, a.status);
   return cudaGetLastError();
@@ -567,9 +569,7 @@ cudaError_t launch_gemv(const GemvArgs& a, cudaStream_t st) {
   // register-fed form: 16 weight rows per CTA; enough warps per CTA (split K) to put about 16
   // warps on each of the GPU's SMs in a single wave
   const int64_t ctas = (a.N + 15) / 16;
-  int dev = 0, sms = 148;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int sms = fp4lib::current_sm_count();
   const int64_t kchunks = (a.K + 127) / 128;
   int64_t warps = (int64_t)sms * 16 / ctas;
   warps = warps < 4 ? 4 : (warps > MAX_WARPS ? MAX_WARPS : warps);

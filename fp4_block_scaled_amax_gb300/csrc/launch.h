@@ -17,6 +17,9 @@ struct QuantArgs {
   uint8_t *codes_row, *scales_row, *codes_col, *scales_col;
   float* amax_out;
   int32_t* status;
+  // UE5M3 only, nullable: atomic max of the row / transposed outputs' scale
+  // codes (zeroed by the caller; launch_ue5m3_finalize turns each into t)
+  uint32_t *sf_max_row, *sf_max_col;
 };
 
 cudaError_t launch_amax(const void* x, int64_t M, int64_t K, int64_t ldx, float* out, cudaStream_t st);
@@ -25,6 +28,11 @@ cudaError_t launch_dequantize(const uint8_t* codes, const uint8_t* scales, bool 
                               int fmt, const float* gptr, bool bf16, void* out, cudaStream_t st);
 cudaError_t launch_ue5m3_to_e4m3(const uint8_t* in, int64_t n, int32_t* t_out, uint8_t* out, int32_t* status,
                                  cudaStream_t st);
+// the same re-encode with a known shift *t (device int)
+cudaError_t launch_ue5m3_reencode(const uint8_t* in, int64_t n, const int32_t* t, uint8_t* out, int32_t* status,
+                                  cudaStream_t st);
+// words[0..n): largest UE5M3 code of a scale set -> its shift t = e_max - 7
+cudaError_t launch_ue5m3_finalize(int32_t* words, int n, cudaStream_t st);
 // UE5M3 scale codes -> up to three E4M3 windows (out: 3 arrays of n codes),
 // shifts t_out[3], windows in use n_out[1]
 cudaError_t launch_ue5m3_windows(const uint8_t* in, int64_t n, int32_t* t_out, int32_t* n_out, uint8_t* out,

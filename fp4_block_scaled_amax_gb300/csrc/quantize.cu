@@ -94,7 +94,8 @@ __global__ void __launch_bounds__(256) k_quant_rows(const uint16_t* __restrict__
                                                     int64_t ldx, const float* __restrict__ gptr,
                                                     uint64_t seed, uint8_t* __restrict__ codes,
                                                     uint8_t* __restrict__ scales,
-                                                    float* __restrict__ amax_out, int32_t* status) {
+                                                    float* __restrict__ amax_out, int32_t* status,
+                                                    uint32_t* __restrict__ sf_max) {
   constexpr int G = ScaleFmt<FMT>::G;
   const int64_t per_row = K / 16;
   const int64_t chunk = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -117,6 +118,13 @@ __global__ void __launch_bounds__(256) k_quant_rows(const uint16_t* __restrict__
   const BlockScale bs = block_scale<FMT>(a, s_enc);
   const uint2 q = quant16<SR, Elem<FMT>::INT4>(w, bs.r, seed, (uint64_t)(row * K + c16 * 16));
   *reinterpret_cast<uint2*>(codes + row * (K / 2) + c16 * 8) = q;
+  if constexpr (FMT == SF_UE5M3) {
+    if (sf_max != nullptr) {
+      // UE5M3 codes order like their values: the largest code gives e_max
+      const unsigned int mc = __reduce_max_sync(mask, bs.code);
+      if ((threadIdx.x & 31) == (unsigned)(__ffs(mask) - 1)) atomicMax(sf_max, mc);
+    }
+  }
   if (G == 16 || (c16 & 1) == 0) {
     const int64_t b = c16 * 16 / G;
     const int64_t nb = K / G;
@@ -146,7 +154,7 @@ __global__ void __launch_bounds__(256) k_quant_tile(
     const uint16_t* __restrict__ x, int64_t M, int64_t K, int64_t ldx, const float* __restrict__ gptr,
     uint64_t seed_row, uint64_t seed_col, uint8_t* __restrict__ codes_row, uint8_t* __restrict__ scales_row,
     uint8_t* __restrict__ codes_col, uint8_t* __restrict__ scales_col, float* __restrict__ amax_out,
-    int32_t* status) {
+    int32_t* status, uint32_t* __restrict__ sf_max_row, uint32_t* __restrict__ sf_max_col) {
   constexpr int G = ScaleFmt<FMT>::G;
   __shared__ __align__(16) uint16_t tile[TILE_M][TILE_K];
   __shared__ float rtab[256];
@@ -181,6 +189,7 @@ __global__ void __launch_bounds__(256) k_quant_tile(
   rtab[threadIdx.x] = code_multiplier<FMT>(threadIdx.x, s_enc);
   __syncthreads();
   float amax_local = 0.0f;
+  uint32_t maxc_row = 0;  // largest row scale code (UE5M3 shift by-product)
 #pragma unroll
   for (int it = 0; it < 2; ++it) {
     const int j = threadIdx.x + 256 * it;
@@ -197,6 +206,7 @@ __global__ void __launch_bounds__(256) k_quant_tile(
         const BlockScale bs = block_scale_tab<FMT>(a, s_enc, rtab);
         const uint2 q = quant16<ROW_SR>(w[it], bs.r, seed_row, (uint64_t)(row * K + col));
         *reinterpret_cast<uint2*>(codes_row + row * (K / 2) + col / 2) = q;
+        maxc_row = max(maxc_row, bs.code);
         if (G == 16 || (cc & 1) == 0) {
           const int64_t b = col / G;
           const int64_t nb = K / G;
@@ -209,12 +219,19 @@ __global__ void __launch_bounds__(256) k_quant_tile(
     const unsigned int am = __reduce_max_sync(0xFFFFFFFFu, __float_as_uint(amax_local));
     if ((threadIdx.x & 31) == 0) atomicMax(reinterpret_cast<unsigned int*>(amax_out), am);
   }
+  if constexpr (DUAL && FMT == SF_UE5M3) {
+    if (sf_max_row != nullptr) {
+      const unsigned int mc = __reduce_max_sync(0xFFFFFFFFu, maxc_row);
+      if ((threadIdx.x & 31) == 0) atomicMax(sf_max_row, mc);
+    }
+  }
   __syncthreads();
 
   // ---- column pass: thread t owns column k0 + t/2, rows m0 + 32*(t%2) .. +31 ----
   const int cl = threadIdx.x >> 1, h = threadIdx.x & 1;
   const int64_t c = k0 + cl;
   const int64_t rbase = m0 + 32 * h;
+  const unsigned cmask = __ballot_sync(0xFFFFFFFFu, c < K && rbase < M);
   if (c >= K || rbase >= M) return;
   const int pc = cl ^ (h << 4);
   uint32_t v[16];
@@ -238,6 +255,12 @@ __global__ void __launch_bounds__(256) k_quant_tile(
     sc0 = b0.code;
   }
   *reinterpret_cast<uint4*>(codes_col + c * (M / 2) + rbase / 2) = make_uint4(q0.x, q0.y, q1.x, q1.y);
+  if constexpr (FMT == SF_UE5M3) {
+    if (sf_max_col != nullptr) {
+      const unsigned int mc = __reduce_max_sync(cmask, max(sc0, sc1));
+      if ((threadIdx.x & 31) == (unsigned)(__ffs(cmask) - 1)) atomicMax(sf_max_col, mc);
+    }
+  }
   const int64_t nb = M / G;
   const int64_t b = rbase / G;
   if constexpr (G == 16) {
@@ -317,10 +340,13 @@ __device__ __forceinline__ int ue5m3_shift_from_maxcode(uint32_t c) {
   return (31 - __clz(m)) - 17 - 7;  // m * 2^-17, floor(log2 m) in 0..2
 }
 
+// FROM_CODE: *tword holds the largest UE5M3 code (the shift follows from it);
+// otherwise *tword is the shift t itself.
+template <bool FROM_CODE>
 __global__ void __launch_bounds__(256) k_ue5m3_reencode(const uint8_t* __restrict__ s, int64_t n,
-                                                        const int32_t* maxcode, uint8_t* __restrict__ out,
+                                                        const int32_t* tword, uint8_t* __restrict__ out,
                                                         int32_t* status) {
-  const int t = ue5m3_shift_from_maxcode((uint32_t)__ldg(maxcode));
+  const int t = FROM_CODE ? ue5m3_shift_from_maxcode((uint32_t)__ldg(tword)) : (int)__ldg(tword);
   // 2^-t as a float (|t| <= 26)
   const float scale = __uint_as_float((uint32_t)(127 - t) << 23);
   bool bad = false;
@@ -333,8 +359,9 @@ __global__ void __launch_bounds__(256) k_ue5m3_reencode(const uint8_t* __restric
   if (__any_sync(0xFFFFFFFFu, bad) && (threadIdx.x & 31) == 0) set_status(status, FP4_ERR_UE5M3_RANGE);
 }
 
-__global__ void k_ue5m3_finalize(int32_t* t_inout) {
-  *t_inout = ue5m3_shift_from_maxcode((uint32_t)*t_inout);
+// n words, each the largest UE5M3 code of a scale set, become its shift t
+__global__ void k_ue5m3_finalize(int32_t* t_inout, int n) {
+  if ((int)threadIdx.x < n) t_inout[threadIdx.x] = ue5m3_shift_from_maxcode((uint32_t)t_inout[threadIdx.x]);
 }
 
 // UE5M3 scales wider than one E4M3 window: with e_max the largest exponent
@@ -433,7 +460,7 @@ static void rows_t(const QuantArgs& a, cudaStream_t st) {
   if (chunks == 0) return;
   k_quant_rows<FMT, SR, MMA, AMAX><<<grid_for(chunks), 256, 0, st>>>(
       static_cast<const uint16_t*>(a.x), a.M, a.K, a.ldx, a.gptr, a.seed_row, a.codes_row, a.scales_row,
-      a.amax_out, a.status);
+      a.amax_out, a.status, a.sf_max_row);
 }
 
 template <int FMT, bool DUAL, bool RSR, bool CSR, bool MMA, bool AMAX>
@@ -442,7 +469,7 @@ static void tile_t(const QuantArgs& a, cudaStream_t st) {
   dim3 grid((unsigned)((a.M + TILE_M - 1) / TILE_M), (unsigned)((a.K + TILE_K - 1) / TILE_K));
   k_quant_tile<FMT, DUAL, RSR, CSR, MMA, AMAX><<<grid, 256, 0, st>>>(
       static_cast<const uint16_t*>(a.x), a.M, a.K, a.ldx, a.gptr, a.seed_row, a.seed_col, a.codes_row,
-      a.scales_row, a.codes_col, a.scales_col, a.amax_out, a.status);
+      a.scales_row, a.codes_col, a.scales_col, a.amax_out, a.status, a.sf_max_row, a.sf_max_col);
 }
 
 // runtime -> template dispatch
@@ -542,9 +569,23 @@ cudaError_t launch_ue5m3_to_e4m3(const uint8_t* in, int64_t n, int32_t* t_out, u
     int64_t blocks = (n + 255) / 256;
     if (blocks > 152 * 8) blocks = 152 * 8;
     k_ue5m3_maxcode<<<(unsigned)blocks, 256, 0, st>>>(in, n, t_out);
-    k_ue5m3_reencode<<<(unsigned)blocks, 256, 0, st>>>(in, n, t_out, out, status);
+    k_ue5m3_reencode<true><<<(unsigned)blocks, 256, 0, st>>>(in, n, t_out, out, status);
   }
-  k_ue5m3_finalize<<<1, 1, 0, st>>>(t_out);
+  k_ue5m3_finalize<<<1, 32, 0, st>>>(t_out, 1);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_ue5m3_reencode(const uint8_t* in, int64_t n, const int32_t* t, uint8_t* out, int32_t* status,
+                                  cudaStream_t st) {
+  if (n == 0) return cudaSuccess;
+  int64_t blocks = (n + 255) / 256;
+  if (blocks > 152 * 8) blocks = 152 * 8;
+  k_ue5m3_reencode<false><<<(unsigned)blocks, 256, 0, st>>>(in, n, t, out, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_ue5m3_finalize(int32_t* words, int n, cudaStream_t st) {
+  k_ue5m3_finalize<<<1, 32, 0, st>>>(words, n);
   return cudaGetLastError();
 }
 

@@ -58,15 +58,17 @@ _SIGS = {
     "fp4_group_size": (_I32, [_I32]),
     "fp4_storage_bytes": (_I32, [_I64, _I64, _I32, _SZP, _SZP]),
     "fp4_amax": (_I32, [_VP, _I64, _I64, _I64, _VP, _VP]),
-    "fp4_quantize": (_I32, [_VP, _I64, _I64, _I64, _I32, _I32, _U64, _VP, _I32, _I32, _VP, _VP, _VP, _VP, _VP]),
+    "fp4_quantize": (_I32, [_VP, _I64, _I64, _I64, _I32, _I32, _U64, _VP, _I32, _I32, _VP, _VP, _VP, _VP, _VP,
+                            _VP]),
     "fp4_quantize_rht": (_I32, [_VP, _I64, _I64, _I64, _I32, _I32, _U64, ctypes.c_uint32, _VP, _I32, _VP, _VP, _VP,
                                 _VP, _VP]),
     "fp4_quantize_dual_rht": (_I32, [_VP, _I64, _I64, _I64, _I32, _I32, _U64, _I32, _U64, ctypes.c_uint32, _VP, _VP,
                                      _I32, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
     "fp4_quantize_dual": (_I32, [_VP, _I64, _I64, _I64, _I32, _I32, _U64, _I32, _U64, _VP, _I32,
-                                 _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
+                                 _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
     "fp4_dequantize": (_I32, [_VP, _VP, _I32, _I64, _I64, _I32, _VP, _I32, _VP, _VP]),
     "fp4_ue5m3_to_e4m3": (_I32, [_VP, _I64, _VP, _VP, _VP, _VP]),
+    "fp4_ue5m3_reencode": (_I32, [_VP, _I64, _VP, _VP, _VP, _VP]),
     "fp4_gemm": (_I32, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _I64, _I64, _I64, _I32, _I32, _I32, _VP, _I64,
                         _VP, _VP]),
     "fp4_gemm_quantize": (_I32, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _I64, _I64, _I64, _I32, _I32, _VP, _I32,
@@ -150,11 +152,12 @@ def fp4_amax(x, amax_out, stream=None):
 
 
 def fp4_quantize(x, fmt, rounding, seed, global_amax, transpose, sfl, codes, scales,
-                 amax_out=None, dev_status=None, stream=None):
+                 amax_out=None, dev_status=None, stream=None, ue5m3_shift_out=None):
     M, K = x.shape
     _check(_lib().fp4_quantize(_ptr(x), M, K, x.stride(0), _fmt(fmt), int(rounding), int(seed),
                                _ptr(global_amax), int(transpose), int(sfl), _ptr(codes), _ptr(scales),
-                               _ptr(amax_out), _ptr(dev_status), _stream(stream)), "fp4_quantize")
+                               _ptr(amax_out), _ptr(ue5m3_shift_out), _ptr(dev_status), _stream(stream)),
+           "fp4_quantize")
 
 
 def fp4_quantize_rht(x, fmt, rounding, seed, rht_mask, global_amax, sf_layout, codes, scales, amax_out=None,
@@ -177,12 +180,13 @@ def fp4_quantize_dual_rht(x, fmt, r_row, seed_row, r_col, seed_col, rht_mask, g_
 
 
 def fp4_quantize_dual(x, fmt, r_row, seed_row, r_col, seed_col, global_amax, sfl, codes_row, scales_row,
-                      codes_col, scales_col, amax_out=None, dev_status=None, stream=None):
+                      codes_col, scales_col, amax_out=None, dev_status=None, stream=None, ue5m3_shift_out=None):
     M, K = x.shape
     _check(_lib().fp4_quantize_dual(_ptr(x), M, K, x.stride(0), _fmt(fmt), int(r_row), int(seed_row),
                                     int(r_col), int(seed_col), _ptr(global_amax), int(sfl),
                                     _ptr(codes_row), _ptr(scales_row), _ptr(codes_col), _ptr(scales_col),
-                                    _ptr(amax_out), _ptr(dev_status), _stream(stream)), "fp4_quantize_dual")
+                                    _ptr(amax_out), _ptr(ue5m3_shift_out), _ptr(dev_status), _stream(stream)),
+           "fp4_quantize_dual")
 
 
 def fp4_dequantize(codes, scales, sfl, M, K, fmt, global_amax, out_dtype, out, stream=None):
@@ -193,6 +197,11 @@ def fp4_dequantize(codes, scales, sfl, M, K, fmt, global_amax, out_dtype, out, s
 def fp4_ue5m3_to_e4m3(scales, t_out, e4m3_out, dev_status=None, stream=None):
     _check(_lib().fp4_ue5m3_to_e4m3(_ptr(scales), scales.numel(), _ptr(t_out), _ptr(e4m3_out),
                                     _ptr(dev_status), _stream(stream)), "fp4_ue5m3_to_e4m3")
+
+
+def fp4_ue5m3_reencode(scales, t, e4m3_out, dev_status=None, stream=None):
+    _check(_lib().fp4_ue5m3_reencode(_ptr(scales), scales.numel(), _ptr(t), _ptr(e4m3_out), _ptr(dev_status),
+                                     _stream(stream)), "fp4_ue5m3_reencode")
 
 
 def fp4_gemm(Aq, As, Bq, Bs, ga, gb, tA, tB, M, N, K, fmt, out_dtype, C, ldc=None, dev_status=None,

@@ -112,6 +112,27 @@ def config4_step(t: int, scale: int = 1):
             "dY": laplace((M, H), s, 1001 + 2 * t, scale=1e-4, mult=g)}
 
 
+def config4_step_device(t: int, device, scale: int = 1):
+    """Config-4 inputs of step t drawn on the device (torch's CUDA Philox
+    generator, seeded per step and tensor): X_t = 1.02^t N(0, 1) and
+    dY_t = 1.02^t Laplace(0, 1e-4), both [32768, 4096] bf16 at full size.
+    The 100-step sequence is too large to draw on the host in reasonable
+    time; the oracle reads these bytes back from the device."""
+    s = SEEDS[4]
+    M, H = _dim(32768, scale), _dim(4096, scale)
+    mult = 1.02 ** t
+    gx = torch.Generator(device=device)
+    gx.manual_seed(s * 1_000_003 + 2 * t)
+    x = torch.randn((M, H), generator=gx, device=device, dtype=torch.float32)
+    x.mul_(mult)
+    gd = torch.Generator(device=device)
+    gd.manual_seed(s * 1_000_003 + 2 * t + 1)
+    # Laplace(0, b) by the inverse CDF of u ~ U(-1/2, 1/2): -b sign(u) log(1 - 2|u|)
+    u = torch.rand((M, H), generator=gd, device=device, dtype=torch.float32).sub_(0.5)
+    d = torch.log1p(u.abs().mul_(-2.0).clamp_(min=-1.0 + 2.0 ** -24)).mul_(u.sign()).mul_(-1e-4 * mult)
+    return {"X": x.to(torch.bfloat16), "dY": d.to(torch.bfloat16)}
+
+
 def config5(batch: int, scale: int = 1):
     s = SEEDS[5]
     F, H = _dim(18944, scale), _dim(3584, scale)

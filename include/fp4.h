@@ -143,6 +143,12 @@ fp4_status fp4_amax(const void* x_bf16, int64_t M, int64_t K, int64_t ldx,
  *           fresh g first and then requires amax_out (which receives it).
  * amax_out: nullable device float; receives max|x| of this call (the value a
  *           refresh would store).
+ * ue5m3_shift_out: nullable device int32, f = UE5M3 only (other formats:
+ *           FP4_ERR_UNSUPPORTED); receives t = e_max - 7 of this call's
+ *           scales, e_max the largest unbiased exponent among them (0 when
+ *           all are zero): the shift fp4_ue5m3_reencode and fp4_gemm take
+ *           for the E4M3 tensor-core emulation ([UE5M3] "Ограничения"),
+ *           found while the scales are made instead of by a second pass.
  * Requirements: M, K >= 0; the blocked dimension a multiple of G; x, codes,
  * scales 16-byte aligned and ldx*2 a multiple of 16; for transpose = 1 also
  * M % 32 == 0 and K % 32 == 0; FP4_SFLAYOUT_MMA needs the output rows % 128 == 0
@@ -151,7 +157,7 @@ fp4_status fp4_quantize(const void* x_bf16, int64_t M, int64_t K, int64_t ldx,
                         fp4_scale_fmt f, fp4_rounding r, uint64_t seed,
                         const float* global_amax, int transpose, fp4_sf_layout sfl,
                         uint8_t* codes, uint8_t* scales, float* amax_out,
-                        int32_t* dev_status, fp4_stream_t stream);
+                        int32_t* ue5m3_shift_out, int32_t* dev_status, fp4_stream_t stream);
 
 /* fp4_quantize (row layout) of the 16 x 16 random Hadamard transform of x:
  * every 16-element block along K first becomes x' = 1/4 * H16 * (s . x), H16
@@ -195,6 +201,8 @@ fp4_status fp4_quantize_dual_rht(const void* x_bf16, int64_t M, int64_t K, int64
 /* Row and transposed quantization of one bf16 [M, K] matrix from a single
  * read: writes exactly what fp4_quantize(transpose=0, r_row, seed_row) and
  * fp4_quantize(transpose=1, r_col, seed_col) would, with the same global amax.
+ * ue5m3_shift_out: nullable device int32[2] (UE5M3 only): the shifts t of the
+ * row and of the transposed scales, as fp4_quantize defines them.
  * Needs M % 32 == 0 and K % 32 == 0 besides fp4_quantize's requirements. */
 fp4_status fp4_quantize_dual(const void* x_bf16, int64_t M, int64_t K, int64_t ldx,
                              fp4_scale_fmt f, fp4_rounding r_row, uint64_t seed_row,
@@ -202,7 +210,8 @@ fp4_status fp4_quantize_dual(const void* x_bf16, int64_t M, int64_t K, int64_t l
                              const float* global_amax, fp4_sf_layout sfl,
                              uint8_t* codes_row, uint8_t* scales_row,
                              uint8_t* codes_col, uint8_t* scales_col,
-                             float* amax_out, int32_t* dev_status, fp4_stream_t stream);
+                             float* amax_out, int32_t* ue5m3_shift_out,
+                             int32_t* dev_status, fp4_stream_t stream);
 
 /* Dequantize codes + scales of an [M, K] tensor (blocks along K):
  * out = f32(f32(e2m1 * s_b) / s_enc) with s_enc from *global_amax as in
@@ -220,6 +229,14 @@ fp4_status fp4_dequantize(const uint8_t* codes, const uint8_t* scales, fp4_sf_la
  * dev_status.  fp4_gemm then multiplies its result by 2^(tA + tB). */
 fp4_status fp4_ue5m3_to_e4m3(const uint8_t* ue5m3_scales, int64_t n, int32_t* t_out,
                              uint8_t* e4m3_out, int32_t* dev_status, fp4_stream_t stream);
+
+/* fp4_ue5m3_to_e4m3 with the shift already known (the ue5m3_shift_out of
+ * fp4_quantize / fp4_quantize_dual, device int *t): one pass over the n
+ * scales, each written as the E4M3 code of s * 2^-t; a scale that is not
+ * exact after the shift is encoded to nearest and raises FP4_ERR_UE5M3_RANGE
+ * in dev_status. */
+fp4_status fp4_ue5m3_reencode(const uint8_t* ue5m3_scales, int64_t n, const int32_t* t,
+                              uint8_t* e4m3_out, int32_t* dev_status, fp4_stream_t stream);
 
 /* UE5M3 scales wider than one E4M3 window (the same emulation, [UE5M3]
  * "Ограничения").  With e(s) = floor(log2 s) for each nonzero scale value and
@@ -262,8 +279,10 @@ fp4_status fp4_gemm_ue5m3_windows(const uint8_t* Aq, const uint8_t* As_windows, 
  * f = E4M3 or E8M0; f = UE5M3 takes the E4M3 scales and shifts produced by
  * fp4_ue5m3_to_e4m3 (tA, tB device ints, required; NULL for other formats).
  * C: float32 or bf16 [M, N] with leading dimension ldc (elements).
- * Requirements: M % 128 == 0, N % 256 == 0, K % 256 == 0, all > 0; pointers
- * 16-byte aligned; ldc * element size a multiple of 16. */
+ * Requirements: M % 128 == 0, N % 128 == 0, K % 256 == 0, all > 0; pointers
+ * 16-byte aligned; ldc * element size a multiple of 16.  (Output tiles are
+ * 256 columns wide; with N % 256 == 128 the last tile's upper half reads
+ * zero-filled code rows and stores nothing.) */
 fp4_status fp4_gemm(const uint8_t* Aq, const uint8_t* As, const uint8_t* Bq, const uint8_t* Bs,
                     const float* ga, const float* gb, const int32_t* tA, const int32_t* tB,
                     int64_t M, int64_t N, int64_t K, fp4_scale_fmt f, fp4_gemm_layout layout,

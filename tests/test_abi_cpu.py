@@ -65,10 +65,10 @@ P = 0x10000  # a fake, 16-byte aligned "device" address; never dereferenced
 def q(**kw):
     lib = _need_lib()
     a = dict(x=P, M=64, K=64, ldx=64, f=0, r=0, seed=0, g=P, tr=0, sfl=0, codes=P, scales=P, amax=None,
-             st=None)
+             shift=None, st=None)
     a.update(kw)
     return lib.fp4_quantize(a["x"], a["M"], a["K"], a["ldx"], a["f"], a["r"], a["seed"], a["g"], a["tr"],
-                            a["sfl"], a["codes"], a["scales"], a["amax"], a["st"], None)
+                            a["sfl"], a["codes"], a["scales"], a["amax"], a["shift"], a["st"], None)
 
 
 def test_quantize_argument_errors():
@@ -85,6 +85,18 @@ def test_quantize_argument_errors():
     assert q(tr=1, M=48) == fp4.FP4_ERR_SHAPE             # transpose needs M % 32
     assert q(sfl=1) == fp4.FP4_ERR_SHAPE                  # MMA layout needs rows % 128
     assert q(g=None, amax=None) == fp4.FP4_ERR_INVALID_ARG  # fresh amax needs amax_out
+    # the UE5M3 shift by-product exists for UE5M3 scales only (checked before any launch)
+    for f in (0, 2, 3):
+        assert q(f=f, shift=P) == fp4.FP4_ERR_UNSUPPORTED
+        assert lib_dual(f=f, shift=P) == fp4.FP4_ERR_UNSUPPORTED
+
+
+def lib_dual(**kw):
+    lib = _need_lib()
+    a = dict(f=0, M=64, K=64, shift=None)
+    a.update(kw)
+    return lib.fp4_quantize_dual(P, a["M"], a["K"], a["K"], a["f"], 0, 0, 0, 0, P, 0, P, P, P, P, None, a["shift"],
+                                 None, None)
 
 
 def test_gemm_argument_errors():
@@ -100,6 +112,7 @@ def test_gemm_argument_errors():
     assert g(f=3) == fp4.FP4_ERR_UNSUPPORTED              # E1M6 has no GEMM
     assert g(f=1) == fp4.FP4_ERR_INVALID_ARG              # UE5M3 needs tA, tB
     assert g(M=100) == fp4.FP4_ERR_SHAPE
+    assert g(N=192, ldc=192) == fp4.FP4_ERR_SHAPE          # N must be a multiple of 128
     assert g(K=128) == fp4.FP4_ERR_SHAPE
     assert g(ldc=100) == fp4.FP4_ERR_SHAPE
     assert g(A=P + 1) == fp4.FP4_ERR_ALIGNMENT
@@ -118,13 +131,15 @@ def test_gemv_and_misc_argument_errors():
     assert lib.fp4_dequantize(P, P, 0, 4, 24, 0, P, 0, P, None) == fp4.FP4_ERR_SHAPE
     assert lib.fp4_ue5m3_to_e4m3(P, 16, None, P, None, None) == fp4.FP4_ERR_INVALID_ARG
     assert lib.fp4_ue5m3_windows(P, 16, P, None, P, None, None) == fp4.FP4_ERR_INVALID_ARG
+    assert lib.fp4_ue5m3_reencode(P, 16, None, P, None, None) == fp4.FP4_ERR_INVALID_ARG
+    assert lib.fp4_ue5m3_reencode(P, -1, P, P, None, None) == fp4.FP4_ERR_SHAPE
     assert lib.fp4_ue5m3_windows(P, -1, P, P, P, None, None) == fp4.FP4_ERR_SHAPE
     w = lambda M=256, N=256, K=256, A=P, C=P, ldc=256, nA=P: lib.fp4_gemm_ue5m3_windows(
         A, P, P, nA, P, P, P, P, P, P, M, N, K, C, ldc, None, None)
     assert w(nA=None) == fp4.FP4_ERR_INVALID_ARG
     assert w(C=None) == fp4.FP4_ERR_INVALID_ARG
     assert w(M=100) == fp4.FP4_ERR_SHAPE
-    assert w(N=128) == fp4.FP4_ERR_SHAPE
+    assert w(N=192) == fp4.FP4_ERR_SHAPE
     assert w(ldc=100) == fp4.FP4_ERR_SHAPE
     assert w(A=P + 1) == fp4.FP4_ERR_ALIGNMENT
     assert w(ldc=258) == fp4.FP4_ERR_ALIGNMENT           # 1032-byte float32 rows
@@ -141,7 +156,6 @@ def test_sweep_formats_rows_only():
     for f in (fp4.FP4_SF_E2M5, fp4.FP4_SF_E3M4, fp4.FP4_SF_E5M2, fp4.FP4_SF_E6M1, fp4.FP4_SF_E7M0,
               fp4.FP4_SF_NVINT4):
         assert q(f=f, tr=1) == fp4.FP4_ERR_UNSUPPORTED
-        assert lib.fp4_quantize_dual(P, 64, 64, 64, f, 0, 0, 0, 0, P, 0, P, P, P, P, None, None,
-                                     None) == fp4.FP4_ERR_UNSUPPORTED
+        assert lib_dual(f=f) == fp4.FP4_ERR_UNSUPPORTED
         assert lib.fp4_gemm(P, P, P, P, P, P, None, None, 128, 256, 256, f, 0, 0, P, 256, None,
                             None) == fp4.FP4_ERR_UNSUPPORTED
