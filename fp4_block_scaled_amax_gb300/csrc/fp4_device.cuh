@@ -43,10 +43,22 @@ __device__ __forceinline__ uint32_t absmax2(uint32_t a, uint32_t b) {
   __nv_bfloat162 m = __hmax2(x, y);
   return *reinterpret_cast<uint32_t*>(&m);
 }
-__device__ __forceinline__ float absmax_words(const uint32_t* w, int n) {
-  uint32_t m = w[0] & 0x7FFF7FFFu;
+// max(|a|, |b|) per bf16 half; the sign bits of the result are the XOR of the
+// inputs' signs and are cleared by the caller once at the end.
+__device__ __forceinline__ uint32_t absmax2_xs(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+// Packed magnitude maxima of n words (each half separately), sign bits clear.
+__device__ __forceinline__ uint32_t absmax_words2(const uint32_t* w, int n) {
+  uint32_t m = w[0];
 #pragma unroll
-  for (int i = 1; i < n; ++i) m = absmax2(m, w[i] & 0x7FFF7FFFu);
+  for (int i = 1; i < n; ++i) m = absmax2_xs(m, w[i]);
+  return m & 0x7FFF7FFFu;
+}
+__device__ __forceinline__ float absmax_words(const uint32_t* w, int n) {
+  const uint32_t m = absmax_words2(w, n);
   return fmaxf(bf16_lo(m), bf16_hi(m));
 }
 
@@ -251,36 +263,39 @@ __device__ __forceinline__ uint32_t e2m1x2_rne(float lo, float hi) {
   return r;
 }
 
-// Stochastic rounding of one value with a 16-bit draw r: lo <= |y| < hi the
-// neighbouring grid values, round up iff r < 65536 * (|y| - lo) / (hi - lo);
-// |y| >= 6 gives 6.  Written on the float pipe, returning the rounded grid
-// value with the sign of x (the caller converts exact grid values to codes):
-//  * the grid step around |y| is 2^(k-1) with k = clamp(floor(log2|y|), 0, 2);
-//    z = |y| * 2^(1-k) is exact and puts the step at 1;
-//  * with rho = r * 2^-16, "up" is frac(z) > rho, so the rounded value in
-//    step units is ceil(z - rho).  z - rho rounded once to float32 (one fma)
-//    has the same ceiling: next to an integer n >= 1 the difference is a
-//    multiple of ulp(z), larger than half an ulp of n, and below 1 it is exact
-//    (or lies in (-1, 0], whose ceiling is 0 either way);
-//  * ceil of t in (-1, 2^22) is (t + 1.5*2^23 rounded up) - 1.5*2^23, both
-//    steps exact; larger t (and +Inf) only ever saturate.
-// All of it runs scaled by the step s = 2^(k-1) (exact for these magnitudes):
-// t*s = |y| - rho*s in one fma, then (t*s + 1.5*2^23*s rounded up) -
-// 1.5*2^23*s = ceil(t)*s, the grid value itself, so only the sign remains to
-// be attached.  The value is a grid value, or 8 and above, which the
-// saturating E2M1 conversion maps to 6.  A zero result keeps the sign of x.
-// rbits is the float32 pattern of 1 + r * 2^-23 (0x3F800000 | r), so
-// rho * s = (rbits - 1) * 2^(k+6).
-__device__ __forceinline__ float e2m1_sr_value(float x, float r, uint32_t rbits) {
+// Stochastic rounding of one value with a 16-bit draw R (reading R8): with
+// lo <= |y| < hi the neighbouring grid values, round up iff
+// R < 65536 * (|y| - lo) / (hi - lo); |y| >= 6 gives 6.  Returns the rounded
+// grid value with the sign of x (the caller converts exact grid values to
+// codes).  It is a carry into the grid-step bit:
+//  * for 1 <= |y| < 8 the E2M1 step is 2^(e-1) with e the binary exponent of
+//    |y|, i.e. bit 22 of its float32 pattern, and f = (|y| - lo)/step is the
+//    22-bit field m below it over 2^22; "R < 65536 f" is "m > 64 R" (R is an
+//    integer), i.e. m + (2^22 - 1 - 64 R) carries into bit 22.  So adding
+//    d = 0x3FFFFF - 64 R and clearing the 22 low bits gives lo or hi; a carry
+//    out of the mantissa moves into the exponent by itself (1.5 -> 2,
+//    3 -> 4, 6 -> 8, which the saturating conversion maps to 6);
+//  * below 1 the step is 0.5 at every magnitude: |y| + 1 rounded up to
+//    float32 lies in [1, 2], where the step sits at bit 22 again, and the
+//    rounding up keeps the decision exact (the threshold lo + 64 R * 2^-23
+//    lies on the float32 grid there, so ceil(|y| + 1) exceeds it iff |y| + 1
+//    does); the same carry then gives 1 + {0, 0.5, 1}, and subtracting the 1
+//    is exact;
+//  * |y| = 0 (a zero block) stays 0; +Inf (|y| overflowed) stays +Inf.
+// d is computed by the caller from the draw (sr_d_lo / sr_d_hi).
+__device__ __forceinline__ float e2m1_sr_value(float x, float r, uint32_t d) {
   const float ay = __fmul_rn(fabsf(x), r);
-  const uint32_t eb = min(max(__float_as_uint(ay) & 0x7F800000u, 0x3F800000u), 0x40800000u);  // 2^k
-  const float s7 = __uint_as_float(eb + (6u << 23));                                           // 2^(k+6)
-  const float rho = __fsub_rn(__uint_as_float(rbits), 1.0f);                                   // r * 2^-23
-  const float t = __fmaf_rn(-rho, s7, ay);
-  const float cs = __fmul_rn(s7, 98304.0f);                                                    // 1.5*2^23*s
-  const float c = __fsub_rn(__fadd_ru(t, cs), cs);
-  return __uint_as_float(__float_as_uint(c) | (__float_as_uint(x) & 0x80000000u));
+  float off;  // 1.0 below 1, else 0.0
+  asm("set.lt.f32.f32 %0, %1, 0f3F800000;" : "=f"(off) : "f"(ay));
+  const float v = __fadd_ru(ay, off);
+  const float q = __uint_as_float((__float_as_uint(v) + d) & 0xFFC00000u);
+  const float m = __fsub_rn(q, off);
+  return __uint_as_float(__float_as_uint(m) | (__float_as_uint(x) & 0x80000000u));
 }
+// The carry constant d = 0x3FFFFF - 64 R of the low and the high 16-bit draw
+// R of a Philox word.
+__device__ __forceinline__ uint32_t sr_d_lo(uint32_t w) { return ((~w & 0xFFFFu) << 6) | 63u; }
+__device__ __forceinline__ uint32_t sr_d_hi(uint32_t w) { return ((~w >> 10) & 0x3FFFC0u) | 63u; }
 // INT4 grid (integers -7..7, two's-complement nibble): nearest with ties to
 // even after clamping to [-7, 7]; adding 1.5 * 2^23 rounds to an integer in
 // float32 and leaves it in the low mantissa bits.
@@ -302,7 +317,8 @@ __device__ __forceinline__ uint32_t int4_sr(float x, float r, uint32_t rbits) {
 }
 
 // 1 + r * 2^-23 (float32 bits 0x3F800000 | r) for the low and high 16-bit
-// halves r of a Philox word: one byte permute each.
+// halves r of a Philox word (the INT4 grid's stochastic rounding): one byte
+// permute each.
 __device__ __forceinline__ uint32_t sr_rbits_lo(uint32_t w) { return __byte_perm(w, 0x3F800000u, 0x7610u); }
 __device__ __forceinline__ uint32_t sr_rbits_hi(uint32_t w) { return __byte_perm(w, 0x3F800000u, 0x7632u); }
 
@@ -319,12 +335,13 @@ __device__ __forceinline__ uint4 philox4x32_10(uint32_t c0, uint32_t c1, uint32_
       k0 += 0x9E3779B9u;
       k1 += 0xBB67AE85u;
     }
-    const uint32_t hi0 = __umulhi(0xD2511F53u, c0), lo0 = 0xD2511F53u * c0;
-    const uint32_t hi1 = __umulhi(0xCD9E8D57u, c2), lo1 = 0xCD9E8D57u * c2;
-    c0 = hi1 ^ c1 ^ k0;
-    c1 = lo1;
-    c2 = hi0 ^ c3 ^ k1;
-    c3 = lo0;
+    // one 32 x 32 -> 64-bit multiply gives both halves of each product
+    const uint64_t p0 = (uint64_t)0xD2511F53u * c0;
+    const uint64_t p1 = (uint64_t)0xCD9E8D57u * c2;
+    c0 = (uint32_t)(p1 >> 32) ^ c1 ^ k0;
+    c1 = (uint32_t)p1;
+    c2 = (uint32_t)(p0 >> 32) ^ c3 ^ k1;
+    c3 = (uint32_t)p0;
   }
   return make_uint4(c0, c1, c2, c3);
 }
@@ -405,8 +422,32 @@ __device__ __forceinline__ uint2 quant16(const uint32_t* w, float r, uint64_t se
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const uint32_t wi = w[4 * h + i];
-        y[8 * h + 2 * i] = e2m1_sr_value(bf16_lo(wi), r, sr_rbits_lo(dw[i]));
-        y[8 * h + 2 * i + 1] = e2m1_sr_value(bf16_hi(wi), r, sr_rbits_hi(dw[i]));
+        y[8 * h + 2 * i] = e2m1_sr_value(bf16_lo(wi), r, sr_d_lo(dw[i]));
+        y[8 * h + 2 * i + 1] = e2m1_sr_value(bf16_hi(wi), r, sr_d_hi(dw[i]));
+      }
+    }
+  }
+  return make_uint2(e2m1x8_rne(y), e2m1x8_rne(y + 8));
+}
+
+// quant16 of one column of a 16-row block held as 16 words, each a row's
+// pair of neighbouring columns: HI selects the high (odd) column.
+template <bool SR, bool HI>
+__device__ __forceinline__ uint2 quant16_col(const uint32_t (&v)[16], float r, uint64_t seed, uint64_t idx0) {
+  float y[16];
+  if constexpr (!SR) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) y[i] = __fmul_rn(HI ? bf16_hi(v[i]) : bf16_lo(v[i]), r);
+  } else {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const uint4 d = sr_draws8(seed, (idx0 >> 3) + h);
+      const uint32_t dw[4] = {d.x, d.y, d.z, d.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint32_t a = v[8 * h + 2 * i], b = v[8 * h + 2 * i + 1];
+        y[8 * h + 2 * i] = e2m1_sr_value(HI ? bf16_hi(a) : bf16_lo(a), r, sr_d_lo(dw[i]));
+        y[8 * h + 2 * i + 1] = e2m1_sr_value(HI ? bf16_hi(b) : bf16_lo(b), r, sr_d_hi(dw[i]));
       }
     }
   }
@@ -476,8 +517,8 @@ __device__ __forceinline__ uint2 quant16f(const float (&v)[16], float r, uint64_
       const uint32_t dw[4] = {d.x, d.y, d.z, d.w};
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        y[8 * h + 2 * i] = e2m1_sr_value(v[8 * h + 2 * i], r, sr_rbits_lo(dw[i]));
-        y[8 * h + 2 * i + 1] = e2m1_sr_value(v[8 * h + 2 * i + 1], r, sr_rbits_hi(dw[i]));
+        y[8 * h + 2 * i] = e2m1_sr_value(v[8 * h + 2 * i], r, sr_d_lo(dw[i]));
+        y[8 * h + 2 * i + 1] = e2m1_sr_value(v[8 * h + 2 * i + 1], r, sr_d_hi(dw[i]));
       }
     }
   }

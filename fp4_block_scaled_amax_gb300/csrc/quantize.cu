@@ -23,6 +23,8 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include "async_sm103.cuh"
+#include "device_cache.h"
 #include "fp4_device.cuh"
 #include "launch.h"
 
@@ -68,12 +70,13 @@ __global__ void __launch_bounds__(256) k_amax(const uint16_t* __restrict__ x, in
       v[u] = i + u * stride < total ? ld_stream(addr(i + u * stride)) : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
-      m = absmax2(m, v[u].x & 0x7FFF7FFFu);
-      m = absmax2(m, v[u].y & 0x7FFF7FFFu);
-      m = absmax2(m, v[u].z & 0x7FFF7FFFu);
-      m = absmax2(m, v[u].w & 0x7FFF7FFFu);
+      m = absmax2_xs(m, v[u].x);
+      m = absmax2_xs(m, v[u].y);
+      m = absmax2_xs(m, v[u].z);
+      m = absmax2_xs(m, v[u].w);
     }
   }
+  m &= 0x7FFF7FFFu;  // the packed maxima carry XOR-ed signs
   float a = fmaxf(bf16_lo(m), bf16_hi(m));
   unsigned int ab = __reduce_max_sync(0xFFFFFFFFu, __float_as_uint(a));
   __shared__ unsigned int warp_max[8];
@@ -270,6 +273,243 @@ __global__ void __launch_bounds__(256) k_quant_tile(
   } else {
     scales_col[MMA ? mma_sf_offset(c, b, nb) : c * nb + b] = (uint8_t)sc0;
   }
+}
+
+// ---------------------------------------------------------------------------
+// K3': persistent TMA-fed dual / transposed quantizer (tiled scale layout)
+// ---------------------------------------------------------------------------
+// One CTA per SM walks 128 x 128 tiles of x (M fastest).  Warp 0 streams
+// each tile into a 4-stage ring of 32 KB stages with two TMA loads (64-column
+// boxes, 128-byte swizzle: 16-byte chunk j of row r sits at chunk j ^ (r % 8));
+// sixteen consumer warps quantize it; warp 17 writes the staged outputs.
+//   row pass   thread (warp w, lane l) takes row 8w + l % 8 and the 16-column
+//              chunks 4j + l / 8 (j = 0, 1): two 16-byte loads each, eight
+//              lanes on eight rows of one chunk (no bank conflict); its 8 code
+//              bytes go straight to global memory (the four chunks of a row in
+//              one instruction fill a 32-byte sector);
+//   col pass   warp w takes box w / 8 and rows 16 (w % 8) .. +15; lane l reads
+//              the 32-bit word of columns 2l, 2l + 1 in each of the 16 rows
+//              (a whole 128-byte row per instruction) and quantizes both
+//              columns' 16-row blocks;
+// the transposed codes (128 output rows x 64 bytes, 64-byte swizzle: chunk j
+// of row c at j ^ ((c / 2) % 4)) and both scale sets (for a 128 x 128 tile,
+// the row scales of rows m0.. and the transposed scales of columns k0.. are
+// each two whole 512-byte atoms of the tiled layout, contiguous in memory)
+// are staged in shared memory and written by one TMA tensor store and two
+// bulk copies.  Staging is double-buffered.  Every wait is bounded.
+constexpr int QD_T = 128;                    // tile rows = tile columns
+constexpr int QD_STAGES = 4;
+constexpr int QD_CONSUMERS = 16;             // warps
+constexpr int QD_THREADS = 32 * (QD_CONSUMERS + 2);
+constexpr int QD_STAGE_BYTES = QD_T * QD_T * 2;  // 32 KB of bf16
+constexpr int QD_COLC_BYTES = QD_T * QD_T / 2;   // 8 KB of transposed codes
+constexpr int QD_SF_BYTES = QD_T * QD_T / 16;    // 1 KB of scales per layout
+constexpr int QD_STG_BYTES = QD_COLC_BYTES + 2 * QD_SF_BYTES;
+constexpr int QD_SMEM_STAGES = 0;
+constexpr int QD_SMEM_STG = QD_SMEM_STAGES + QD_STAGES * QD_STAGE_BYTES;
+constexpr int QD_SMEM_RTAB = QD_SMEM_STG + 2 * QD_STG_BYTES;
+constexpr int QD_SMEM_BAR = QD_SMEM_RTAB + 256 * 4;
+constexpr int QD_SMEM_TOTAL = QD_SMEM_BAR + 8 * (2 * QD_STAGES + 4) + 16;
+constexpr int QD_SMEM_LAUNCH = QD_SMEM_TOTAL + 1024;  // base aligned up to 1024
+static_assert(QD_SMEM_STG % 1024 == 0 && QD_STG_BYTES % 1024 == 0, "swizzled buffers need 1024-byte alignment");
+
+struct QdParams {
+  const float* gptr;
+  uint64_t seed_row, seed_col;
+  int64_t M, K;
+  uint8_t* codes_row;
+  uint8_t* scales_row;
+  uint8_t* scales_col;
+  float* amax_out;
+  int32_t* status;
+  uint32_t* sf_max_row;
+  uint32_t* sf_max_col;
+};
+
+__device__ __forceinline__ void qd_tma_store_2d(const CUtensorMap* map, uint32_t src, int x, int y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(src), "r"(x), "r"(y)
+               : "memory");
+}
+__device__ __forceinline__ void qd_bulk_store(void* dst, uint32_t src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src), "r"(bytes)
+               : "memory");
+}
+// scale (row r, block b) of a 128-row x 8-block tile inside its two atoms
+__device__ __forceinline__ int qd_sf_off(int r, int b) { return (b >> 2) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4 + (b & 3); }
+
+template <int FMT, bool DO_ROW, bool ROW_SR, bool COL_SR, bool AMAX>
+__global__ void __launch_bounds__(QD_THREADS, 1)
+    k_quant_dual_tma(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_ccol,
+                     QdParams p) {
+  using namespace fp4async;
+  static_assert(ScaleFmt<FMT>::G == 16, "16-element blocks only");
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  float* rtab = reinterpret_cast<float*>(smem + QD_SMEM_RTAB);
+  const uint32_t bar_full = sbase + QD_SMEM_BAR;
+  const uint32_t bar_empty = bar_full + 8 * QD_STAGES;
+  const uint32_t bar_stg_full = bar_empty + 8 * QD_STAGES;  // [2]
+  const uint32_t bar_stg_free = bar_stg_full + 16;          // [2]
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + QD_SMEM_BAR + 8 * (2 * QD_STAGES + 4));
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int m_tiles = (int)(p.M / QD_T), k_tiles = (int)(p.K / QD_T);
+  const int ntiles = m_tiles * k_tiles;
+  const float s_enc =
+      global_encode_scale<FMT>(__ldg(p.gptr), (blockIdx.x == 0 && threadIdx.x == 0) ? p.status : nullptr);
+  if (threadIdx.x < 256) rtab[threadIdx.x] = code_multiplier<FMT>(threadIdx.x, s_enc);
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < QD_STAGES; ++s) {
+      mbar_init(bar_full + 8 * s, 1);
+      mbar_init(bar_empty + 8 * s, QD_CONSUMERS);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar_stg_full + 8 * b, QD_CONSUMERS);
+      mbar_init(bar_stg_free + 8 * b, 1);
+    }
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  __syncthreads();
+
+  if (warp == 0) {
+    // ------------------------------ producer ------------------------------
+    if (lane == 0) {
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_x)) : "memory");
+      int it = 0;
+      for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++it) {
+        const int s = it % QD_STAGES;
+        if (it >= QD_STAGES &&
+            !wait_bounded(bar_empty + 8 * s, ((it / QD_STAGES) - 1) & 1, abort_flag, p.status))
+          break;
+        if (*abort_flag) break;
+        const int m0 = (t % m_tiles) * QD_T, k0 = (t / m_tiles) * QD_T;
+        const uint32_t fb = bar_full + 8 * s, dst = sbase + QD_SMEM_STAGES + s * QD_STAGE_BYTES;
+        mbar_expect_tx(fb, QD_STAGE_BYTES);
+        tma_load_2d(dst, &tm_x, fb, k0, m0);
+        tma_load_2d(dst + QD_STAGE_BYTES / 2, &tm_x, fb, k0 + 64, m0);
+      }
+    }
+  } else if (warp <= QD_CONSUMERS) {
+    // ------------------------------ consumers -----------------------------
+    const int cw = warp - 1;
+    float amax_local = 0.0f;
+    uint32_t maxc_row = 0, maxc_col = 0;
+    // row pass: row 8 cw + l % 8, chunks 4 j + l / 8
+    const int rr = 8 * cw + (lane & 7), rq = lane >> 3;
+    // col pass: box cw / 8, row block cw % 8, columns 2 l, 2 l + 1 of the box
+    const int cbox = cw >> 3, crb = cw & 7;
+    int it = 0;
+    for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++it) {
+      const int s = it % QD_STAGES, b = it & 1;
+      const int m0 = (t % m_tiles) * QD_T, k0 = (t / m_tiles) * QD_T;
+      if (!wait_lane0(bar_full + 8 * s, (it / QD_STAGES) & 1, abort_flag, p.status, lane)) break;
+      if ((it >> 1) > 0 && !wait_lane0(bar_stg_free + 8 * b, ((it >> 1) - 1) & 1, abort_flag, p.status, lane))
+        break;
+      const uint8_t* stage = smem + QD_SMEM_STAGES + s * QD_STAGE_BYTES;
+      uint8_t* stg = smem + QD_SMEM_STG + b * QD_STG_BYTES;
+      uint8_t* stg_colc = stg;
+      uint8_t* stg_sfr = stg + QD_COLC_BYTES;
+      uint8_t* stg_sfc = stg_sfr + QD_SF_BYTES;
+      if constexpr (DO_ROW) {
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          const int c = 4 * j + rq;  // 16-column chunk of the tile
+          const uint8_t* row = stage + j * (QD_STAGE_BYTES / 2) + rr * 128;
+          const uint4 v0 = *reinterpret_cast<const uint4*>(row + (((2 * rq) ^ (rr & 7)) << 4));
+          const uint4 v1 = *reinterpret_cast<const uint4*>(row + (((2 * rq + 1) ^ (rr & 7)) << 4));
+          const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+          const float a = absmax_words(w, 8);
+          amax_local = fmaxf(amax_local, a);
+          const BlockScale bs = block_scale_tab<FMT>(a, s_enc, rtab);
+          maxc_row = max(maxc_row, bs.code);
+          const int64_t grow = m0 + rr, gcol = k0 + 16 * c;
+          const uint2 q = quant16<ROW_SR>(w, bs.r, p.seed_row, (uint64_t)(grow * p.K + gcol));
+          *reinterpret_cast<uint2*>(p.codes_row + grow * (p.K / 2) + gcol / 2) = q;
+          stg_sfr[qd_sf_off(rr, c)] = (uint8_t)bs.code;
+        }
+      }
+      {
+        uint32_t v[16];
+        const uint8_t* box = stage + cbox * (QD_STAGE_BYTES / 2);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int r = 16 * crb + i;
+          v[i] = *reinterpret_cast<const uint32_t*>(box + r * 128 + (((lane >> 2) ^ (r & 7)) << 4) + (lane & 3) * 4);
+        }
+        const uint32_t am2 = absmax_words2(v, 16);  // both columns' block maxima
+        const float a_lo = bf16_lo(am2), a_hi = bf16_hi(am2);
+        if constexpr (!DO_ROW) amax_local = fmaxf(amax_local, fmaxf(a_lo, a_hi));
+        const BlockScale b0 = block_scale_tab<FMT>(a_lo, s_enc, rtab);
+        const BlockScale b1 = block_scale_tab<FMT>(a_hi, s_enc, rtab);
+        maxc_col = max(maxc_col, max(b0.code, b1.code));
+        const int c0 = 64 * cbox + 2 * lane;  // tile column of the low half
+        const uint64_t i0 = (uint64_t)(k0 + c0) * (uint64_t)p.M + (uint64_t)(m0 + 16 * crb);
+        const uint2 q0 = quant16_col<COL_SR, false>(v, b0.r, p.seed_col, i0);
+        const uint2 q1 = quant16_col<COL_SR, true>(v, b1.r, p.seed_col, i0 + (uint64_t)p.M);
+        // staged transposed codes: output row c, bytes 8 crb .. +7 (64-byte swizzle)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int c = c0 + h;
+          *reinterpret_cast<uint2*>(stg_colc + c * 64 + (((crb >> 1) ^ ((c >> 1) & 3)) << 4) + (crb & 1) * 8) =
+              h ? q1 : q0;
+        }
+        stg_sfc[qd_sf_off(c0, crb)] = (uint8_t)b0.code;
+        stg_sfc[qd_sf_off(c0 + 1, crb)] = (uint8_t)b1.code;
+      }
+      // the stage may refill; the staged outputs go to the async proxy
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(bar_empty + 8 * s);
+        mbar_arrive(bar_stg_full + 8 * b);
+      }
+    }
+    if constexpr (AMAX) {
+      const unsigned int am = __reduce_max_sync(0xFFFFFFFFu, __float_as_uint(amax_local));
+      if (lane == 0) atomicMax(reinterpret_cast<unsigned int*>(p.amax_out), am);
+    }
+    if constexpr (FMT == SF_UE5M3) {
+      if (DO_ROW && p.sf_max_row != nullptr) {
+        const unsigned int mc = __reduce_max_sync(0xFFFFFFFFu, maxc_row);
+        if (lane == 0) atomicMax(p.sf_max_row, mc);
+      }
+      if (p.sf_max_col != nullptr) {
+        const unsigned int mc = __reduce_max_sync(0xFFFFFFFFu, maxc_col);
+        if (lane == 0) atomicMax(p.sf_max_col, mc);
+      }
+    }
+  } else {
+    // ------------------------------ storer --------------------------------
+    if (lane == 0) {
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_ccol)) : "memory");
+      int it = 0;
+      for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++it) {
+        const int b = it & 1;
+        if (!wait_bounded(bar_stg_full + 8 * b, (it >> 1) & 1, abort_flag, p.status)) break;
+        const int m0 = (t % m_tiles) * QD_T, k0 = (t / m_tiles) * QD_T;
+        const uint32_t stg = sbase + QD_SMEM_STG + b * QD_STG_BYTES;
+        qd_tma_store_2d(&tm_ccol, stg, m0 / 2, k0);
+        if (DO_ROW)
+          qd_bulk_store(p.scales_row + ((int64_t)(m0 / QD_T) * (p.K / 64) + k0 / 64) * 512, stg + QD_COLC_BYTES,
+                        QD_SF_BYTES);
+        qd_bulk_store(p.scales_col + ((int64_t)(k0 / QD_T) * (p.M / 64) + m0 / 64) * 512,
+                      stg + QD_COLC_BYTES + QD_SF_BYTES, QD_SF_BYTES);
+        asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+        // the staging buffer is free once these copies have read it
+        asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+        mbar_arrive(bar_stg_free + 8 * b);
+      }
+      asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+    }
+  }
+  __syncwarp();
+  __syncthreads();
+  drain_after_abort(abort_flag);
 }
 
 // ---------------------------------------------------------------------------
@@ -472,6 +712,85 @@ static void tile_t(const QuantArgs& a, cudaStream_t st) {
       a.scales_row, a.codes_col, a.scales_col, a.amax_out, a.status, a.sf_max_row, a.sf_max_col);
 }
 
+// The TMA-fed dual / transposed quantizer: 16-element blocks, tiled scale
+// layout, M and K multiples of 128.  cudaErrorNotSupported (before any
+// launch) sends the call to k_quant_tile instead.
+template <int FMT, bool DO_ROW, bool RSR, bool CSR, bool AM>
+static cudaError_t dual_tma_t(const QuantArgs& a, cudaStream_t st) {
+  auto fn = fp4async::encode_fn();
+  if (fn == nullptr) return cudaErrorNotSupported;
+  CUtensorMap mx, mc;
+  {
+    cuuint64_t dims[2] = {(cuuint64_t)a.K, (cuuint64_t)a.M};
+    cuuint64_t strides[1] = {(cuuint64_t)(a.ldx * 2)};
+    cuuint32_t box[2] = {64u, (cuuint32_t)QD_T};
+    cuuint32_t estr[2] = {1u, 1u};
+    if (fn(&mx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(a.x), dims, strides, box, estr,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorNotSupported;
+  }
+  {
+    cuuint64_t dims[2] = {(cuuint64_t)(a.M / 2), (cuuint64_t)a.K};
+    cuuint64_t strides[1] = {(cuuint64_t)(a.M / 2)};
+    cuuint32_t box[2] = {64u, (cuuint32_t)QD_T};
+    cuuint32_t estr[2] = {1u, 1u};
+    if (fn(&mc, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, a.codes_col, dims, strides, box, estr,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorNotSupported;
+  }
+  auto kern = k_quant_dual_tma<FMT, DO_ROW, RSR, CSR, AM>;
+  static fp4lib::DeviceInts attr_set;
+  cudaError_t e = cudaSuccess;
+  attr_set.get([&] {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, QD_SMEM_LAUNCH);
+    return e == cudaSuccess ? 1 : 0;
+  });
+  if (e != cudaSuccess) return e;
+  QdParams p{};
+  p.gptr = a.gptr;
+  p.seed_row = a.seed_row;
+  p.seed_col = a.seed_col;
+  p.M = a.M;
+  p.K = a.K;
+  p.codes_row = a.codes_row;
+  p.scales_row = a.scales_row;
+  p.scales_col = a.scales_col;
+  p.amax_out = a.amax_out;
+  p.status = a.status;
+  p.sf_max_row = a.sf_max_row;
+  p.sf_max_col = a.sf_max_col;
+  const int64_t tiles = (a.M / QD_T) * (a.K / QD_T);
+  const int sms = fp4lib::current_sm_count();
+  const unsigned grid = (unsigned)(tiles < sms ? tiles : sms);
+  kern<<<grid, QD_THREADS, QD_SMEM_LAUNCH, st>>>(mx, mc, p);
+  return cudaGetLastError();
+}
+
+template <int FMT>
+static cudaError_t dispatch_dual_tma(const QuantArgs& a, cudaStream_t st) {
+  if constexpr (ScaleFmt<FMT>::G != 16 || Elem<FMT>::INT4) {
+    return cudaErrorNotSupported;
+  } else {
+    if (!a.mma || a.M % QD_T != 0 || a.K % QD_T != 0 || a.M == 0 || a.K == 0) return cudaErrorNotSupported;
+    const bool amax = a.amax_by_product;
+    if (a.mode == QuantArgs::DUAL) {
+#define DT_CASE(RS, CS, AM) \
+  if (a.row_sr == RS && a.col_sr == CS && amax == AM) return dual_tma_t<FMT, true, RS, CS, AM>(a, st);
+      DT_CASE(false, false, false) DT_CASE(false, false, true) DT_CASE(false, true, false) DT_CASE(false, true, true)
+      DT_CASE(true, false, false) DT_CASE(true, false, true) DT_CASE(true, true, false) DT_CASE(true, true, true)
+#undef DT_CASE
+    } else if (a.mode == QuantArgs::COLS) {
+      if (a.col_sr && amax) return dual_tma_t<FMT, false, false, true, true>(a, st);
+      if (a.col_sr) return dual_tma_t<FMT, false, false, true, false>(a, st);
+      if (amax) return dual_tma_t<FMT, false, false, false, true>(a, st);
+      return dual_tma_t<FMT, false, false, false, false>(a, st);
+    }
+    return cudaErrorNotSupported;
+  }
+}
+
 // runtime -> template dispatch
 template <int FMT>
 static void dispatch_fmt(const QuantArgs& a, cudaStream_t st) {
@@ -514,7 +833,17 @@ static cudaError_t dispatch_rows_only(const QuantArgs& a, cudaStream_t st) {
 }
 
 cudaError_t launch_quantize(const QuantArgs& a, cudaStream_t st) {
-  cudaError_t e = cudaSuccess;
+  cudaError_t e = cudaErrorNotSupported;
+  if (a.mode != QuantArgs::ROWS) {
+    switch (a.fmt) {
+      case FP4_SF_E4M3: e = dispatch_dual_tma<SF_E4M3>(a, st); break;
+      case FP4_SF_UE5M3: e = dispatch_dual_tma<SF_UE5M3>(a, st); break;
+      case FP4_SF_E1M6: e = dispatch_dual_tma<SF_E1M6>(a, st); break;
+      default: break;
+    }
+    if (e != cudaErrorNotSupported) return e;
+  }
+  e = cudaSuccess;
   switch (a.fmt) {
     case FP4_SF_E4M3: dispatch_fmt<SF_E4M3>(a, st); break;
     case FP4_SF_UE5M3: dispatch_fmt<SF_UE5M3>(a, st); break;
