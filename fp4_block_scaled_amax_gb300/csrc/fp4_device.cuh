@@ -218,20 +218,39 @@ __device__ __forceinline__ float code_multiplier(uint32_t code, float s_enc) {
   return (s_b == 0.0f) ? 0.0f : __fdiv_rn(s_enc, s_b);
 }
 
+// f32(a / D) for D = 6 or 7 and a block maximum a that is a bf16 value (at
+// most 8 significant bits): q0 = f32(a * f32(1/D)), the exact residual
+// a - D q0 by one fma, and q0 + residual * f32(1/D) by another equal the
+// correctly rounded quotient for every 8-bit significand (checked
+// exhaustively); the binade only scales the result while it stays normal, so
+// small a takes the division itself.
+template <int D>
+__device__ __forceinline__ float div_small_exact(float a) {
+  static_assert(D == 6 || D == 7, "divisor");
+  if (!(a >= 7.8886091e-31f)) return __fdiv_rn(a, (float)D);  // below 2^-100 (and zero)
+  const float c = D == 6 ? __uint_as_float(0x3E2AAAABu) : __uint_as_float(0x3E124925u);  // f32(1/D)
+  const float q0 = __fmul_rn(a, c);
+  const float res = __fmaf_rn(-(float)D, q0, a);
+  return __fmaf_rn(res, c, q0);
+}
+
 // Block scale with the multiplier looked up in a per-CTA table of all codes.
-template <int FMT>
+// BF16_AMAX: a_b is a bf16 value (the block maximum of bf16 inputs), so the
+// division by the grid maximum takes div_small_exact.
+template <int FMT, bool BF16_AMAX = false>
 __device__ __forceinline__ BlockScale block_scale_tab(float a_b, float s_enc, const float* rtab) {
   BlockScale out;
   if constexpr (e8m0_scales<FMT>()) {
     out.code = ScaleFmt<SF_E8M0>::encode_from_amax(a_b);
   } else {
-    out.code = ScaleFmt<FMT>::encode(__fmul_rn(__fdiv_rn(a_b, elem_max<FMT>()), s_enc));
+    const float a6 = BF16_AMAX ? div_small_exact<(int)elem_max<FMT>()>(a_b) : __fdiv_rn(a_b, elem_max<FMT>());
+    out.code = ScaleFmt<FMT>::encode(__fmul_rn(a6, s_enc));
   }
   out.r = rtab[out.code];
   return out;
 }
 
-template <int FMT>
+template <int FMT, bool BF16_AMAX = false>
 __device__ __forceinline__ BlockScale block_scale(float a_b, float s_enc) {
   BlockScale out;
   float s_b;
@@ -239,7 +258,8 @@ __device__ __forceinline__ BlockScale block_scale(float a_b, float s_enc) {
     out.code = ScaleFmt<SF_E8M0>::encode_from_amax(a_b);
     s_b = ScaleFmt<SF_E8M0>::decode(out.code);
   } else {
-    const float s_real = __fmul_rn(__fdiv_rn(a_b, elem_max<FMT>()), s_enc);
+    const float a6 = BF16_AMAX ? div_small_exact<(int)elem_max<FMT>()>(a_b) : __fdiv_rn(a_b, elem_max<FMT>());
+    const float s_real = __fmul_rn(a6, s_enc);
     out.code = ScaleFmt<FMT>::encode(s_real);
     s_b = ScaleFmt<FMT>::decode(out.code);
   }
@@ -285,17 +305,18 @@ __device__ __forceinline__ uint32_t e2m1x2_rne(float lo, float hi) {
 // d is computed by the caller from the draw (sr_d_lo / sr_d_hi).
 __device__ __forceinline__ float e2m1_sr_value(float x, float r, uint32_t d) {
   const float ay = __fmul_rn(fabsf(x), r);
-  float off;  // 1.0 below 1, else 0.0
-  asm("set.lt.f32.f32 %0, %1, 0f3F800000;" : "=f"(off) : "f"(ay));
+  // 1.0 below 1, else 0.0: saturate(2^24 (1 - ay)) (exact: 1 - ay >= 2^-24 below 1)
+  float off;
+  asm("fma.rn.sat.f32 %0, %1, 0fCB800000, 0f4B800000;" : "=f"(off) : "f"(ay));
   const float v = __fadd_ru(ay, off);
   const float q = __uint_as_float((__float_as_uint(v) + d) & 0xFFC00000u);
   const float m = __fsub_rn(q, off);
   return __uint_as_float(__float_as_uint(m) | (__float_as_uint(x) & 0x80000000u));
 }
 // The carry constant d = 0x3FFFFF - 64 R of the low and the high 16-bit draw
-// R of a Philox word.
-__device__ __forceinline__ uint32_t sr_d_lo(uint32_t w) { return ((~w & 0xFFFFu) << 6) | 63u; }
-__device__ __forceinline__ uint32_t sr_d_hi(uint32_t w) { return ((~w >> 10) & 0x3FFFC0u) | 63u; }
+// R of a Philox word (one multiply-add each).
+__device__ __forceinline__ uint32_t sr_d_lo(uint32_t w) { return (w & 0xFFFFu) * 0xFFFFFFC0u + 0x3FFFFFu; }
+__device__ __forceinline__ uint32_t sr_d_hi(uint32_t w) { return (w >> 16) * 0xFFFFFFC0u + 0x3FFFFFu; }
 // INT4 grid (integers -7..7, two's-complement nibble): nearest with ties to
 // even after clamping to [-7, 7]; adding 1.5 * 2^23 rounds to an integer in
 // float32 and leaves it in the low mantissa bits.
@@ -327,6 +348,34 @@ __device__ __forceinline__ uint32_t sr_rbits_hi(uint32_t w) { return __byte_perm
 // (c0,c1,c2,c3) -> (hi(M1*c2)^c1^k0, lo(M1*c2), hi(M0*c0)^c3^k1, lo(M0*c0)),
 // the key advanced by the Weyl constants between rounds.
 // ---------------------------------------------------------------------------
+// The ten round keys of a seed (key = (seed low, seed high), advanced by the
+// Weyl constants), computed once per thread where it draws many times.
+struct PhiloxKey {
+  uint32_t k0[10], k1[10];
+  __device__ __forceinline__ explicit PhiloxKey(uint64_t seed) {
+    uint32_t a = (uint32_t)seed, b = (uint32_t)(seed >> 32);
+#pragma unroll
+    for (int i = 0; i < 10; ++i) {
+      k0[i] = a;
+      k1[i] = b;
+      a += 0x9E3779B9u;
+      b += 0xBB67AE85u;
+    }
+  }
+};
+__device__ __forceinline__ uint4 philox4x32_10(uint32_t c0, uint32_t c1, uint32_t c2, uint32_t c3,
+                                               const PhiloxKey& key) {
+#pragma unroll
+  for (int i = 0; i < 10; ++i) {
+    const uint64_t p0 = (uint64_t)0xD2511F53u * c0;
+    const uint64_t p1 = (uint64_t)0xCD9E8D57u * c2;
+    c0 = (uint32_t)(p1 >> 32) ^ c1 ^ key.k0[i];
+    c1 = (uint32_t)p1;
+    c2 = (uint32_t)(p0 >> 32) ^ c3 ^ key.k1[i];
+    c3 = (uint32_t)p0;
+  }
+  return make_uint4(c0, c1, c2, c3);
+}
 __device__ __forceinline__ uint4 philox4x32_10(uint32_t c0, uint32_t c1, uint32_t c2, uint32_t c3,
                                                uint32_t k0, uint32_t k1) {
 #pragma unroll
@@ -351,6 +400,9 @@ __device__ __forceinline__ uint4 philox4x32_10(uint32_t c0, uint32_t c1, uint32_
 __device__ __forceinline__ uint4 sr_draws8(uint64_t seed, uint64_t blk) {
   return philox4x32_10((uint32_t)blk, (uint32_t)(blk >> 32), 0u, 0u, (uint32_t)seed,
                        (uint32_t)(seed >> 32));
+}
+__device__ __forceinline__ uint4 sr_draws8(const PhiloxKey& key, uint64_t blk) {
+  return philox4x32_10((uint32_t)blk, (uint32_t)(blk >> 32), 0u, 0u, key);
 }
 __device__ __forceinline__ uint32_t draw16(const uint4& w, int j) {
   const uint32_t v = (j >> 1) == 0 ? w.x : (j >> 1) == 1 ? w.y : (j >> 1) == 2 ? w.z : w.w;
@@ -377,8 +429,8 @@ __device__ __forceinline__ uint32_t e2m1x8_rne(const float* y) {
   return r;
 }
 
-template <bool SR, bool INT4 = false>
-__device__ __forceinline__ uint2 quant16(const uint32_t* w, float r, uint64_t seed, uint64_t idx0) {
+template <bool SR, bool INT4 = false, class KEY = uint64_t>
+__device__ __forceinline__ uint2 quant16(const uint32_t* w, float r, const KEY& seed, uint64_t idx0) {
   if constexpr (INT4) {
     uint32_t nib[16];
     if constexpr (!SR) {
@@ -432,8 +484,8 @@ __device__ __forceinline__ uint2 quant16(const uint32_t* w, float r, uint64_t se
 
 // quant16 of one column of a 16-row block held as 16 words, each a row's
 // pair of neighbouring columns: HI selects the high (odd) column.
-template <bool SR, bool HI>
-__device__ __forceinline__ uint2 quant16_col(const uint32_t (&v)[16], float r, uint64_t seed, uint64_t idx0) {
+template <bool SR, bool HI, class KEY = uint64_t>
+__device__ __forceinline__ uint2 quant16_col(const uint32_t (&v)[16], float r, const KEY& seed, uint64_t idx0) {
   float y[16];
   if constexpr (!SR) {
 #pragma unroll

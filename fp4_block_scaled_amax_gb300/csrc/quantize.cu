@@ -118,7 +118,7 @@ __global__ void __launch_bounds__(256) k_quant_rows(const uint16_t* __restrict__
     if ((threadIdx.x & 31) == (unsigned)(__ffs(mask) - 1)) atomicMax(reinterpret_cast<unsigned int*>(amax_out), am);
   }
   if constexpr (G == 32) a = fmaxf(a, __shfl_xor_sync(mask, a, 1));
-  const BlockScale bs = block_scale<FMT>(a, s_enc);
+  const BlockScale bs = block_scale<FMT, true>(a, s_enc);
   const uint2 q = quant16<SR, Elem<FMT>::INT4>(w, bs.r, seed, (uint64_t)(row * K + c16 * 16));
   *reinterpret_cast<uint2*>(codes + row * (K / 2) + c16 * 8) = q;
   if constexpr (FMT == SF_UE5M3) {
@@ -206,7 +206,7 @@ __global__ void __launch_bounds__(256) k_quant_tile(
       if constexpr (G == 32) a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 1));
       if (valid[it]) {
         const int64_t row = m0 + r, col = k0 + cc * 16;
-        const BlockScale bs = block_scale_tab<FMT>(a, s_enc, rtab);
+        const BlockScale bs = block_scale_tab<FMT, true>(a, s_enc, rtab);
         const uint2 q = quant16<ROW_SR>(w[it], bs.r, seed_row, (uint64_t)(row * K + col));
         *reinterpret_cast<uint2*>(codes_row + row * (K / 2) + col / 2) = q;
         maxc_row = max(maxc_row, bs.code);
@@ -245,14 +245,14 @@ __global__ void __launch_bounds__(256) k_quant_tile(
   uint2 q0, q1;
   uint32_t sc0, sc1 = 0;
   if constexpr (G == 16) {
-    const BlockScale b0 = block_scale_tab<FMT>(absmax_words(v, 8), s_enc, rtab);
-    const BlockScale b1 = block_scale_tab<FMT>(absmax_words(v + 8, 8), s_enc, rtab);
+    const BlockScale b0 = block_scale_tab<FMT, true>(absmax_words(v, 8), s_enc, rtab);
+    const BlockScale b1 = block_scale_tab<FMT, true>(absmax_words(v + 8, 8), s_enc, rtab);
     q0 = quant16<COL_SR>(v, b0.r, seed_col, idx0);
     q1 = quant16<COL_SR>(v + 8, b1.r, seed_col, idx0 + 16);
     sc0 = b0.code;
     sc1 = b1.code;
   } else {
-    const BlockScale b0 = block_scale_tab<FMT>(absmax_words(v, 16), s_enc, rtab);
+    const BlockScale b0 = block_scale_tab<FMT, true>(absmax_words(v, 16), s_enc, rtab);
     q0 = quant16<COL_SR>(v, b0.r, seed_col, idx0);
     q1 = quant16<COL_SR>(v + 8, b0.r, seed_col, idx0 + 16);
     sc0 = b0.code;
@@ -403,6 +403,7 @@ __global__ void __launch_bounds__(QD_THREADS, 1)
     const int rr = 8 * cw + (lane & 7), rq = lane >> 3;
     // col pass: box cw / 8, row block cw % 8, columns 2 l, 2 l + 1 of the box
     const int cbox = cw >> 3, crb = cw & 7;
+    const PhiloxKey key_row(p.seed_row), key_col(p.seed_col);
     int it = 0;
     for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++it) {
       const int s = it % QD_STAGES, b = it & 1;
@@ -425,10 +426,10 @@ __global__ void __launch_bounds__(QD_THREADS, 1)
           const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
           const float a = absmax_words(w, 8);
           amax_local = fmaxf(amax_local, a);
-          const BlockScale bs = block_scale_tab<FMT>(a, s_enc, rtab);
+          const BlockScale bs = block_scale_tab<FMT, true>(a, s_enc, rtab);
           maxc_row = max(maxc_row, bs.code);
           const int64_t grow = m0 + rr, gcol = k0 + 16 * c;
-          const uint2 q = quant16<ROW_SR>(w, bs.r, p.seed_row, (uint64_t)(grow * p.K + gcol));
+          const uint2 q = quant16<ROW_SR>(w, bs.r, key_row, (uint64_t)(grow * p.K + gcol));
           *reinterpret_cast<uint2*>(p.codes_row + grow * (p.K / 2) + gcol / 2) = q;
           stg_sfr[qd_sf_off(rr, c)] = (uint8_t)bs.code;
         }
@@ -444,13 +445,13 @@ __global__ void __launch_bounds__(QD_THREADS, 1)
         const uint32_t am2 = absmax_words2(v, 16);  // both columns' block maxima
         const float a_lo = bf16_lo(am2), a_hi = bf16_hi(am2);
         if constexpr (!DO_ROW) amax_local = fmaxf(amax_local, fmaxf(a_lo, a_hi));
-        const BlockScale b0 = block_scale_tab<FMT>(a_lo, s_enc, rtab);
-        const BlockScale b1 = block_scale_tab<FMT>(a_hi, s_enc, rtab);
+        const BlockScale b0 = block_scale_tab<FMT, true>(a_lo, s_enc, rtab);
+        const BlockScale b1 = block_scale_tab<FMT, true>(a_hi, s_enc, rtab);
         maxc_col = max(maxc_col, max(b0.code, b1.code));
         const int c0 = 64 * cbox + 2 * lane;  // tile column of the low half
         const uint64_t i0 = (uint64_t)(k0 + c0) * (uint64_t)p.M + (uint64_t)(m0 + 16 * crb);
-        const uint2 q0 = quant16_col<COL_SR, false>(v, b0.r, p.seed_col, i0);
-        const uint2 q1 = quant16_col<COL_SR, true>(v, b1.r, p.seed_col, i0 + (uint64_t)p.M);
+        const uint2 q0 = quant16_col<COL_SR, false>(v, b0.r, key_col, i0);
+        const uint2 q1 = quant16_col<COL_SR, true>(v, b1.r, key_col, i0 + (uint64_t)p.M);
         // staged transposed codes: output row c, bytes 8 crb .. +7 (64-byte swizzle)
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
