@@ -1023,8 +1023,9 @@ def gemv_shapes_study(step, reps=5, launches=32):
     3584 and W_down 3584 x 18944 (NVFP4, quantized once), at batch 1, 8 and
     64: per-launch time over `launches` back-to-back launches that rotate over
     enough weight copies to exceed L2 (each launch streams its weights from
-    HBM).  Batch <= 8 runs the shared-memory (TMA) form, batch 64 the
-    register-fed one.  Outside the timed step."""
+    HBM), issued one by one and replayed from a CUDA graph.  Every batch runs
+    the TMA-fed kernel (K is a multiple of 256); W_down's long K splits over
+    clusters of CTAs.  Outside the timed step."""
     from fp4_block_scaled_amax_gb300 import synth
     fp4 = step.fp4
     dev = step.Y.device
@@ -1053,17 +1054,29 @@ def gemv_shapes_study(step, reps=5, launches=32):
                     fp4.fp4_gemv_w4a16(c, sc, amax, x, b, N, K, BF, y)
 
             loop()
-            ts = []
-            for _ in range(reps):
-                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                e0.record(st)
+            # the same launches replayed from one CUDA graph (no host launch cost between them)
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph):
                 loop()
-                e1.record(st)
-                torch.cuda.synchronize()
-                ts.append(e0.elapsed_time(e1) * 1e3 / launches)
-            us = statistics.median(ts)
-            gbs = (wbytes + 2 * b * (N + K)) / us / 1e3
-            out[f"batch_{b}"] = {"us": round(us, 2), "GB/s": round(gbs, 1)}
+            graph.replay()
+
+            def timed(fn):
+                ts = []
+                for _ in range(reps):
+                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    e0.record(st)
+                    fn()
+                    e1.record(st)
+                    torch.cuda.synchronize()
+                    ts.append(e0.elapsed_time(e1) * 1e3 / launches)
+                return statistics.median(ts)
+
+            us, gus = timed(loop), timed(graph.replay)
+            nbytes = wbytes + 2 * b * (N + K)
+            out[f"batch_{b}"] = {"us": round(us, 2), "GB/s": round(nbytes / us / 1e3, 1),
+                                 "graph_us": round(gus, 2), "graph_GB/s": round(nbytes / gus / 1e3, 1),
+                                 "graph_frac": round(nbytes / gus / 1e3 / peaks()[0], 4)}
+            del graph
         res[f"{wname} {N}x{K}"] = out
         del ws
     return res

@@ -134,26 +134,6 @@ __device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* map, uint32
                "r"(src), "r"(x), "r"(y)
                : "memory");
 }
-// The same store with an L2 cache policy (the output streams through L2).
-__device__ __forceinline__ void tma_store_2d_hint(const CUtensorMap* map, uint32_t src, int x, int y, uint64_t pol) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group.L2::cache_hint [%0, {%2, %3}], [%1], %4;" ::"l"(
-          reinterpret_cast<uint64_t>(map)),
-      "r"(src), "r"(x), "r"(y), "l"(pol)
-      : "memory");
-}
-// L2 cache policies: operands every round re-reads stay (evict_last); the
-// output leaves first (evict_first).
-__device__ __forceinline__ uint64_t policy_evict_last() {
-  uint64_t p;
-  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
-  return p;
-}
-__device__ __forceinline__ uint64_t policy_evict_first() {
-  uint64_t p;
-  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
-  return p;
-}
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
@@ -161,14 +141,6 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
   asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
                "l"(src), "r"(bytes), "r"(bar)
                : "memory");
-}
-__device__ __forceinline__ void bulk_load_hint(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar,
-                                               uint64_t pol) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
-          dst),
-      "l"(src), "r"(bytes), "r"(bar), "l"(pol)
-      : "memory");
 }
 
 // ---- tcgen05 --------------------------------------------------------------
@@ -238,14 +210,6 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
       "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, "
       "%4}], [%2];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
-      : "memory");
-}
-__device__ __forceinline__ void tma_load_2d_pair_hint(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y,
-                                                      uint64_t pol) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint "
-      "[%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "l"(pol)
       : "memory");
 }
 // Block-scaled FP4 MMA of the CTA pair (M = 256), and the commit that arrives
@@ -349,7 +313,7 @@ __device__ __forceinline__ bool skip_pass(const Params& p) {
 template <bool BF16, class PL>
 __device__ __forceinline__ void store_block(const uint32_t (&r)[2][32], float alpha, uint8_t* stage_buf,
                                             uint32_t stage_addr, const CUtensorMap* tmap_c, int row0, int col0,
-                                            int lane, bool accumulate, uint64_t out_policy) {
+                                            int lane, bool accumulate) {
   constexpr int OB = PL::OUT_ROW_BYTES;
   constexpr int BLK_COLS = OB / (BF16 ? 2 : 4);  // columns per staged row
   constexpr int VECS = OB / 16;                  // 16-byte vectors per staged row
@@ -387,7 +351,7 @@ __device__ __forceinline__ void store_block(const uint32_t (&r)[2][32], float al
     __syncwarp();
     if (lane == 0) {
       if (accumulate) tma_reduce_add_2d(tmap_c, stage_addr, col0 + BLK_COLS * b, row0);
-      else tma_store_2d_hint(tmap_c, stage_addr, col0 + BLK_COLS * b, row0, out_policy);
+      else tma_store_2d(tmap_c, stage_addr, col0 + BLK_COLS * b, row0);
       bulk_commit();
     }
   }
@@ -696,7 +660,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const float alpha = epilogue_alpha<FMT>(p);
     uint8_t* stage_buf = smem + SMEM_OUT + ew * STAGE_BYTES;
     const uint32_t stage_addr = smem_u32(stage_buf);
-    const uint64_t out_policy = policy_evict_first();  // the output streams out through L2
     uint32_t acc_phase = 0;
     for (int u = cluster_id; u < num_units; u += num_clusters) {
       const int mt = u % m_groups, nt = u / m_groups;
@@ -714,7 +677,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       // 64-column slabs at or past N (a half tile) hold no output
       if (nt * BN + EPI_COLS * cblk < p.N)
         store_block<BF16, PL>(r, alpha, stage_buf, stage_addr, &tmap_c, mt * BM + 32 * quarter,
-                              nt * BN + EPI_COLS * cblk, lane, p.accumulate != 0, out_policy);
+                              nt * BN + EPI_COLS * cblk, lane, p.accumulate != 0);
     }
     if (lane == 0) bulk_wait0();
     __syncwarp();
@@ -842,8 +805,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (lane == 0 && run) {
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_a)) : "memory");
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_b)) : "memory");
-      // B panels are re-read by every round of units (units walk N fastest)
-      const uint64_t keep = policy_evict_last();
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
@@ -857,8 +818,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           if (leader) mbar_expect_tx(bar_full + 8 * stage, 2 * (A_BYTES + B_STAGE));
           const uint32_t fb = lead_full + 8 * stage;
           tma_load_2d_pair(sbase + SMEM_A + stage * A_BYTES, &tmap_a, fb, ks * (BK / 2), mp * PM + BM * (int)crank);
-          tma_load_2d_pair_hint(sbase + SMEM_B + stage * B_STAGE, &tmap_b, fb, ks * (BK / 2),
-                                nt * BN + (BN / 2) * (int)crank, keep);
+          tma_load_2d_pair(sbase + SMEM_B + stage * B_STAGE, &tmap_b, fb, ks * (BK / 2),
+                           nt * BN + (BN / 2) * (int)crank);
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
@@ -922,7 +883,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   } else if (warp == SF_PRODUCER_WARP) {
     // ------------------------------ scale producer ------------------------
     if (lane == 0 && run) {
-      const uint64_t keep = policy_evict_last();
       int slot = 0;
       uint32_t phase = 0;
       bool ok = true;
@@ -941,10 +901,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           mbar_expect_tx(sb, SFA_BYTES + 2 * SFB_HALF);
           bulk_load(sbase + SMEM_SFA + slot * SFA_MAX, p.As + a_slab * sf_row_stride + (int64_t)ks * SFA_BYTES,
                     SFA_BYTES, sb);
-          bulk_load_hint(sbase + SMEM_SFB + slot * SFB_MAX, p.Bs + (2 * nt) * sf_row_stride + (int64_t)ks * SFB_HALF,
-                         SFB_HALF, sb, keep);
-          bulk_load_hint(sbase + SMEM_SFB + slot * SFB_MAX + SFB_HALF,
-                         p.Bs + b_hi * sf_row_stride + (int64_t)ks * SFB_HALF, SFB_HALF, sb, keep);
+          bulk_load(sbase + SMEM_SFB + slot * SFB_MAX, p.Bs + (2 * nt) * sf_row_stride + (int64_t)ks * SFB_HALF,
+                    SFB_HALF, sb);
+          bulk_load(sbase + SMEM_SFB + slot * SFB_MAX + SFB_HALF,
+                    p.Bs + b_hi * sf_row_stride + (int64_t)ks * SFB_HALF, SFB_HALF, sb);
           if (++slot == SF_SLOTS) {
             slot = 0;
             phase ^= 1u;
@@ -1017,7 +977,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const float alpha = epilogue_alpha<FMT>(p);
     uint8_t* stage_buf = smem + SMEM_OUT + ew * STAGE_BYTES;
     const uint32_t stage_addr = smem_u32(stage_buf);
-    const uint64_t out_policy = policy_evict_first();  // the output streams out through L2
     float s_enc_out = 1.0f, amax_local = 0.0f;
     if constexpr (QOUT) s_enc_out = fp4dev::global_encode_scale<fp4dev::SF_E4M3>(__ldg(p.q_g), p.status);
     uint32_t acc_phase = 0;
@@ -1040,7 +999,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                        s_enc_out, amax_local);
       } else {
         store_block<BF16, PL>(r, alpha, stage_buf, stage_addr, &tmap_c, mp * PM + BM * (int)crank + 32 * quarter,
-                              nt * BN + EPI_COLS * cblk, lane, p.accumulate != 0, out_policy);
+                              nt * BN + EPI_COLS * cblk, lane, p.accumulate != 0);
       }
     }
     if constexpr (QOUT) {

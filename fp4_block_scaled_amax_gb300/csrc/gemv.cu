@@ -329,8 +329,8 @@ __device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity) {
 template <int WPT, int NT>
 __global__ void __launch_bounds__(NT == 1 ? 32 * (1 + 4 * 6) : 32 * (1 + 2 * 8))
     k_gemv_w4a16_tma(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant__ CUtensorMap tm_scales,
-                     const __grid_constant__ CUtensorMap tm_x, const float* __restrict__ gw, int batch, int N, int nk,
-                     int T, int S, bool bf16_out, void* __restrict__ y, int32_t* status) {
+                     const __grid_constant__ CUtensorMap tm_x, const float* __restrict__ gw, int batch, int N,
+                     int nk_total, int T, int S, int ksplit, bool bf16_out, void* __restrict__ y, int32_t* status) {
   using namespace fp4async;
   using L = TvLayout<WPT, NT>;
   constexpr int BW = 8 * NT;  // batch columns per tile
@@ -346,7 +346,13 @@ __global__ void __launch_bounds__(NT == 1 ? 32 * (1 + 4 * 6) : 32 * (1 + 2 * 8))
   float* const red = reinterpret_cast<float*>(base_ptr + S * stage_bytes);  // [WPT*T][16][BW]
   const uint32_t bars = base + S * stage_bytes + (uint32_t)nwarps * 16 * BW * 4;  // full[S], empty[S]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n0 = blockIdx.x * 16 * T;
+  // split K: the ksplit CTAs of a cluster share the tiles and each takes a
+  // contiguous run of the K stages; rank 0 sums the partial results
+  uint32_t rank = 0;
+  if (ksplit > 1) asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(rank));
+  const int n0 = (blockIdx.x / ksplit) * 16 * T;
+  const int it0 = (int)(((int64_t)nk_total * rank) / ksplit);
+  const int nk = (int)(((int64_t)nk_total * (rank + 1)) / ksplit) - it0;
 
   if (threadIdx.x == 0) {
     abort_flag = 0;
@@ -371,13 +377,14 @@ __global__ void __launch_bounds__(NT == 1 ? 32 * (1 + 4 * 6) : 32 * (1 + 2 * 8))
         const uint32_t full = bars + 8 * s;
         const uint32_t st = base + s * stage_bytes;
         mbar_expect_tx(full, tx);
+        const int gs = it0 + it;  // the stage's place along K
 #pragma unroll
         for (int i = 0; i < L::CODE_BOXES; ++i)
-          tma_load_2d(st + code_box * i, &tm_codes, full, it * (L::SC / 2) + 128 * i, n0);
+          tma_load_2d(st + code_box * i, &tm_codes, full, gs * (L::SC / 2) + 128 * i, n0);
 #pragma unroll
         for (int i = 0; i < L::X_BOXES; ++i)
-          tma_load_2d(st + code_bytes + L::X_BOX_BYTES * i, &tm_x, full, it * L::SC + 64 * i, 0);
-        tma_load_2d(st + code_bytes + L::x_bytes(), &tm_scales, full, it * L::SB, n0);
+          tma_load_2d(st + code_bytes + L::X_BOX_BYTES * i, &tm_x, full, gs * L::SC + 64 * i, 0);
+        tma_load_2d(st + code_bytes + L::x_bytes(), &tm_scales, full, gs * L::SB, n0);
         issued = it + 1;
         if (++s == S) {
           s = 0;
@@ -466,20 +473,43 @@ __global__ void __launch_bounds__(NT == 1 ? 32 * (1 + 4 * 6) : 32 * (1 + 2 * 8))
     }
   }
   __syncthreads();
-  const float s_enc = fp4dev::global_encode_scale<fp4dev::SF_E4M3>(__ldg(gw), nullptr);
-  const int rows = 16 * T;
-  for (int i = threadIdx.x; i < rows * BW; i += blockDim.x) {
-    const int b = i / rows, r = i % rows;
-    const int n = n0 + r;
-    if (n >= N || b >= batch) continue;
-    const int t = r >> 4, rr = r & 15;
-    const float* p = red + ((size_t)(WPT * t) * 16 + rr) * BW + b;
-    float v = 0.0f;
+  if (ksplit > 1) {
+    // every CTA's partial sums are in its shared memory before rank 0 reads them
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+  }
+  if (rank == 0) {
+    const float s_enc = fp4dev::global_encode_scale<fp4dev::SF_E4M3>(__ldg(gw), nullptr);
+    const int rows = 16 * T;
+    for (int i = threadIdx.x; i < rows * BW; i += blockDim.x) {
+      const int b = i / rows, r = i % rows;
+      const int n = n0 + r;
+      if (n >= N || b >= batch) continue;
+      const int t = r >> 4, rr = r & 15;
+      const float* p = red + ((size_t)(WPT * t) * 16 + rr) * BW + b;
+      float v = 0.0f;
 #pragma unroll
-    for (int k = 0; k < WPT; ++k) v = __fadd_rn(v, p[k * 16 * BW]);
-    v = __fdiv_rn(__fmul_rn(v, 256.0f), s_enc);
-    if (bf16_out) static_cast<__nv_bfloat16*>(y)[(int64_t)b * N + n] = __float2bfloat16_rn(v);
-    else static_cast<float*>(y)[(int64_t)b * N + n] = v;
+      for (int k = 0; k < WPT; ++k) v = __fadd_rn(v, p[k * 16 * BW]);
+      // the other ranks' partial sums, in rank order (a fixed summation order)
+      for (int q = 1; q < ksplit; ++q) {
+        uint32_t remote;
+        asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(p)), "r"(q));
+#pragma unroll
+        for (int k = 0; k < WPT; ++k) {
+          float pv;
+          asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(pv) : "r"(remote + 4u * k * 16 * BW));
+          v = __fadd_rn(v, pv);
+        }
+      }
+      v = __fdiv_rn(__fmul_rn(v, 256.0f), s_enc);
+      if (bf16_out) static_cast<__nv_bfloat16*>(y)[(int64_t)b * N + n] = __float2bfloat16_rn(v);
+      else static_cast<float*>(y)[(int64_t)b * N + n] = v;
+    }
+  }
+  if (ksplit > 1) {
+    // no CTA leaves while rank 0 may still read its shared memory
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
   }
 }
 
@@ -499,11 +529,12 @@ bool make_map(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64
 int sm_count() { return fp4lib::current_sm_count(); }
 
 template <int WPT, int NT>
-cudaError_t launch_tma_t(const fp4lib::GemvArgs& a, int T, cudaStream_t st) {
+cudaError_t launch_tma_t(const fp4lib::GemvArgs& a, int T, int ksplit, cudaStream_t st) {
   using L = TvLayout<WPT, NT>;
   const int64_t tiles = (a.N + 15) / 16;
-  const int64_t ctas = (tiles + T - 1) / T;
-  const int nk = (int)((a.K + L::SC - 1) / L::SC);
+  const int64_t ctas = (tiles + T - 1) / T * ksplit;
+  const int nk_total = (int)((a.K + L::SC - 1) / L::SC);
+  const int nk = (nk_total + ksplit - 1) / ksplit;  // the most stages one CTA streams
   const size_t red_bytes = (size_t)WPT * T * 16 * 8 * NT * 4;
   // batch <= 8: a 200 KB ring; larger batches: what fits beside the reduction buffer
   const size_t budget =
@@ -538,9 +569,20 @@ cudaError_t launch_tma_t(const fp4lib::GemvArgs& a, int T, cudaStream_t st) {
   });
   if (e != cudaSuccess) return e;
   if (allowed <= 0 || smem > (size_t)allowed) return cudaErrorNotSupported;
-  k_gemv_w4a16_tma<WPT, NT><<<(unsigned)ctas, 32 * (1 + WPT * T), smem, st>>>(mc, ms, mx, a.gw, (int)a.batch, (int)a.N, nk,
-                                                                         T, S, a.bf16_out, a.y, a.status);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)ksplit;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3((unsigned)ctas, 1, 1);
+  cfg.blockDim = dim3(32 * (1 + WPT * T), 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = ksplit > 1 ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, k_gemv_w4a16_tma<WPT, NT>, mc, ms, mx, a.gw, (int)a.batch, (int)a.N, nk_total, T, S,
+                            ksplit, a.bf16_out, a.y, a.status);
 }
 
 // Returns cudaErrorNotSupported (before launching anything) when the shape or
@@ -551,12 +593,28 @@ cudaError_t launch_gemv_tma(const fp4lib::GemvArgs& a, cudaStream_t st) {
     return cudaErrorNotSupported;
   const int64_t tiles = (a.N + 15) / 16;
   const int sms = sm_count();
-  int T = (int)((tiles + sms - 1) / sms);
-  T = T < 1 ? 1 : (T > TV_MAX_TILES ? TV_MAX_TILES : T);
+  // tiles per CTA and K split: the fewest split ways whose CTAs cover at least
+  // 90 % of the SMs (a split needs at least 4 stages per CTA), else the best
+  int T = 1, ksplit = 1;
+  double best = -1.0;
+  for (int s = 1; s <= 4; s *= 2) {
+    int t = (int)((tiles * s + sms - 1) / sms);
+    t = t < 1 ? 1 : t;
+    if (t > TV_MAX_TILES) continue;
+    const int64_t stages = a.K / 256;  // 256-column stages at the least
+    if (s > 1 && stages < 4 * s) continue;
+    const double cover = (double)(((tiles + t - 1) / t) * s) / sms;
+    if (cover > best + 0.02) {
+      best = cover;
+      T = t;
+      ksplit = s;
+    }
+    if (cover >= 0.9) break;
+  }
   // eight batch tiles of 8 rows: 512-column stages (four warps per tile) when a CTA holds few tiles,
   // 256-column stages (two warps per tile) otherwise
-  if (a.batch > 8) return T <= 3 ? launch_tma_t<4, 8>(a, T, st) : launch_tma_t<2, 8>(a, T, st);
-  return T <= 6 ? launch_tma_t<4, 1>(a, T, st) : launch_tma_t<2, 1>(a, T, st);
+  if (a.batch > 8) return T <= 3 ? launch_tma_t<4, 8>(a, T, ksplit, st) : launch_tma_t<2, 8>(a, T, ksplit, st);
+  return T <= 6 ? launch_tma_t<4, 1>(a, T, ksplit, st) : launch_tma_t<2, 1>(a, T, ksplit, st);
 }
 
 }  // namespace
