@@ -51,71 +51,22 @@ STEP_FLOPS = 3 * 2 * M_TOK * N_FFN * K_HID
 WORKLOAD = "llama2-7b-mlp-linear-fwd-bwd"
 METRIC = "NVFP4 GEMM TFLOPS & quantize GB/s at 7B shapes, % of FP4-MMA/HBM peak"
 FP4_PER_BF16 = 6.0  # nominal dense FP4 / bf16 tensor ratio on GB300 (13.5 / 2.25 PFLOP/s)
-# DRAM bytes (read + write) per launch from one ncu capture of the full-size
-# step (`ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum`, one pass),
+# DRAM bytes (read + write) per launch of the full-size step, from ncu
+# captures of one kernel at a time (`ncu --metrics dram__bytes_read.sum,
+# dram__bytes_write.sum,gpu__time_duration.sum -k <kernel> -c 3`, one pass),
 # valid only while the kernel sources still hash to the recorded value.
 # gemm: mean over the fwd, dgrad and wgrad launches; quant_dual: the step's
-# three dual quantizations together; gemv: one launch.  Writes still held in
-# L2 when a kernel ends do not appear in its DRAM bytes.
-NCU_TRAFFIC = {"gemm": {"bytes": 291.5e6, "src": "dd8052b50d94f2a0",
-                        "files": ["gemm_sm103.cu", "async_sm103.cuh", "fp4_device.cuh"]},
-               "quant_dual": {"bytes": 751.9e6, "src": "ee5a8ae16859e27f",
-                              "files": ["quantize.cu", "fp4_device.cuh"]},
-               "gemv": {"bytes": 25.45e6, "src": "6e6c84997c1e2aac",
-                        "files": ["gemv.cu", "async_sm103.cuh", "fp4_device.cuh"]}}
+# three dual quantizations together; gemv, amax: one launch.  Writes still
+# held in L2 when a kernel ends do not appear in its DRAM bytes.
+NCU_TRAFFIC = {"gemm": {"bytes": 292.28e6, "src": "1b145e4098c46dc4",
+                        "files": ["gemm_sm103.cu", "async_sm103.cuh", "fp4_device.cuh", "device_cache.h"]},
+               "quant_dual": {"bytes": 803.79e6, "src": "f4b4a27adc565d34",
+                              "files": ["quantize.cu", "async_sm103.cuh", "fp4_device.cuh", "device_cache.h"]},
+               "gemv": {"bytes": 25.45e6, "src": "579ab50a10fda9d8",
+                        "files": ["gemv.cu", "async_sm103.cuh", "fp4_device.cuh", "device_cache.h"]},
+               "amax": {"bytes": 586.5e6, "src": "f4b4a27adc565d34",
+                        "files": ["quantize.cu", "async_sm103.cuh", "fp4_device.cuh", "device_cache.h"]}}
 
-
-def parse():
-    p = argparse.ArgumentParser()
-    p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=10)
-    p.add_argument("--warmup", type=int, default=3)
-    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    p.add_argument("--no-e2e", action="store_true")
-    p.add_argument("--no-cpu-baseline", action="store_true")
-    p.add_argument("--studies", default="all",
-                   help="comma-separated side studies to run (default: all), e.g. formats,stack")
-    p.add_argument("--no-studies", action="store_true",
-                   help="skip the side measurements after the timed steps (for ncu launch lists)")
-    p.add_argument("--tokens", type=int, default=16384,
-                   help="token count M (default: the workload's 16384; smaller only for ncu captures)")
-    return p.parse_args()
-
-
-# ---------------------------------------------------------------------------
-# distributed plumbing (one process per GPU)
-# ---------------------------------------------------------------------------
-
-def dist_env():
-    rank = int(os.environ.get("RANK", "0"))
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    return rank, world, local
-
-
-def dist_init(world, backend):
-    if world > 1 and not torch.distributed.is_initialized():
-        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
-        torch.distributed.init_process_group(backend)
-
-
-def barrier(world):
-    if world > 1:
-        torch.distributed.barrier()
-
-
-def max_over_ranks(value: float, world: int, device=None) -> float:
-    """Largest value over all ranks (the slowest rank sets the time)."""
-    if world == 1:
-        return value
-    t = torch.tensor([value], dtype=torch.float64, device=device)
-    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-    return float(t.item())
-
-
-# ---------------------------------------------------------------------------
-# peaks, clocks, cpu baseline
-# ---------------------------------------------------------------------------
 
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
@@ -214,6 +165,9 @@ def cores():
 # the GPU step
 # ---------------------------------------------------------------------------
 
+STEP_EVENTS = 9  # start, after the amax launch, after each dual quantizer, after each GEMM, after the GEMV
+
+
 class LinearStep:
     """Device buffers of one step and the sequence of library calls."""
 
@@ -243,10 +197,10 @@ class LinearStep:
         self.xg = d["x_dec"].to(device)
         self.yg = torch.empty((GEMV_BATCH, N), dtype=torch.bfloat16, device=device)
         self.status = torch.zeros(1, dtype=torch.int32, device=device)
-        self.launches_per_step = 10
+        self.launches_per_step = 8  # amax of all three, 3 dual quantizers, 3 GEMMs, 1 GEMV
 
     def run(self, ev=None):
-        """One step; ev: optional list of 11 CUDA events recorded between kernels."""
+        """One step; ev: optional list of STEP_EVENTS CUDA events recorded between kernels."""
         fp4 = self.fp4
         RNE, SR, MMA = fp4.FP4_ROUND_RNE, fp4.FP4_ROUND_STOCHASTIC, fp4.FP4_SFLAYOUT_MMA
         M, K, N = M_TOK, K_HID, N_FFN
@@ -257,29 +211,30 @@ class LinearStep:
                 ev[i].record(st)
 
         mark(0)
+        # the three fresh global amaxes in one launch
+        fp4.fp4_amax_n([self.X, self.W, self.dY], self.amax)
+        mark(1)
         for j, (name, rr, sr, rc, sc) in enumerate([("X", RNE, 0, SR, 1236), ("W", RNE, 0, RNE, 0),
                                                      ("dY", SR, 1234, SR, 1235)]):
             x = getattr(self, name)
             a = self.amax[j:j + 1]
-            fp4.fp4_amax(x, a)
-            mark(1 + 2 * j)
             cr, srs, cc, scs = self.q[name]
             fp4.fp4_quantize_dual(x, "E4M3", rr, sr, rc, sc, a, MMA, cr, srs, cc, scs, None, self.status)
-            mark(2 + 2 * j)
+            mark(2 + j)
         qX, qW, qd = self.q["X"], self.q["W"], self.q["dY"]
         aX, aW, ad = self.amax[0:1], self.amax[1:2], self.amax[2:3]
         BF = fp4.FP4_OUT_BF16
         fp4.fp4_gemm(qX[0], qX[1], qW[0], qW[1], aX, aW, None, None, M, N, K, "E4M3", BF, self.Y,
                      dev_status=self.status)
-        mark(7)
+        mark(5)
         fp4.fp4_gemm(qd[0], qd[1], qW[2], qW[3], ad, aW, None, None, M, K, N, "E4M3", BF, self.dX,
                      dev_status=self.status)
-        mark(8)
+        mark(6)
         fp4.fp4_gemm(qd[2], qd[3], qX[2], qX[3], ad, aX, None, None, N, K, M, "E4M3", BF, self.dW,
                      dev_status=self.status)
-        mark(9)
+        mark(7)
         fp4.fp4_gemv_w4a16(self.Wg_codes, self.Wg_scales, self.Wg_amax, self.xg, GEMV_BATCH, N, K, BF, self.yg)
-        mark(10)
+        mark(8)
 
 
 # ---------------------------------------------------------------------------
@@ -817,10 +772,10 @@ def step_variants_study(step, flush, reps=5):
         torch.matmul(step.dY.t(), step.X, out=step.dW)
 
     def fp4_step(fresh):
+        if fresh:
+            fp4.fp4_amax_n([step.X, step.W, step.dY], step.amax)
         for j, (name, rr, sr, rc, sc) in enumerate(plan):
             x, a = getattr(step, name), step.amax[j:j + 1]
-            if fresh:
-                fp4.fp4_amax(x, a)
             cr, srs, cc, scs = step.q[name]
             fp4.fp4_quantize_dual(x, "E4M3", rr, sr, rc, sc, a, MMA, cr, srs, cc, scs)
         gemms(step.amax)
@@ -1162,7 +1117,7 @@ def run_ours(args, rank, world, local):
     if int(step.status.item()) != 0:
         raise RuntimeError(f"device status {int(step.status.item())} during warm-up")
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(11)] for _ in range(args.steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(STEP_EVENTS)] for _ in range(args.steps)]
     barrier(world)
     torch.cuda.synchronize()
     with ClockSampler(device) as clk:
@@ -1177,14 +1132,14 @@ def run_ours(args, rank, world, local):
     def span(e, a, z):
         return e[a].elapsed_time(e[z])
 
-    step_ms = [span(e, 0, 10) for e in evs]
+    step_ms = [span(e, 0, 8) for e in evs]
     ms = statistics.mean(step_ms)
     ms_max = max_over_ranks(ms, world, device)
-    gemm_ms = [span(e, i, i + 1) for e in evs for i in (6, 7, 8)]
-    fwd_ms = [span(e, 6, 7) for e in evs]
-    quant_ms = [span(e, 2 * j + 1, 2 * j + 2) for e in evs for j in range(3)]
-    amax_ms = [span(e, 2 * j, 2 * j + 1) for e in evs for j in range(3)]
-    gemv_ms = [span(e, 9, 10) for e in evs]
+    gemm_ms = [span(e, i, i + 1) for e in evs for i in (4, 5, 6)]
+    fwd_ms = [span(e, 4, 5) for e in evs]
+    quant_ms = [span(e, 1 + j, 2 + j) for e in evs for j in range(3)]
+    amax_ms = [span(e, 0, 1) for e in evs]
+    gemv_ms = [span(e, 7, 8) for e in evs]
 
     hbm, bf16, src = peaks()
     fp4_peak = bf16 * FP4_PER_BF16
@@ -1261,7 +1216,7 @@ def run_ours(args, rank, world, local):
                      "achieved": round(gemm_tflops, 1), "peak": round(fp4_peak, 1), "unit": "TFLOP/s",
                      "frac": round(gemm_tflops / fp4_peak, 4), "traffic": traffic_v,
                      "peak_source": f"{src}: bf16 burst {bf16} x {FP4_PER_BF16} (nominal FP4/bf16)"},
-        "roofline_quantize": {"kernel": "k_quant_tile (dual, 3.125 B/elem; X, W, dY per step)", "bound": "hbm",
+        "roofline_quantize": {"kernel": "k_quant_dual_tma (dual, 3.125 B/elem; X, W, dY per step)", "bound": "hbm",
                               "achieved": round(q_gbs, 1), "peak": hbm, "unit": "GB/s",
                               "frac": round(q_gbs / hbm, 4), "traffic": qtraffic_v, "peak_source": src},
         "quantize_modes": qmodes,
@@ -1278,6 +1233,10 @@ def run_ours(args, rank, world, local):
         "gemv_qwen_mlp_shapes": gv_shapes,
         "step_cuda_graph": step_graph,
         "amax_gbs": round(a_gbs, 1),
+        "roofline_amax": {"kernel": "k_amax_n (X, W, dY in one launch, 2 B/elem read)", "bound": "hbm",
+                          "achieved": round(a_gbs, 1), "peak": hbm, "unit": "GB/s", "frac": round(a_gbs / hbm, 4),
+                          "traffic": traffic_of("amax"), "peak_source": src,
+                          "note": "the first launch after the L2 flush also writes back the flush's dirty lines"},
         "gemv_w4a16": {"batch": GEMV_BATCH, "N": N_FFN, "K": K_HID, "us": round(statistics.mean(gemv_ms) * 1e3, 2),
                        "GB/s": round(gv_gbs, 1), "frac": round(gv_gbs / hbm, 4), "traffic": gvtraffic_v},
         "kernel_ms": {"fwd_gemm": round(statistics.mean(fwd_ms), 4),

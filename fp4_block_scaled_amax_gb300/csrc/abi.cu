@@ -105,6 +105,20 @@ fp4_status fp4_amax(const void* x_bf16, int64_t M, int64_t K, int64_t ldx, float
   return cuda_status(fp4lib::launch_amax(x_bf16, M, K, ldx, amax_out, (cudaStream_t)stream));
 }
 
+fp4_status fp4_amax_n(int n, const void* const* x_bf16, const int64_t* M, const int64_t* K, const int64_t* ldx,
+                      float* amax_out, fp4_stream_t stream) {
+  if (n < 0 || n > fp4lib::AMAX_N_MAX) return FP4_ERR_SHAPE;
+  if (n == 0) return FP4_OK;
+  if (x_bf16 == nullptr || M == nullptr || K == nullptr || ldx == nullptr || amax_out == nullptr)
+    return FP4_ERR_INVALID_ARG;
+  for (int i = 0; i < n; ++i) {
+    if (M[i] < 0 || K[i] < 0 || ldx[i] < K[i] || K[i] % 8 != 0) return FP4_ERR_SHAPE;
+    if (x_bf16[i] == nullptr && M[i] * K[i] > 0) return FP4_ERR_INVALID_ARG;
+    if (!aligned16(x_bf16[i]) || (ldx[i] * 2) % 16 != 0) return FP4_ERR_ALIGNMENT;
+  }
+  return cuda_status(fp4lib::launch_amax_n(n, x_bf16, M, K, ldx, amax_out, (cudaStream_t)stream));
+}
+
 fp4_status fp4_quantize(const void* x_bf16, int64_t M, int64_t K, int64_t ldx, fp4_scale_fmt f, fp4_rounding r,
                         uint64_t seed, const float* global_amax, int transpose, fp4_sf_layout sfl, uint8_t* codes,
                         uint8_t* scales, float* amax_out, int32_t* ue5m3_shift_out, int32_t* dev_status,

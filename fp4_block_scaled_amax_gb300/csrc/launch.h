@@ -23,6 +23,10 @@ struct QuantArgs {
 };
 
 cudaError_t launch_amax(const void* x, int64_t M, int64_t K, int64_t ldx, float* out, cudaStream_t st);
+constexpr int AMAX_N_MAX = 8;
+// the amaxes of n <= AMAX_N_MAX tensors (host arrays of their pointers and sizes) into out[0..n)
+cudaError_t launch_amax_n(int n, const void* const* x, const int64_t* M, const int64_t* K, const int64_t* ldx,
+                          float* out, cudaStream_t st);
 cudaError_t launch_quantize(const QuantArgs& a, cudaStream_t st);
 cudaError_t launch_dequantize(const uint8_t* codes, const uint8_t* scales, bool mma, int64_t M, int64_t K,
                               int fmt, const float* gptr, bool bf16, void* out, cudaStream_t st);

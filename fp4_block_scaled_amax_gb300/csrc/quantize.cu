@@ -89,6 +89,57 @@ __global__ void __launch_bounds__(256) k_amax(const uint16_t* __restrict__ x, in
   }
 }
 
+// Several tensors in one launch: CTA b works on tensor i with
+// cta_begin[i] <= b < cta_begin[i + 1] (CTA counts in proportion to size).
+struct AmaxN {
+  const uint16_t* x[fp4lib::AMAX_N_MAX];
+  int64_t M[fp4lib::AMAX_N_MAX], K[fp4lib::AMAX_N_MAX], ldx[fp4lib::AMAX_N_MAX];
+  int cta_begin[fp4lib::AMAX_N_MAX + 1];
+  int n;
+};
+
+__global__ void __launch_bounds__(256) k_amax_n(const __grid_constant__ AmaxN a, float* __restrict__ out) {
+  int i = 0;
+  while (i + 1 < a.n && (int)blockIdx.x >= a.cta_begin[i + 1]) ++i;
+  const int b = (int)blockIdx.x - a.cta_begin[i], nb = a.cta_begin[i + 1] - a.cta_begin[i];
+  const int64_t K = a.K[i], ldx = a.ldx[i];
+  const int64_t per_row = K / 8;
+  const int64_t total = a.M[i] * per_row;
+  const int64_t stride = (int64_t)nb * blockDim.x;
+  const bool dense = ldx == K;
+  const uint16_t* x = a.x[i];
+  uint32_t m = 0;
+  auto addr = [&](int64_t c) -> const uint16_t* {
+    if (dense) return x + c * 8;
+    const int64_t r = c / per_row;
+    return x + r * ldx + (c - r * per_row) * 8;
+  };
+  for (int64_t c = (int64_t)b * blockDim.x + threadIdx.x; c < total; c += 8 * stride) {
+    uint4 v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+      v[u] = c + u * stride < total ? ld_stream(addr(c + u * stride)) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      m = absmax2_xs(m, v[u].x);
+      m = absmax2_xs(m, v[u].y);
+      m = absmax2_xs(m, v[u].z);
+      m = absmax2_xs(m, v[u].w);
+    }
+  }
+  m &= 0x7FFF7FFFu;
+  const float am = fmaxf(bf16_lo(m), bf16_hi(m));
+  unsigned int ab = __reduce_max_sync(0xFFFFFFFFu, __float_as_uint(am));
+  __shared__ unsigned int warp_max[8];
+  if ((threadIdx.x & 31) == 0) warp_max[threadIdx.x >> 5] = ab;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    unsigned int v = threadIdx.x < (blockDim.x >> 5) ? warp_max[threadIdx.x] : 0u;
+    v = __reduce_max_sync(0xFFFFFFFFu, v);
+    if (threadIdx.x == 0) atomicMax(reinterpret_cast<unsigned int*>(out + i), v);
+  }
+}
+
 // ---------------------------------------------------------------------------
 // K1: row quantizer (blocks along K)
 // ---------------------------------------------------------------------------
@@ -692,6 +743,36 @@ cudaError_t launch_amax(const void* x, int64_t M, int64_t K, int64_t ldx, float*
   const int64_t cap = 152 * 8;
   if (blocks > cap) blocks = cap;
   k_amax<<<(unsigned)blocks, 256, 0, st>>>(static_cast<const uint16_t*>(x), M, K, ldx, out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_amax_n(int n, const void* const* x, const int64_t* M, const int64_t* K, const int64_t* ldx,
+                          float* out, cudaStream_t st) {
+  cudaError_t e = cudaMemsetAsync(out, 0, sizeof(float) * n, st);
+  if (e != cudaSuccess || n == 0) return e;
+  AmaxN a{};
+  a.n = n;
+  int64_t total = 0;
+  for (int i = 0; i < n; ++i) total += M[i] * (K[i] / 8);
+  if (total == 0) return cudaSuccess;
+  // the same cap as one fp4_amax launch, shared out by size (at least one CTA each)
+  const int64_t cap = 152 * 8;
+  int64_t blocks_total = (total + 255) / 256;
+  if (blocks_total > cap) blocks_total = cap;
+  int begin = 0;
+  for (int i = 0; i < n; ++i) {
+    a.x[i] = static_cast<const uint16_t*>(x[i]);
+    a.M[i] = M[i];
+    a.K[i] = K[i];
+    a.ldx[i] = ldx[i];
+    a.cta_begin[i] = begin;
+    const int64_t chunks = M[i] * (K[i] / 8);
+    int64_t nb = (chunks * blocks_total + total - 1) / total;
+    nb = nb < 1 ? 1 : nb;
+    begin += (int)nb;
+  }
+  a.cta_begin[n] = begin;
+  k_amax_n<<<(unsigned)begin, 256, 0, st>>>(a, out);
   return cudaGetLastError();
 }
 

@@ -58,6 +58,7 @@ _SIGS = {
     "fp4_group_size": (_I32, [_I32]),
     "fp4_storage_bytes": (_I32, [_I64, _I64, _I32, _SZP, _SZP]),
     "fp4_amax": (_I32, [_VP, _I64, _I64, _I64, _VP, _VP]),
+    "fp4_amax_n": (_I32, [_I32, _VP, _VP, _VP, _VP, _VP, _VP]),
     "fp4_quantize": (_I32, [_VP, _I64, _I64, _I64, _I32, _I32, _U64, _VP, _I32, _I32, _VP, _VP, _VP, _VP, _VP,
                             _VP]),
     "fp4_quantize_rht": (_I32, [_VP, _I64, _I64, _I64, _I32, _I32, _U64, ctypes.c_uint32, _VP, _I32, _VP, _VP, _VP,
@@ -149,6 +150,16 @@ def fp4_storage_bytes(rows: int, cols: int, fmt) -> tuple:
 def fp4_amax(x, amax_out, stream=None):
     M, K = x.shape
     _check(_lib().fp4_amax(_ptr(x), M, K, x.stride(0), _ptr(amax_out), _stream(stream)), "fp4_amax")
+
+
+def fp4_amax_n(xs, amax_out, stream=None):
+    """xs: a sequence of bf16 [M, K] CUDA tensors; amax_out: CUDA float32 tensor of len(xs)."""
+    n = len(xs)
+    ptrs = (ctypes.c_void_p * max(n, 1))(*[_ptr(x) for x in xs])
+    Ms = (ctypes.c_int64 * max(n, 1))(*[x.shape[0] for x in xs])
+    Ks = (ctypes.c_int64 * max(n, 1))(*[x.shape[1] for x in xs])
+    lds = (ctypes.c_int64 * max(n, 1))(*[x.stride(0) for x in xs])
+    _check(_lib().fp4_amax_n(n, ptrs, Ms, Ks, lds, _ptr(amax_out), _stream(stream)), "fp4_amax_n")
 
 
 def fp4_quantize(x, fmt, rounding, seed, global_amax, transpose, sfl, codes, scales,

@@ -122,6 +122,14 @@ fp4_status fp4_storage_bytes(int64_t rows, int64_t cols, fp4_scale_fmt f,
 fp4_status fp4_amax(const void* x_bf16, int64_t M, int64_t K, int64_t ldx,
                     float* amax_out, fp4_stream_t stream);
 
+/* fp4_amax of n tensors (1 <= n <= 8; n == 0 does nothing) in one launch:
+ * x_bf16[i], M[i], K[i], ldx[i] are HOST arrays describing tensor i (device
+ * pointers, the same requirements as fp4_amax each), and amax_out[i] (device
+ * float[n]) receives max |x_i|.  One launch for the several fresh amaxes a
+ * step needs, instead of one short launch per tensor. */
+fp4_status fp4_amax_n(int n, const void* const* x_bf16, const int64_t* M, const int64_t* K,
+                      const int64_t* ldx, float* amax_out, fp4_stream_t stream);
+
 /* Quantize a bf16 [M, K] matrix to FP4 codes plus block scales.
  * Method ([NVFP4/MX] "Метод", [UE5M3] "Что сделали", [FP4-REV]
  * "Стохастическая квантизация"), all float32 steps correctly rounded:

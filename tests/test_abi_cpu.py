@@ -128,6 +128,16 @@ def test_gemv_and_misc_argument_errors():
     assert lib.fp4_gemv_w4a16(P, P, None, P, 1, 128, 256, 0, P, None, None) == fp4.FP4_ERR_INVALID_ARG
     assert lib.fp4_amax(P, 4, 12, 12, P, None) == fp4.FP4_ERR_SHAPE
     assert lib.fp4_amax(P, 4, 16, 16, None, None) == fp4.FP4_ERR_INVALID_ARG
+    arr = lambda t, *v: (t * len(v))(*v)
+    xs = arr(ctypes.c_void_p, P, P)
+    i64 = ctypes.c_int64
+    assert lib.fp4_amax_n(9, xs, arr(i64, 4, 4), arr(i64, 16, 16), arr(i64, 16, 16), P, None) == fp4.FP4_ERR_SHAPE
+    assert lib.fp4_amax_n(2, xs, arr(i64, 4, 4), arr(i64, 16, 12), arr(i64, 16, 16), P, None) == fp4.FP4_ERR_SHAPE
+    assert lib.fp4_amax_n(2, xs, arr(i64, 4, 4), arr(i64, 16, 16), arr(i64, 16, 16), None, None) == \
+        fp4.FP4_ERR_INVALID_ARG
+    assert lib.fp4_amax_n(2, arr(ctypes.c_void_p, P, P + 8), arr(i64, 4, 4), arr(i64, 16, 16), arr(i64, 16, 16), P,
+                          None) == fp4.FP4_ERR_ALIGNMENT
+    assert lib.fp4_amax_n(0, None, None, None, None, None, None) == fp4.FP4_OK
     assert lib.fp4_dequantize(P, P, 0, 4, 24, 0, P, 0, P, None) == fp4.FP4_ERR_SHAPE
     assert lib.fp4_ue5m3_to_e4m3(P, 16, None, P, None, None) == fp4.FP4_ERR_INVALID_ARG
     assert lib.fp4_ue5m3_windows(P, 16, P, None, P, None, None) == fp4.FP4_ERR_INVALID_ARG

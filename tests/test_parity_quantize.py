@@ -108,6 +108,21 @@ def test_edge_cases():
             check(xb, fmt, rnd, 77, transpose=True)
 
 
+def test_amax_n_equals_single_calls():
+    # three tensors in one launch (one strided, one empty) against max |x| and fp4_amax
+    fp4 = lib()
+    big = dev(synth.normal((384, 1040), 12, 0, outlier_p=0.01, outlier_mult=50.0))
+    xs = [dev(synth.laplace((1000, 256), 12, 1, scale=1e-4)), big[:, :1024], dev(torch.zeros((0, 64)).bfloat16())]
+    out = torch.full((3,), -1.0, dtype=torch.float32, device="cuda")
+    fp4.fp4_amax_n(xs, out)
+    got = host(out)
+    for i, x in enumerate(xs):
+        want = float(x.float().abs().max()) if x.numel() else 0.0
+        one = torch.zeros(1, dtype=torch.float32, device="cuda")
+        fp4.fp4_amax(x, one)
+        assert got[i] == np.float32(want) == host(one)[0], i
+
+
 def test_nonfinite_stored_amax_reports_status():
     x = synth.normal((32, 64), 1, 0)
     _, _, _, st = gpu_quant(x, "E4M3", "rne", 0, g=float("inf"))
