@@ -68,6 +68,58 @@ NCU_TRAFFIC = {"gemm": {"bytes": 292.28e6, "src": "1b145e4098c46dc4",
                         "files": ["quantize.cu", "async_sm103.cuh", "fp4_device.cuh", "device_cache.h"]}}
 
 
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=10)
+    p.add_argument("--warmup", type=int, default=3)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--studies", default="all",
+                   help="comma-separated side studies to run (default: all), e.g. formats,stack")
+    p.add_argument("--no-studies", action="store_true",
+                   help="skip the side measurements after the timed steps (for ncu launch lists)")
+    p.add_argument("--tokens", type=int, default=16384,
+                   help="token count M (default: the workload's 16384; smaller only for ncu captures)")
+    return p.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (one process per GPU)
+# ---------------------------------------------------------------------------
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def dist_init(world, backend):
+    if world > 1 and not torch.distributed.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        torch.distributed.init_process_group(backend)
+
+
+def barrier(world):
+    if world > 1:
+        torch.distributed.barrier()
+
+
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """Largest value over all ranks (the slowest rank sets the time)."""
+    if world == 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# peaks, clocks, cpu baseline
+# ---------------------------------------------------------------------------
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
