@@ -55,3 +55,12 @@ def test_two_rank_gloo_max_and_reference_rank0_only():
     assert [d["world"] for d in res] == [2, 2]
     assert all(d["slowest"] == 2.5 for d in res)
     assert res[1]["reference_line"] is None  # non-zero ranks print nothing and do no work
+
+
+def test_bench_parses_its_default_arguments(monkeypatch):
+    import sys
+    import bench
+    monkeypatch.setattr(sys, "argv", ["bench.py"])
+    a = bench.parse()
+    assert a.gpus == 1 and a.steps >= 1 and a.warmup >= 3 and a.impl == "ours"
+    assert set(bench.STUDIES) >= {"formats", "stack", "gemv_shapes"}
