@@ -25,7 +25,7 @@ COMMON = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE
           "--expt-relaxed-constexpr"]
 # the quantizer's float32 steps must stay single correctly rounded operations
 PER_FILE = {"quantize.cu": ["-fmad=false"], "rht.cu": ["-fmad=false"]}
-SOURCES = ["abi.cu", "quantize.cu", "rht.cu", "gemv.cu", "gemm_sm103.cu"]
+SOURCES = ["abi.cu", "quantize.cu", "rht.cu", "gemv.cu", "gemv_umma.cu", "gemm_sm103.cu"]
 
 
 def _nvcc() -> str:

@@ -622,7 +622,9 @@ cudaError_t launch_gemv_tma(const fp4lib::GemvArgs& a, cudaStream_t st) {
 namespace fp4lib {
 
 cudaError_t launch_gemv(const GemvArgs& a, cudaStream_t st) {
-  const cudaError_t e = launch_gemv_tma(a, st);
+  cudaError_t e = launch_gemv_umma(a, st);  // batch > 8: tensor-memory accumulation
+  if (e != cudaErrorNotSupported) return e;
+  e = launch_gemv_tma(a, st);
   if (e != cudaErrorNotSupported) return e;
   // register-fed form: 16 weight rows per CTA; enough warps per CTA (split K) to put about 16
   // warps on each of the GPU's SMs in a single wave

@@ -99,5 +99,7 @@ struct GemvArgs {
   int32_t* status;
 };
 cudaError_t launch_gemv(const GemvArgs& a, cudaStream_t st);
+// batches of 9..64 on the tcgen05 tensor cores (gemv_umma.cu); cudaErrorNotSupported otherwise
+cudaError_t launch_gemv_umma(const GemvArgs& a, cudaStream_t st);
 
 }  // namespace fp4lib

@@ -61,20 +61,36 @@ def test_gemv_wide_scale_range():
     assert (qw["scales"] < 8).any() and (qw["scales"] > 0).any()  # subnormal scale codes occur
     nib = np.concatenate([qw["codes"] & 15, qw["codes"] >> 4])
     assert np.isin(np.arange(16), nib).all()
-    for b in (2, 8):
+    for b in (2, 8, 13, 64):
         run(W, synth.normal((b, K), 32, b), "bf16")
 
 
-def test_gemv_status_word_stays_clear():
+def test_gemv_ragged_rows_tensor_core_form():
+    # batches 9..64 with K % 256 == 0 take the tcgen05 form (128 weight rows per
+    # CTA, batch padded to 64 with zeros); N = 1000 leaves the last tile partly
+    # past the end of W; K = 4096 splits K over a cluster of CTAs
+    for K in (1024, 4096):
+        W = synth.normal((1000, K), 34, K, std=0.02)
+        for b in (9, 40, 64):
+            run(W, synth.normal((b, K), 34, K + b), "f32" if b != 40 else "bf16")
+
+
+def test_gemv_tensor_core_form_falls_back_for_k_not_multiple_of_256():
+    W = synth.normal((384, 1056), 35, 0, std=0.02)
+    run(W, synth.normal((33, 1056), 35, 1))
+
+
+@pytest.mark.parametrize("batch", [8, 64])
+def test_gemv_status_word_stays_clear(batch):
     fp4 = lib()
     W = synth.normal((4608, 768), 33, 0, std=0.02)
-    x = synth.normal((8, 768), 33, 1)
+    x = synth.normal((batch, 768), 33, 1)
     qw = Q.quantize(f32(W), "E4M3")
-    y = torch.empty((8, 4608), dtype=torch.float32, device="cuda")
+    y = torch.empty((batch, 4608), dtype=torch.float32, device="cuda")
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
     gw = torch.tensor([qw["amax"]], dtype=torch.float32, device="cuda")
     for _ in range(3):
-        fp4.fp4_gemv_w4a16(dev(qw["codes"]), dev(qw["scales"]), gw, dev(x), 8, 4608, 768, fp4.FP4_OUT_F32, y,
+        fp4.fp4_gemv_w4a16(dev(qw["codes"]), dev(qw["scales"]), gw, dev(x), batch, 4608, 768, fp4.FP4_OUT_F32, y,
                            dev_status=st)
     assert int(host(st)[0]) == 0
     yr, S = Gm.gemv_ref(qw["codes"], qw["scales"], qw["amax"], f32(x))
