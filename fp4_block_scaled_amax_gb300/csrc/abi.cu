@@ -430,24 +430,33 @@ fp4_status fp4_gemm(const uint8_t* Aq, const uint8_t* As, const uint8_t* Bq, con
   return cuda_status(fp4lib::launch_gemm(a, (cudaStream_t)stream));
 }
 
-fp4_status fp4_gemm_quantize(const uint8_t* Aq, const uint8_t* As, const uint8_t* Bq, const uint8_t* Bs,
-                             const float* ga, const float* gb, const int32_t* tA, const int32_t* tB, int64_t M,
-                             int64_t N, int64_t K, fp4_scale_fmt f, fp4_gemm_layout layout, const float* g_out,
-                             fp4_rounding r_out, uint64_t seed_out, fp4_sf_layout sfl_out, uint8_t* C_codes,
-                             uint8_t* C_scales, float* C_amax_out, int32_t* dev_status, fp4_stream_t stream) {
+namespace {
+
+// fp4_gemm_quantize and its dual form: row blocks (C_codes, C_scales) and/or
+// column blocks (Ct_codes, Ct_scales) of bf16(C).
+fp4_status gemm_quantize(const uint8_t* Aq, const uint8_t* As, const uint8_t* Bq, const uint8_t* Bs,
+                         const float* ga, const float* gb, const int32_t* tA, const int32_t* tB, int64_t M,
+                         int64_t N, int64_t K, fp4_scale_fmt f, fp4_gemm_layout layout, const float* g_out,
+                         fp4_rounding r_row, uint64_t seed_row, fp4_rounding r_col, uint64_t seed_col,
+                         fp4_sf_layout sfl_out, uint8_t* C_codes, uint8_t* C_scales, uint8_t* Ct_codes,
+                         uint8_t* Ct_scales, float* C_amax_out, int32_t* dev_status, fp4_stream_t stream) {
   if (layout != FP4_LAYOUT_TN || !valid_fmt((int)f)) return FP4_ERR_INVALID_ARG;
-  if (r_out != FP4_ROUND_RNE && r_out != FP4_ROUND_STOCHASTIC) return FP4_ERR_INVALID_ARG;
+  if (r_row != FP4_ROUND_RNE && r_row != FP4_ROUND_STOCHASTIC) return FP4_ERR_INVALID_ARG;
+  if (r_col != FP4_ROUND_RNE && r_col != FP4_ROUND_STOCHASTIC) return FP4_ERR_INVALID_ARG;
   if (sfl_out != FP4_SFLAYOUT_PLAIN && sfl_out != FP4_SFLAYOUT_MMA) return FP4_ERR_INVALID_ARG;
   if (f == FP4_SF_E1M6 || sweep_fmt((int)f)) return FP4_ERR_UNSUPPORTED;
-  if (Aq == nullptr || As == nullptr || Bq == nullptr || Bs == nullptr || C_codes == nullptr ||
-      C_scales == nullptr || g_out == nullptr)
+  if (Aq == nullptr || As == nullptr || Bq == nullptr || Bs == nullptr || g_out == nullptr)
+    return FP4_ERR_INVALID_ARG;
+  // each output is a pair of buffers, given together; at least one pair
+  if ((C_codes == nullptr) != (C_scales == nullptr) || (Ct_codes == nullptr) != (Ct_scales == nullptr) ||
+      (C_codes == nullptr && Ct_codes == nullptr))
     return FP4_ERR_INVALID_ARG;
   if (f != FP4_SF_E8M0 && (ga == nullptr || gb == nullptr)) return FP4_ERR_INVALID_ARG;
   if (f == FP4_SF_UE5M3 && (tA == nullptr || tB == nullptr)) return FP4_ERR_INVALID_ARG;
   if (M <= 0 || N <= 0 || K <= 0 || M % 128 != 0 || N % 128 != 0 || K % 256 != 0) return FP4_ERR_SHAPE;
   if (M % 256 != 0) return FP4_ERR_UNSUPPORTED;  // the quantizing epilogue runs on CTA pairs
   if (!aligned16(Aq) || !aligned16(As) || !aligned16(Bq) || !aligned16(Bs) || !aligned16(C_codes) ||
-      !aligned16(C_scales))
+      !aligned16(C_scales) || !aligned16(Ct_codes) || !aligned16(Ct_scales))
     return FP4_ERR_ALIGNMENT;
   cudaStream_t st = (cudaStream_t)stream;
   if (C_amax_out != nullptr) {
@@ -475,10 +484,37 @@ fp4_status fp4_gemm_quantize(const uint8_t* Aq, const uint8_t* As, const uint8_t
   a.q_scales = C_scales;
   a.q_g = g_out;
   a.q_amax_out = C_amax_out;
-  a.q_seed = seed_out;
-  a.q_sr = r_out == FP4_ROUND_STOCHASTIC;
+  a.q_seed = seed_row;
+  a.q_sr = r_row == FP4_ROUND_STOCHASTIC;
   a.q_mma = sfl_out == FP4_SFLAYOUT_MMA;
+  a.qt_codes = Ct_codes;
+  a.qt_scales = Ct_scales;
+  a.qt_seed = seed_col;
+  a.qt_sr = r_col == FP4_ROUND_STOCHASTIC;
   return cuda_status(fp4lib::launch_gemm(a, st));
+}
+
+}  // namespace
+
+fp4_status fp4_gemm_quantize(const uint8_t* Aq, const uint8_t* As, const uint8_t* Bq, const uint8_t* Bs,
+                             const float* ga, const float* gb, const int32_t* tA, const int32_t* tB, int64_t M,
+                             int64_t N, int64_t K, fp4_scale_fmt f, fp4_gemm_layout layout, const float* g_out,
+                             fp4_rounding r_out, uint64_t seed_out, fp4_sf_layout sfl_out, uint8_t* C_codes,
+                             uint8_t* C_scales, float* C_amax_out, int32_t* dev_status, fp4_stream_t stream) {
+  if (C_codes == nullptr || C_scales == nullptr) return FP4_ERR_INVALID_ARG;
+  return gemm_quantize(Aq, As, Bq, Bs, ga, gb, tA, tB, M, N, K, f, layout, g_out, r_out, seed_out, FP4_ROUND_RNE, 0,
+                       sfl_out, C_codes, C_scales, nullptr, nullptr, C_amax_out, dev_status, stream);
+}
+
+fp4_status fp4_gemm_quantize_dual(const uint8_t* Aq, const uint8_t* As, const uint8_t* Bq, const uint8_t* Bs,
+                                  const float* ga, const float* gb, const int32_t* tA, const int32_t* tB,
+                                  int64_t M, int64_t N, int64_t K, fp4_scale_fmt f, fp4_gemm_layout layout,
+                                  const float* g_out, fp4_rounding r_row, uint64_t seed_row, fp4_rounding r_col,
+                                  uint64_t seed_col, fp4_sf_layout sfl_out, uint8_t* C_codes, uint8_t* C_scales,
+                                  uint8_t* Ct_codes, uint8_t* Ct_scales, float* C_amax_out, int32_t* dev_status,
+                                  fp4_stream_t stream) {
+  return gemm_quantize(Aq, As, Bq, Bs, ga, gb, tA, tB, M, N, K, f, layout, g_out, r_row, seed_row, r_col, seed_col,
+                       sfl_out, C_codes, C_scales, Ct_codes, Ct_scales, C_amax_out, dev_status, stream);
 }
 
 fp4_status fp4_gemv_w4a16(const uint8_t* Wq, const uint8_t* Ws, const float* gw, const void* x_bf16,

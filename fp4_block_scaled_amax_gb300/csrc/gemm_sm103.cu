@@ -294,6 +294,10 @@ struct Params {
   float* q_amax_out;
   uint64_t q_seed;
   int q_sr, q_mma;
+  uint8_t* qt_codes;  // column blocks (nullable; q_codes may then be null)
+  uint8_t* qt_scales;
+  uint64_t qt_seed;
+  int qt_sr;
   // multi-pass GEMM (UE5M3 scale windows): add to C instead of storing it, and
   // skip the launch when window wa of A or wb of B is unused (device counts)
   int accumulate;
@@ -357,13 +361,21 @@ __device__ __forceinline__ void store_block(const uint32_t (&r)[2][32], float al
   }
 }
 
-// Quantizing epilogue of one warp: row `row` (this lane) x 64 columns from
-// col0, exactly what fp4_quantize (E4M3 scales, 16-element blocks along N)
-// makes of the bf16 output the other epilogue would store: bf16(acc * alpha),
-// block amax, scale, RNE or Philox SR at output-layout indices row * N + col,
-// 32 code bytes and 4 scale bytes per lane.
-__device__ __forceinline__ void quant_epilogue(const uint32_t (&r)[2][32], float alpha, const Params& p, int row,
-                                               int col0, float s_enc_out, float& amax_local) {
+// Quantizing epilogue of one warp: rows row0 .. row0 + 31 (row0 + lane in
+// this lane) x 64 columns from col0 of bf16(acc * alpha), the values the
+// other epilogue would store, quantized as fp4_quantize would (E4M3 scales,
+// block amax, scale, RNE or Philox SR at output-layout indices):
+//  * row blocks (p.q_codes): 16 columns of the lane's row, indices
+//    row * N + col; 32 code bytes and 4 scale bytes per lane;
+//  * column blocks (p.qt_codes), the layout of C^T: 16 rows of one column,
+//    indices col * M + row.  The warp's 32 x 64 values pass through its
+//    2 KB staging buffer 32 columns at a time (row-major, 64 bytes a row,
+//    16-byte chunks XOR-swizzled by row); lane l then holds columns 2 (l % 16)
+//    and + 1 of rows 16 (l / 16) .. + 15 and quantizes both 16-row blocks.
+__device__ __forceinline__ void quant_epilogue(const uint32_t (&r)[2][32], float alpha, const Params& p, int row0,
+                                               int lane, int col0, float s_enc_out, float& amax_local,
+                                               uint8_t* stage) {
+  const int row = row0 + lane;
   uint32_t w[32];
 #pragma unroll
   for (int i = 0; i < 32; ++i) {
@@ -373,27 +385,64 @@ __device__ __forceinline__ void quant_epilogue(const uint32_t (&r)[2][32], float
     const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
     w[i] = *reinterpret_cast<const uint32_t*>(&h);
   }
-  uint32_t q[8];
-  uint32_t sc = 0;
+  if (p.q_codes != nullptr) {
+    uint32_t q[8];
+    uint32_t sc = 0;
 #pragma unroll
-  for (int blk = 0; blk < 4; ++blk) {
-    const uint32_t* wb = w + 8 * blk;
-    const float a = fp4dev::absmax_words(wb, 8);
-    amax_local = fmaxf(amax_local, a);
-    const fp4dev::BlockScale bs = fp4dev::block_scale<fp4dev::SF_E4M3, true>(a, s_enc_out);
-    const uint64_t idx0 = (uint64_t)row * (uint64_t)p.N + (uint64_t)(col0 + 16 * blk);
-    const uint2 qq = p.q_sr ? fp4dev::quant16<true>(wb, bs.r, p.q_seed, idx0)
-                            : fp4dev::quant16<false>(wb, bs.r, p.q_seed, idx0);
-    q[2 * blk] = qq.x;
-    q[2 * blk + 1] = qq.y;
-    sc |= bs.code << (8 * blk);
+    for (int blk = 0; blk < 4; ++blk) {
+      const uint32_t* wb = w + 8 * blk;
+      const float a = fp4dev::absmax_words(wb, 8);
+      amax_local = fmaxf(amax_local, a);
+      const fp4dev::BlockScale bs = fp4dev::block_scale<fp4dev::SF_E4M3, true>(a, s_enc_out);
+      const uint64_t idx0 = (uint64_t)row * (uint64_t)p.N + (uint64_t)(col0 + 16 * blk);
+      const uint2 qq = p.q_sr ? fp4dev::quant16<true>(wb, bs.r, p.q_seed, idx0)
+                              : fp4dev::quant16<false>(wb, bs.r, p.q_seed, idx0);
+      q[2 * blk] = qq.x;
+      q[2 * blk + 1] = qq.y;
+      sc |= bs.code << (8 * blk);
+    }
+    uint4* dst = reinterpret_cast<uint4*>(p.q_codes + (int64_t)row * (p.N / 2) + col0 / 2);
+    dst[0] = make_uint4(q[0], q[1], q[2], q[3]);
+    dst[1] = make_uint4(q[4], q[5], q[6], q[7]);
+    const int64_t nb = p.N / 16, b = col0 / 16;
+    const int64_t off = p.q_mma ? fp4dev::mma_sf_offset(row, b, nb) : (int64_t)row * nb + b;
+    *reinterpret_cast<uint32_t*>(p.q_scales + off) = sc;
+  } else {
+    amax_local = fmaxf(amax_local, fp4dev::absmax_words(w, 32));
   }
-  uint4* dst = reinterpret_cast<uint4*>(p.q_codes + (int64_t)row * (p.N / 2) + col0 / 2);
-  dst[0] = make_uint4(q[0], q[1], q[2], q[3]);
-  dst[1] = make_uint4(q[4], q[5], q[6], q[7]);
-  const int64_t nb = p.N / 16, b = col0 / 16;
-  const int64_t off = p.q_mma ? fp4dev::mma_sf_offset(row, b, nb) : (int64_t)row * nb + b;
-  *reinterpret_cast<uint32_t*>(p.q_scales + off) = sc;
+  if (p.qt_codes == nullptr) return;
+  const int cp = lane & 15, rb = lane >> 4;
+  const int m = row0 + 16 * rb;  // first row of this lane's blocks
+  const int64_t mh = p.M / 2, nbt = p.M / 16, bt = m / 16;
+#pragma unroll
+  for (int hh = 0; hh < 2; ++hh) {
+    __syncwarp();  // the previous half's reads are done
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      *reinterpret_cast<uint4*>(stage + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4)) =
+          make_uint4(w[16 * hh + 4 * j], w[16 * hh + 4 * j + 1], w[16 * hh + 4 * j + 2], w[16 * hh + 4 * j + 3]);
+    __syncwarp();
+    uint32_t v[16];  // rows m .. m + 15, columns (2 cp, 2 cp + 1) of this half
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const int rr = 16 * rb + i;
+      v[i] = *reinterpret_cast<const uint32_t*>(stage + rr * 64 + (((cp >> 2) ^ ((rr >> 1) & 3)) << 4) + (cp & 3) * 4);
+    }
+    const uint32_t am2 = fp4dev::absmax_words2(v, 16);
+    const fp4dev::BlockScale b0 = fp4dev::block_scale<fp4dev::SF_E4M3, true>(fp4dev::bf16_lo(am2), s_enc_out);
+    const fp4dev::BlockScale b1 = fp4dev::block_scale<fp4dev::SF_E4M3, true>(fp4dev::bf16_hi(am2), s_enc_out);
+    const int n = col0 + 32 * hh + 2 * cp;  // the low column; its C^T row
+    const uint64_t i0 = (uint64_t)n * (uint64_t)p.M + (uint64_t)m;
+    const uint2 q0 = p.qt_sr ? fp4dev::quant16_col<true, false>(v, b0.r, p.qt_seed, i0)
+                             : fp4dev::quant16_col<false, false>(v, b0.r, p.qt_seed, i0);
+    const uint2 q1 = p.qt_sr ? fp4dev::quant16_col<true, true>(v, b1.r, p.qt_seed, i0 + (uint64_t)p.M)
+                             : fp4dev::quant16_col<false, true>(v, b1.r, p.qt_seed, i0 + (uint64_t)p.M);
+    *reinterpret_cast<uint2*>(p.qt_codes + (int64_t)n * mh + m / 2) = q0;
+    *reinterpret_cast<uint2*>(p.qt_codes + (int64_t)(n + 1) * mh + m / 2) = q1;
+    p.qt_scales[p.q_mma ? fp4dev::mma_sf_offset(n, bt, nbt) : (int64_t)n * nbt + bt] = (uint8_t)b0.code;
+    p.qt_scales[p.q_mma ? fp4dev::mma_sf_offset(n + 1, bt, nbt) : (int64_t)(n + 1) * nbt + bt] = (uint8_t)b1.code;
+  }
+  __syncwarp();
 }
 
 // Epilogue scale of the accumulator: alpha = 1 / (s_encA * s_encB), times
@@ -995,8 +1044,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (lane == 0) mbar_arrive_cluster(lead_acc_empty);
       if (nt * BN + EPI_COLS * cblk >= p.N) continue;  // a slab past N (half tile): no output
       if constexpr (QOUT) {
-        quant_epilogue(r, alpha, p, mp * PM + BM * (int)crank + 32 * quarter + lane, nt * BN + EPI_COLS * cblk,
-                       s_enc_out, amax_local);
+        quant_epilogue(r, alpha, p, mp * PM + BM * (int)crank + 32 * quarter, lane, nt * BN + EPI_COLS * cblk,
+                       s_enc_out, amax_local, stage_buf);
       } else {
         store_block<BF16, PL>(r, alpha, stage_buf, stage_addr, &tmap_c, mp * PM + BM * (int)crank + 32 * quarter,
                               nt * BN + EPI_COLS * cblk, lane, p.accumulate != 0);
@@ -1129,8 +1178,9 @@ cudaError_t launch_pair(const fp4lib::GemmArgs& a, cudaStream_t st) {
   if (err != cudaSuccess) return err;
   if (max_clusters <= 0) return cudaErrorInvalidConfiguration;
   CUtensorMap ma, mb, mc;
-  // with a quantized output the C map is never used; it is built over the code buffer
-  void* cbase = QOUT ? static_cast<void*>(a.q_codes) : a.C;
+  // with a quantized output the C map is never used; it is built over a code
+  // buffer of the same size (M x N/2 bytes, either layout)
+  void* cbase = QOUT ? static_cast<void*>(a.q_codes != nullptr ? a.q_codes : a.qt_codes) : a.C;
   const int64_t cn = QOUT ? a.N / 4 : a.N, cld = QOUT ? a.N / 4 : a.ldc;
   if (!make_code_map(&ma, a.Aq, a.M, a.K / 2, BM) || !make_code_map(&mb, a.Bq, a.N, a.K / 2, BN / 2) ||
       !make_out_map(&mc, cbase, a.M, cn, cld, QOUT ? true : BF16, PL::OUT_ROW_BYTES))
@@ -1158,6 +1208,10 @@ cudaError_t launch_pair(const fp4lib::GemmArgs& a, cudaStream_t st) {
   p.q_seed = a.q_seed;
   p.q_sr = a.q_sr ? 1 : 0;
   p.q_mma = a.q_mma ? 1 : 0;
+  p.qt_codes = a.qt_codes;
+  p.qt_scales = a.qt_scales;
+  p.qt_seed = a.qt_seed;
+  p.qt_sr = a.qt_sr ? 1 : 0;
   const int units = (int)((a.M / (2 * BM)) * ((a.N + BN - 1) / BN));
   const int clusters = units < max_clusters ? units : max_clusters;
   cfg.gridDim = dim3((unsigned)(2 * clusters), 1, 1);

@@ -74,13 +74,19 @@ struct GemmArgs {
   void* C;
   int32_t* status;
   // quantized output instead of C (fp4_gemm_quantize): NVFP4 codes and scales
-  // of bf16(C) under the stored global amax q_g
+  // of bf16(C) in row blocks (nullable when qt_codes is given) under the
+  // stored global amax q_g
   bool qout;
   uint8_t *q_codes, *q_scales;
   const float* q_g;
   float* q_amax_out;  // nullable: max |bf16(C)|
   uint64_t q_seed;
   bool q_sr, q_mma;
+  // column-block output of bf16(C) (16 elements along M, codes [N, M/2]);
+  // nullable, as is q_codes when this one is given
+  uint8_t *qt_codes, *qt_scales;
+  uint64_t qt_seed;
+  bool qt_sr;
   // multi-pass GEMM over UE5M3 scale windows: add into C (float32 output),
   // and skip the launch if window wa of A or wb of B is unused
   bool accumulate;

@@ -74,6 +74,8 @@ _SIGS = {
                         _VP, _VP]),
     "fp4_gemm_quantize": (_I32, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _I64, _I64, _I64, _I32, _I32, _VP, _I32,
                                  _U64, _I32, _VP, _VP, _VP, _VP, _VP]),
+    "fp4_gemm_quantize_dual": (_I32, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _I64, _I64, _I64, _I32, _I32, _VP,
+                                      _I32, _U64, _I32, _U64, _I32, _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
     "fp4_ue5m3_windows": (_I32, [_VP, _I64, _VP, _VP, _VP, _VP, _VP]),
     "fp4_gemm_ue5m3_windows": (_I32, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _I64, _I64, _I64, _VP, _I64,
                                       _VP, _VP]),
@@ -228,6 +230,16 @@ def fp4_gemm_quantize(Aq, As, Bq, Bs, ga, gb, tA, tB, M, N, K, fmt, g_out, round
                                     M, N, K, _fmt(fmt), FP4_LAYOUT_TN, _ptr(g_out), int(rounding), int(seed),
                                     int(sf_layout), _ptr(C_codes), _ptr(C_scales), _ptr(C_amax_out),
                                     _ptr(dev_status), _stream(stream)), "fp4_gemm_quantize")
+
+
+def fp4_gemm_quantize_dual(Aq, As, Bq, Bs, ga, gb, tA, tB, M, N, K, fmt, g_out, r_row, seed_row, r_col, seed_col,
+                           sf_layout, C_codes, C_scales, Ct_codes, Ct_scales, C_amax_out=None, dev_status=None,
+                           stream=None):
+    _check(_lib().fp4_gemm_quantize_dual(_ptr(Aq), _ptr(As), _ptr(Bq), _ptr(Bs), _ptr(ga), _ptr(gb), _ptr(tA),
+                                         _ptr(tB), M, N, K, _fmt(fmt), FP4_LAYOUT_TN, _ptr(g_out), int(r_row),
+                                         int(seed_row), int(r_col), int(seed_col), int(sf_layout), _ptr(C_codes),
+                                         _ptr(C_scales), _ptr(Ct_codes), _ptr(Ct_scales), _ptr(C_amax_out),
+                                         _ptr(dev_status), _stream(stream)), "fp4_gemm_quantize_dual")
 
 
 def fp4_ue5m3_windows(scales, t_out, n_windows_out, out, dev_status=None, stream=None):

@@ -316,6 +316,26 @@ fp4_status fp4_gemm_quantize(const uint8_t* Aq, const uint8_t* As, const uint8_t
                              fp4_sf_layout sfl_out, uint8_t* C_codes, uint8_t* C_scales,
                              float* C_amax_out, int32_t* dev_status, fp4_stream_t stream);
 
+/* fp4_gemm_quantize with both quantized layouts of C from the one GEMM: row
+ * blocks (16 elements along N: codes [M, N/2], what fp4_quantize(bf16(C),
+ * transpose = 0, r_row, seed_row) makes) and column blocks (16 elements along
+ * M, the layout of C^T: codes [N, M/2], E4M3 scales of (n, m/16), Philox
+ * indices n * M + m: what fp4_quantize(bf16(C), transpose = 1, r_col,
+ * seed_col) makes), under the one stored global amax g_out, as
+ * fp4_quantize_dual defines them.  The column layout is the operand the
+ * backward pass needs along M (the next layer's wgrad takes X^T; dgrad's
+ * output dX feeds the previous layer's wgrad as dX^T): [UE5M3] "Что
+ * сделали" runs every linear in FP4 forward and backward.  Either pair of
+ * outputs may be NULL (both pointers of a pair together), not both;
+ * C_amax_out as fp4_gemm_quantize.  Requirements as fp4_gemm_quantize. */
+fp4_status fp4_gemm_quantize_dual(const uint8_t* Aq, const uint8_t* As, const uint8_t* Bq, const uint8_t* Bs,
+                                  const float* ga, const float* gb, const int32_t* tA, const int32_t* tB,
+                                  int64_t M, int64_t N, int64_t K, fp4_scale_fmt f, fp4_gemm_layout layout,
+                                  const float* g_out, fp4_rounding r_row, uint64_t seed_row,
+                                  fp4_rounding r_col, uint64_t seed_col, fp4_sf_layout sfl_out,
+                                  uint8_t* C_codes, uint8_t* C_scales, uint8_t* Ct_codes, uint8_t* Ct_scales,
+                                  float* C_amax_out, int32_t* dev_status, fp4_stream_t stream);
+
 /* Weight-only NVFP4 linear ([W4A16] "Метод"): y[b, n] = sum_k deq(W)[n, k] * x[b, k],
  * deq(W) = e2m1 * s_b / s_enc(*gw) (E4M3 scales, G = 16, FP4_SFLAYOUT_PLAIN),
  * x bf16 [batch, K] (row stride K), float32 accumulation, y [batch, N] float32

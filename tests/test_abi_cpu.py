@@ -120,6 +120,27 @@ def test_gemm_argument_errors():
     assert g(C=None) == fp4.FP4_ERR_INVALID_ARG
 
 
+def test_gemm_quantize_dual_argument_errors():
+    lib = _need_lib()
+
+    def g(**kw):
+        a = dict(M=256, N=256, K=256, rr=0, rc=0, sfl=0, C=P, Cs=P, Ct=P, Cts=P, A=P)
+        a.update(kw)
+        return lib.fp4_gemm_quantize_dual(a["A"], P, P, P, P, P, None, None, a["M"], a["N"], a["K"], 0, 0, P,
+                                          a["rr"], 0, a["rc"], 0, a["sfl"], a["C"], a["Cs"], a["Ct"], a["Cts"],
+                                          None, None, None)
+
+    assert g(C=None, Cs=None, Ct=None, Cts=None) == fp4.FP4_ERR_INVALID_ARG  # no output at all
+    assert g(Cs=None) == fp4.FP4_ERR_INVALID_ARG                            # half a pair
+    assert g(Cts=None) == fp4.FP4_ERR_INVALID_ARG
+    assert g(rc=2) == fp4.FP4_ERR_INVALID_ARG
+    assert g(sfl=2) == fp4.FP4_ERR_INVALID_ARG
+    assert g(M=128) == fp4.FP4_ERR_UNSUPPORTED                              # CTA pairs only
+    assert g(K=128) == fp4.FP4_ERR_SHAPE
+    assert g(Ct=P + 8) == fp4.FP4_ERR_ALIGNMENT
+    assert g(A=P + 1) == fp4.FP4_ERR_ALIGNMENT
+
+
 def test_gemv_and_misc_argument_errors():
     lib = _need_lib()
     assert lib.fp4_gemv_w4a16(P, P, P, P, 0, 128, 256, 0, P, None, None) == fp4.FP4_ERR_SHAPE

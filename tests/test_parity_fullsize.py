@@ -256,6 +256,36 @@ def test_gemm_quantize_epilogue_fullsize_identical(step):
         assert torch.equal(c1, c2) and torch.equal(s1, s2), rnd
 
 
+def test_gemm_quantize_dual_epilogue_fullsize_identical(step):
+    # fp4_gemm_quantize_dual on the forward GEMM: row blocks == fp4_quantize(Y),
+    # column blocks == fp4_quantize(Y, transpose = 1), byte for byte
+    bench, d, s = step
+    fp4 = s.fp4
+    M, N, K = bench.M_TOK, bench.N_FFN, bench.K_HID
+    qX, qW = s.q["X"], s.q["W"]
+    aX, aW = s.amax[0:1], s.amax[1:2]
+    dev = s.Y.device
+    Y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    fp4.fp4_gemm(qX[0], qX[1], qW[0], qW[1], aX, aW, None, None, M, N, K, "E4M3", fp4.FP4_OUT_BF16, Y)
+    gY = Y.float().abs().max().reshape(1)
+    RNE, SR, MMA = fp4.FP4_ROUND_RNE, fp4.FP4_ROUND_STOCHASTIC, fp4.FP4_SFLAYOUT_MMA
+    rc, rs = torch.empty((M, N // 2), dtype=torch.uint8, device=dev), torch.empty(M * N // 16, dtype=torch.uint8,
+                                                                                 device=dev)
+    tc, ts = torch.empty((N, M // 2), dtype=torch.uint8, device=dev), torch.empty_like(rs)
+    fp4.fp4_quantize(Y, "E4M3", RNE, 0, gY, False, MMA, rc, rs, None)
+    fp4.fp4_quantize(Y, "E4M3", SR, 91, gY, True, MMA, tc, ts, None)
+    fc, fs, ftc, fts = torch.empty_like(rc), torch.empty_like(rs), torch.empty_like(tc), torch.empty_like(ts)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    amax = torch.zeros(1, dtype=torch.float32, device=dev)
+    fp4.fp4_gemm_quantize_dual(qX[0], qX[1], qW[0], qW[1], aX, aW, None, None, M, N, K, "E4M3", gY, RNE, 0, SR, 91,
+                               MMA, fc, fs, ftc, fts, amax, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    assert torch.equal(fc, rc) and torch.equal(fs, rs)
+    assert torch.equal(ftc, tc) and torch.equal(fts, ts)
+    assert float(amax) == float(gY)
+
+
 def test_ue5m3_windows_fullsize_one_window_identical(step):
     # X and W quantized with UE5M3 scales (fresh amaxes) fit one window: the window
     # GEMM equals the single-shift GEMM bit for bit at 16384 x 11008 x 4096
