@@ -1091,17 +1091,23 @@ def gemv_shapes_study(step, reps=5, launches=32):
 
 def fused_epilogue_study(step, flush, reps=5):
     """The forward GEMM Y = X W^T with Y quantized for the next layer (NVFP4,
-    RNE rows, the stored amax of Y): the GEMM writing bf16 Y followed by the
-    row quantizer, against the GEMM quantizing Y in its epilogue
-    (fp4_gemm_quantize).  Outside the timed step."""
+    the stored amax of Y), outside the timed step:
+      * rows only (RNE): the GEMM writing bf16 Y followed by the row
+        quantizer, against the GEMM quantizing Y in its epilogue
+        (fp4_gemm_quantize);
+      * rows (RNE) and columns (SR, the layout of Y^T the backward pass
+        takes): the GEMM, then the one-read dual quantizer, against the dual
+        quantizing epilogue (fp4_gemm_quantize_dual)."""
     fp4 = step.fp4
     M, N, K = M_TOK, N_FFN, K_HID
     qX, qW = step.q["X"], step.q["W"]
     aX, aW = step.amax[0:1], step.amax[1:2]
-    BF, RNE, MMA = fp4.FP4_OUT_BF16, fp4.FP4_ROUND_RNE, fp4.FP4_SFLAYOUT_MMA
+    BF, RNE, SR, MMA = fp4.FP4_OUT_BF16, fp4.FP4_ROUND_RNE, fp4.FP4_ROUND_STOCHASTIC, fp4.FP4_SFLAYOUT_MMA
     dev = step.Y.device
     codes = torch.empty((M, N // 2), dtype=torch.uint8, device=dev)
     scales = torch.empty(M * N // 16, dtype=torch.uint8, device=dev)
+    tcodes = torch.empty((N, M // 2), dtype=torch.uint8, device=dev)
+    tscales = torch.empty(M * N // 16, dtype=torch.uint8, device=dev)
     fp4.fp4_gemm(qX[0], qX[1], qW[0], qW[1], aX, aW, None, None, M, N, K, "E4M3", BF, step.Y)
     gY = step.Y.float().abs().max().reshape(1)  # the stored amax of Y
     st = torch.cuda.current_stream()
@@ -1114,8 +1120,17 @@ def fused_epilogue_study(step, flush, reps=5):
         fp4.fp4_gemm_quantize(qX[0], qX[1], qW[0], qW[1], aX, aW, None, None, M, N, K, "E4M3", gY, RNE, 0, MMA,
                               codes, scales)
 
+    def two_calls_dual():
+        fp4.fp4_gemm(qX[0], qX[1], qW[0], qW[1], aX, aW, None, None, M, N, K, "E4M3", BF, step.Y)
+        fp4.fp4_quantize_dual(step.Y, "E4M3", RNE, 0, SR, 9, gY, MMA, codes, scales, tcodes, tscales, None)
+
+    def one_call_dual():
+        fp4.fp4_gemm_quantize_dual(qX[0], qX[1], qW[0], qW[1], aX, aW, None, None, M, N, K, "E4M3", gY, RNE, 0, SR,
+                                   9, MMA, codes, scales, tcodes, tscales)
+
     res = {}
-    for name, fn in (("gemm_then_quantize", two_calls), ("gemm_quantize_epilogue", one_call)):
+    for name, fn in (("gemm_then_quantize", two_calls), ("gemm_quantize_epilogue", one_call),
+                     ("gemm_then_quantize_dual", two_calls_dual), ("gemm_quantize_dual_epilogue", one_call_dual)):
         fn()
         ts = []
         for _ in range(reps):
@@ -1127,8 +1142,9 @@ def fused_epilogue_study(step, flush, reps=5):
             torch.cuda.synchronize()
             ts.append(e0.elapsed_time(e1))
         res[name] = round(statistics.median(ts), 4)
-    return {"gemm": f"fwd {M}x{N}x{K} E4M3, Y -> NVFP4 rows (RNE, stored amax)", "unit": "ms", **res,
-            "fused_tflops": round(2 * M * N * K / (res["gemm_quantize_epilogue"] * 1e-3) / 1e12, 1)}
+    return {"gemm": f"fwd {M}x{N}x{K} E4M3, Y -> NVFP4 rows (RNE) [+ columns (SR)], stored amax", "unit": "ms", **res,
+            "fused_tflops": round(2 * M * N * K / (res["gemm_quantize_epilogue"] * 1e-3) / 1e12, 1),
+            "fused_dual_tflops": round(2 * M * N * K / (res["gemm_quantize_dual_epilogue"] * 1e-3) / 1e12, 1)}
 
 
 def make_inputs():
@@ -1149,7 +1165,24 @@ def src_hash(names):
 
 
 STUDIES = ("formats", "cublaslt", "config2", "stack", "gemv_shapes", "step_graph", "gemv_graph", "variants",
-           "windows", "qmodes", "sweep", "hadamard", "fused")
+           "windows", "qmodes", "sweep", "hadamard", "fused", "ceiling")
+
+
+def tensor_ceiling_study():
+    """The tensor cores' FLOP per clock per SM on this GPU, from the package's
+    tc_ceiling program (each SM streams 2048 MMAs of one form from one warp,
+    no waits between them): kind::f16 bf16 (M 128, N 256, K 16), the FP4
+    GEMM's own form (kind::mxf4nvf4 scale_vec::4X, CTA pair, M 256, N 256,
+    K 64) and MXFP4 (scale_vec::2X, M 128).  Runs as its own process, outside
+    the timed step."""
+    from fp4_block_scaled_amax_gb300 import build as b
+    exe = b.build_ceiling()
+    r = subprocess.run([exe], capture_output=True, text=True, timeout=120)
+    if r.returncode != 0:
+        return {"error": (r.stdout + r.stderr).strip()[-300:]}
+    d = json.loads(r.stdout.strip().splitlines()[-1])
+    d["fp4_to_bf16_per_clock"] = round(d["nvf4_pair_flop_per_clk_sm"] / d["bf16_flop_per_clk_sm"], 3)
+    return d
 
 
 def run_ours(args, rank, world, local):
@@ -1209,7 +1242,7 @@ def run_ours(args, rank, world, local):
     qtraffic_v = traffic_of("quant_dual")
     gvtraffic_v = traffic_of("gemv")
 
-    qmodes = sweep = hadamard = fused_ep = variants = windows = gv_graph = step_graph = gv_shapes = None
+    qmodes = sweep = hadamard = fused_ep = variants = windows = gv_graph = step_graph = gv_shapes = ceiling = None
     formats = cublas = cfg2 = stack = None
     chosen = set() if args.no_studies else (
         set(STUDIES) if args.studies == "all" else set(x.strip() for x in args.studies.split(",")))
@@ -1242,6 +1275,8 @@ def run_ours(args, rank, world, local):
         hadamard = hadamard_study(step, step.fp4, flush, device)
     if "fused" in chosen:
         fused_ep = fused_epilogue_study(step, flush)
+    if "ceiling" in chosen:
+        ceiling = tensor_ceiling_study()
     e2e = None
     if not args.no_e2e:
         e2e = run_e2e(step, d, args, world, device)
@@ -1298,6 +1333,15 @@ def run_ours(args, rank, world, local):
         "gpu_launches": step.launches_per_step * args.steps,
         "clocks": clk.summary(),
     }
+    if ceiling is not None:
+        line["tensor_ceiling"] = ceiling
+        mhz = line["clocks"].get("sm_mhz")
+        if "nvf4_pair_flop_per_clk_sm" in ceiling and mhz:
+            # the FP4 MMA's own ceiling at the SM clock sampled during the timed steps
+            c = ceiling["nvf4_pair_flop_per_clk_sm"] * ceiling["sms"] * mhz * 1e6 / 1e12
+            line["roofline"]["mma_ceiling"] = {
+                "tflops": round(c, 1), "frac": round(gemm_tflops / c, 4), "sm_mhz": mhz,
+                "basis": "tc_ceiling: kind::mxf4nvf4 4X pair FLOP/clk/SM x SMs x median SM clock of the timed steps"}
     if e2e is not None:
         line["e2e"] = e2e
     if rank == 0 and not args.no_cpu_baseline:
