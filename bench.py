@@ -1030,9 +1030,11 @@ def gemv_shapes_study(step, reps=5, launches=32):
     3584 and W_down 3584 x 18944 (NVFP4, quantized once), at batch 1, 8 and
     64: per-launch time over `launches` back-to-back launches that rotate over
     enough weight copies to exceed L2 (each launch streams its weights from
-    HBM), issued one by one and replayed from a CUDA graph.  Every batch runs
-    the TMA-fed kernel (K is a multiple of 256); W_down's long K splits over
-    clusters of CTAs.  Outside the timed step."""
+    HBM), issued one by one and replayed from a CUDA graph.  K is a multiple
+    of 256 on both shapes, so batches 1 and 8 run the TMA-fed mma.sync kernel
+    (k_gemv_w4a16_tma) and batch 64 the tcgen05 one (k_gemv_w4a16_umma); the
+    long K of W_down splits over clusters of CTAs in both.  Outside the
+    timed step."""
     from fp4_block_scaled_amax_gb300 import synth
     fp4 = step.fp4
     dev = step.Y.device
