@@ -17,7 +17,9 @@
 // Two forms share the roles below.  When M is a multiple of 256, clusters of
 // two CTAs run cta_group::2 MMAs on 256 x 256 output tiles (k_gemm_fp4_pair):
 // each SM holds half of the B tile, so it streams A + B/2 per K step.
-// Otherwise one CTA per SM runs 128 x 256 tiles (k_gemm_fp4).
+// Otherwise one CTA per SM runs 128 x 256 tiles (k_gemm_fp4).  N is a
+// multiple of 128: a half last tile reads zero-filled code rows (the TMA's
+// out-of-range fill) and stores nothing past N.
 //
 // Kernel structure (one CTA per SM, persistent over 128 x 256 output tiles,
 // 23 warps):
@@ -40,9 +42,14 @@
 //   warps 7-22   epilogue: each warp drains 32 rows x 64 columns of the
 //                float32 accumulator with tcgen05.ld, releases the tensor
 //                memory at once (the next tile's MMAs overlap the rest), scales,
-//                converts and stages 32-row x 16-byte blocks in shared memory
-//                (512 bytes per warp, which leaves room for a 4-stage ring), and
-//                writes them with TMA bulk-tensor stores.
+//                converts and stages 32-row blocks of 16-byte rows (long K: 512
+//                bytes per warp, which leaves room for a 4-stage ring) or
+//                64-byte rows (2 KB) in shared memory, and writes them with TMA
+//                bulk-tensor stores.  With a quantized output
+//                (fp4_gemm_quantize[_dual], CTA pairs) the warp instead
+//                quantizes bf16(acc * alpha): row blocks from its registers,
+//                column blocks (the layout of C^T) after passing the values
+//                through its 2 KB staging buffer.
 // Every mbarrier wait is bounded: on expiry the CTA records FP4_ERR_TIMEOUT in
 // the status word and winds down instead of spinning.  Once aborted, the
 // producers issue no further copies, and the CTA waits a fixed ~10 ms for

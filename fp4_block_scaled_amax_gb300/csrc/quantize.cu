@@ -11,14 +11,23 @@
 //
 // Kernels:
 //   k_amax            max|x| of a bf16 matrix (fresh global amax), 2 B/elem read.
+//   k_amax_n          the same for up to eight matrices in one launch.
 //   k_quant_rows      blocks along K; one thread per 16 elements straight from
 //                     two 128-bit loads; 2 + 0.5 + 1/G B per element.
+//   k_quant_dual_tma  persistent dual (row + transposed) quantizer over 128 x
+//                     128 tiles loaded by TMA into a 4-stage ring; transposed
+//                     codes and both scale layouts staged and stored by TMA /
+//                     bulk copies (MMA scale layout, G = 16, M and K multiples
+//                     of 128): 2 + 2 * (0.5 + 1/16) B per element.
 //   k_quant_tile      64 x 128 tile staged in shared memory; writes the
 //                     transposed quantization (blocks along M) and, in the dual
 //                     form, the row quantization from the same read:
-//                     2 + 2 * (0.5 + 1/G) B per element.
+//                     2 + 2 * (0.5 + 1/G) B per element (the other layouts
+//                     and formats).
 //   k_dequant         codes + scales -> float32 / bf16.
-//   k_ue5m3_*         UE5M3 -> shifted E4M3 re-encode for the tensor-core path.
+//   k_ue5m3_*         UE5M3 -> shifted E4M3 re-encode for the tensor-core path,
+//                     the shift from the quantizers' largest scale code, and
+//                     the multi-window split of wide UE5M3 scales.
 //   k_encode_scales, k_philox_bits16   conformance helpers (same device code).
 #include <cstdint>
 #include <cuda_runtime.h>

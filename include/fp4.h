@@ -341,9 +341,12 @@ fp4_status fp4_gemm_quantize_dual(const uint8_t* Aq, const uint8_t* As, const ui
  * x bf16 [batch, K] (row stride K), float32 accumulation, y [batch, N] float32
  * or bf16 (row stride N).  Requirements: 1 <= batch <= 64, N > 0, K % 32 == 0,
  * pointers 16-byte aligned.  K % 256 == 0 streams W through shared memory
- * with TMA (any batch up to 64); its waits are bounded and a wait that expires
- * records FP4_ERR_TIMEOUT in *dev_status (optional int32 device word, first
- * error wins). */
+ * with TMA: batches up to 8 on mma.sync, 9..64 on tcgen05 with the expanded
+ * weights in tensor memory, a long K split over a thread-block cluster whose
+ * CTAs add their partial sums in a fixed order (the result does not depend on
+ * timing).  Its waits are bounded and a wait that expires records
+ * FP4_ERR_TIMEOUT in *dev_status (optional int32 device word, first error
+ * wins). */
 fp4_status fp4_gemv_w4a16(const uint8_t* Wq, const uint8_t* Ws, const float* gw,
                           const void* x_bf16, int64_t batch, int64_t N, int64_t K,
                           fp4_out_dtype od, void* y, int32_t* dev_status, fp4_stream_t stream);
