@@ -1178,8 +1178,11 @@ def tensor_ceiling_study():
     K 64) and MXFP4 (scale_vec::2X, M 128).  Runs as its own process, outside
     the timed step."""
     from fp4_block_scaled_amax_gb300 import build as b
-    exe = b.build_ceiling()
-    r = subprocess.run([exe], capture_output=True, text=True, timeout=120)
+    try:
+        exe = b.build_ceiling()
+        r = subprocess.run([exe], capture_output=True, text=True, timeout=120)
+    except (OSError, RuntimeError, subprocess.SubprocessError) as e:
+        return {"error": str(e)[-300:]}
     if r.returncode != 0:
         return {"error": (r.stdout + r.stderr).strip()[-300:]}
     d = json.loads(r.stdout.strip().splitlines()[-1])
