@@ -326,6 +326,13 @@ __device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity) {
   }
 }
 
+// Prefetch of a tensor-map tile into L2 (no shared memory, no barrier).
+__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* map, int x, int y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y)
+               : "memory");
+}
+
 template <int WPT, int NT>
 __global__ void __launch_bounds__(NT == 1 ? 32 * (1 + 4 * 6) : 32 * (1 + 2 * 8))
     k_gemv_w4a16_tma(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant__ CUtensorMap tm_scales,
@@ -354,6 +361,9 @@ __global__ void __launch_bounds__(NT == 1 ? 32 * (1 + 4 * 6) : 32 * (1 + 2 * 8))
   const int it0 = (int)(((int64_t)nk_total * rank) / ksplit);
   const int nk = (int)(((int64_t)nk_total * (rank + 1)) / ksplit) - it0;
 
+  // a GEMV launched after this one may start its CTAs as these exit (they
+  // wait for this grid before they read its activations)
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (threadIdx.x == 0) {
     abort_flag = 0;
     for (int s = 0; s < S; ++s) {
@@ -371,6 +381,19 @@ __global__ void __launch_bounds__(NT == 1 ? 32 * (1 + 4 * 6) : 32 * (1 + 2 * 8))
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_scales)) : "memory");
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_x)) : "memory");
       const uint32_t tx = code_bytes + L::x_bytes() + 16u * L::SB * T;
+      // The weights do not depend on a preceding kernel: those of the first
+      // two stages are prefetched into L2 while it may still be running
+      // (programmatic dependent launch); then every stage loads as usual,
+      // codes, activations and scales, once that kernel has completed.  (A
+      // deeper prefetch queues ahead of the real loads when nothing precedes.)
+      const int pre = nk < 2 ? nk : 2;
+      for (int it = 0; it < pre; ++it) {
+        const int gs = it0 + it;
+#pragma unroll
+        for (int i = 0; i < L::CODE_BOXES; ++i) tma_prefetch_l2_2d(&tm_codes, gs * (L::SC / 2) + 128 * i, n0);
+        tma_prefetch_l2_2d(&tm_scales, gs * L::SB, n0);
+      }
+      asm volatile("griddepcontrol.wait;" ::: "memory");
       int issued = 0;
       for (int it = 0, s = 0, ph = 0; it < nk; ++it) {
         if (it >= S && !wait_bounded(bars + 8 * (S + s), ph ^ 1, &abort_flag, status)) break;
@@ -395,6 +418,8 @@ __global__ void __launch_bounds__(NT == 1 ? 32 * (1 + 4 * 6) : 32 * (1 + 2 * 8))
       for (int it = issued > S ? issued - S : 0; it < issued; ++it) wait_drain(bars + 8 * (it % S), (it / S) & 1);
     }
   } else {
+    // everything these warps read or write follows the preceding kernel
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int cw = warp - 1, t = cw / WPT, qt = cw % WPT;
     const int g = lane >> 2, q = lane & 3;
     const int j = 4 * qt + q;  // the lane's 32-column chunk of the stage
@@ -570,17 +595,21 @@ cudaError_t launch_tma_t(const fp4lib::GemvArgs& a, int T, int ksplit, cudaStrea
   if (e != cudaSuccess) return e;
   if (allowed <= 0 || smem > (size_t)allowed) return cudaErrorNotSupported;
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = (unsigned)ksplit;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
+  // programmatic dependent launch: the kernel may start while the preceding
+  // kernel in the stream finishes (it waits for it before reading x)
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = (unsigned)ksplit;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
   cfg.gridDim = dim3((unsigned)ctas, 1, 1);
   cfg.blockDim = dim3(32 * (1 + WPT * T), 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   cfg.attrs = attr;
-  cfg.numAttrs = ksplit > 1 ? 1 : 0;
+  cfg.numAttrs = ksplit > 1 ? 2 : 1;
   return cudaLaunchKernelEx(&cfg, k_gemv_w4a16_tma<WPT, NT>, mc, ms, mx, a.gw, (int)a.batch, (int)a.N, nk_total, T, S,
                             ksplit, a.bf16_out, a.y, a.status);
 }

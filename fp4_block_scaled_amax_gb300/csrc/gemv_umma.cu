@@ -43,6 +43,13 @@ namespace {
 
 using namespace fp4async;
 
+// Prefetch of a tensor-map tile into L2 (no shared memory, no barrier).
+__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* map, int x, int y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y)
+               : "memory");
+}
+
 constexpr int UM_ROWS = 128;     // weight rows per CTA (the MMA's M)
 constexpr int UM_BATCH = 64;     // batch rows of the MMA (its N); smaller batches read zeros
 constexpr int UM_KSTAGE = 256;   // columns per TMA stage
@@ -165,6 +172,9 @@ struct UmParams {
 __global__ void __launch_bounds__(UM_THREADS, 1)
     k_gemv_w4a16_umma(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant__ CUtensorMap tm_scales,
                       const __grid_constant__ CUtensorMap tm_x, UmParams p) {
+  // a GEMV launched after this one may start its CTAs as these exit (they
+  // wait for this grid before they read its activations)
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
@@ -207,6 +217,9 @@ __global__ void __launch_bounds__(UM_THREADS, 1)
   __syncthreads();
   um_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // everything the warps other than the producer read or write follows the
+  // preceding kernel (the producer waits after prefetching weights)
+  if (warp != 0) asm volatile("griddepcontrol.wait;" ::: "memory");
 
   if (warp == 0) {
     // ------------------------------ TMA producer --------------------------
@@ -214,6 +227,14 @@ __global__ void __launch_bounds__(UM_THREADS, 1)
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_codes)) : "memory");
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_scales)) : "memory");
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_x)) : "memory");
+      // the weights of the first two stages stream into L2 while a preceding
+      // kernel may still run (programmatic dependent launch); every stage then
+      // loads as usual once it has completed
+      for (int it = 0; it < nk && it < 2; ++it) {
+        tma_prefetch_l2_2d(&tm_codes, (it0 + it) * (UM_KSTAGE / 2), n0);
+        tma_prefetch_l2_2d(&tm_scales, (it0 + it) * (UM_KSTAGE / 16), n0);
+      }
+      asm volatile("griddepcontrol.wait;" ::: "memory");
       for (int it = 0; it < nk; ++it) {
         const int s = it % UM_STAGES;
         if (it >= UM_STAGES &&
@@ -431,17 +452,20 @@ cudaError_t launch_gemv_umma(const GemvArgs& a, cudaStream_t st) {
   p.y = a.y;
   p.status = a.status;
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = (unsigned)ksplit;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
+  // programmatic dependent launch, as for the TMA-fed form
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = (unsigned)ksplit;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
   cfg.gridDim = dim3((unsigned)(tiles * ksplit), 1, 1);
   cfg.blockDim = dim3(UM_THREADS, 1, 1);
   cfg.dynamicSmemBytes = UM_SMEM_LAUNCH;
   cfg.stream = st;
   cfg.attrs = attr;
-  cfg.numAttrs = ksplit > 1 ? 1 : 0;
+  cfg.numAttrs = ksplit > 1 ? 2 : 1;
   return cudaLaunchKernelEx(&cfg, k_gemv_w4a16_umma, mc, ms, mx, p);
 }
 

@@ -75,6 +75,30 @@ def test_gemv_ragged_rows_tensor_core_form():
             run(W, synth.normal((b, K), 34, K + b), "f32" if b != 40 else "bf16")
 
 
+@pytest.mark.parametrize("batch", [1, 8, 40])
+def test_gemv_dependent_chain_reads_the_previous_output(batch):
+    # each launch takes the previous launch's output as its activations; the
+    # launches overlap (programmatic dependent launch), so a launch that read
+    # its activations before the previous one finished would fail here
+    fp4 = lib()
+    K = 2048
+    W = synth.normal((K, K), 38, 0, std=0.04)
+    qw = Q.quantize(f32(W), "E4M3")
+    codes, scales = dev(qw["codes"]), dev(qw["scales"])
+    gw = torch.tensor([qw["amax"]], dtype=torch.float32, device="cuda")
+    xs = [synth.normal((batch, K), 38, batch).cuda()]
+    for _ in range(6):
+        y = torch.empty((batch, K), dtype=torch.bfloat16, device="cuda")
+        fp4.fp4_gemv_w4a16(codes, scales, gw, xs[-1], batch, K, K, fp4.FP4_OUT_BF16, y)
+        xs.append(y)
+    torch.cuda.synchronize()
+    for i in range(6):
+        yr, S = Gm.gemv_ref(qw["codes"], qw["scales"], qw["amax"], f32(xs[i].cpu()))
+        yg = host(xs[i + 1].float())
+        bound = Gm.gemm_bound(S) + np.abs(yr) * 2.0 ** -8
+        assert (np.abs(yg - yr) <= bound).all(), f"link {i}"
+
+
 def test_gemv_tensor_core_form_falls_back_for_k_not_multiple_of_256():
     W = synth.normal((384, 1056), 35, 0, std=0.02)
     run(W, synth.normal((33, 1056), 35, 1))
