@@ -62,7 +62,7 @@ NCU_TRAFFIC = {"gemm": {"bytes": 292.47e6, "src": "60119a0c183c0f0c",
                         "files": ["gemm_sm103.cu", "async_sm103.cuh", "fp4_device.cuh", "device_cache.h"]},
                "quant_dual": {"bytes": 803.88e6, "src": "8c40991c55aa01e1",
                               "files": ["quantize.cu", "async_sm103.cuh", "fp4_device.cuh", "device_cache.h"]},
-               "gemv": {"bytes": 25.45e6, "src": "af48789a098843e4",
+               "gemv": {"bytes": 25.45e6, "src": "ae9a6aadbb359671",
                         "files": ["gemv.cu", "async_sm103.cuh", "fp4_device.cuh", "device_cache.h"]},
                "amax": {"bytes": 586.2e6, "src": "8c40991c55aa01e1",
                         "files": ["quantize.cu", "async_sm103.cuh", "fp4_device.cuh", "device_cache.h"]}}
