@@ -287,30 +287,30 @@ __device__ __forceinline__ uint32_t e2m1x2_rne(float lo, float hi) {
 // lo <= |y| < hi the neighbouring grid values, round up iff
 // R < 65536 * (|y| - lo) / (hi - lo); |y| >= 6 gives 6.  Returns the rounded
 // grid value with the sign of x (the caller converts exact grid values to
-// codes).  It is a carry into the grid-step bit:
-//  * for 1 <= |y| < 8 the E2M1 step is 2^(e-1) with e the binary exponent of
-//    |y|, i.e. bit 22 of its float32 pattern, and f = (|y| - lo)/step is the
-//    22-bit field m below it over 2^22; "R < 65536 f" is "m > 64 R" (R is an
-//    integer), i.e. m + (2^22 - 1 - 64 R) carries into bit 22.  So adding
-//    d = 0x3FFFFF - 64 R and clearing the 22 low bits gives lo or hi; a carry
-//    out of the mantissa moves into the exponent by itself (1.5 -> 2,
-//    3 -> 4, 6 -> 8, which the saturating conversion maps to 6);
-//  * below 1 the step is 0.5 at every magnitude: |y| + 1 rounded up to
-//    float32 lies in [1, 2], where the step sits at bit 22 again, and the
-//    rounding up keeps the decision exact (the threshold lo + 64 R * 2^-23
-//    lies on the float32 grid there, so ceil(|y| + 1) exceeds it iff |y| + 1
-//    does); the same carry then gives 1 + {0, 0.5, 1}, and subtracting the 1
-//    is exact;
-//  * |y| = 0 (a zero block) stays 0; +Inf (|y| overflowed) stays +Inf.
-// d is computed by the caller from the draw (sr_d_lo / sr_d_hi).
+// codes).  It is a carry into the grid-step bit of z = |y| * 2^-126:
+//  * for 1 <= |y| < 8, z is normal and exact, and the E2M1 step is 2^(e-1)
+//    with e the binary exponent of |y|, i.e. bit 22 of the float32 pattern
+//    of z; f = (|y| - lo)/step is the 22-bit field m below it over 2^22, and
+//    "R < 65536 f" is "m > 64 R" (R is an integer), i.e. m + (2^22 - 1 - 64 R)
+//    carries into bit 22.  So adding d = 0x3FFFFF - 64 R and clearing the 22
+//    low bits gives lo or hi; a carry out of the mantissa moves into the
+//    exponent by itself (1.5 -> 2, 3 -> 4, 6 -> 8, which the saturating
+//    conversion maps to 6);
+//  * below 1, z is subnormal: its pattern is the integer |y| * 2^23 rounded
+//    up (the product is rounded toward +inf), so bit 22 is again the step
+//    0.5 and the same carry applies; rounding up keeps the decision exact,
+//    as the threshold lo + 64 R * 2^-23 lies on that grid and a value rounded
+//    up exceeds it iff the value itself does; 0.5 + 0.5 carries into the
+//    exponent field and gives 1 * 2^-126, the normal pattern of 1;
+//  * |y| = 0 stays 0; +Inf stays +Inf.
+// Multiplying back by 2^126 is exact on the grid values.  d is computed by
+// the caller from the draw (sr_d_lo / sr_d_hi).
 __device__ __forceinline__ float e2m1_sr_value(float x, float r, uint32_t d) {
   const float ay = __fmul_rn(fabsf(x), r);
-  // 1.0 below 1, else 0.0: saturate(2^24 (1 - ay)) (exact: 1 - ay >= 2^-24 below 1)
-  float off;
-  asm("fma.rn.sat.f32 %0, %1, 0fCB800000, 0f4B800000;" : "=f"(off) : "f"(ay));
-  const float v = __fadd_ru(ay, off);
-  const float q = __uint_as_float((__float_as_uint(v) + d) & 0xFFC00000u);
-  const float m = __fsub_rn(q, off);
+  float z;
+  asm("mul.rp.f32 %0, %1, 0f00800000;" : "=f"(z) : "f"(ay));  // ay * 2^-126, subnormals kept
+  const float q = __uint_as_float((__float_as_uint(z) + d) & 0xFFC00000u);
+  const float m = __fmul_rn(q, 0x1p126f);  // exact: * 2^126
   return __uint_as_float(__float_as_uint(m) | (__float_as_uint(x) & 0x80000000u));
 }
 // The carry constant d = 0x3FFFFF - 64 R of the low and the high 16-bit draw
@@ -404,6 +404,19 @@ __device__ __forceinline__ uint4 sr_draws8(uint64_t seed, uint64_t blk) {
 __device__ __forceinline__ uint4 sr_draws8(const PhiloxKey& key, uint64_t blk) {
   return philox4x32_10((uint32_t)blk, (uint32_t)(blk >> 32), 0u, 0u, key);
 }
+// A block index below 2^32 (a tensor of fewer than 2^35 elements): the
+// counter's second word is a literal zero, which removes a multiply from the
+// second round and an xor from the first.
+__device__ __forceinline__ uint4 sr_draws8(const PhiloxKey& key, uint32_t blk) {
+  return philox4x32_10(blk, 0u, 0u, 0u, key);
+}
+// Where the draws of 16 consecutive elements start: an element index (a
+// multiple of 8), or SrIdx32, the block index itself when it fits 32 bits.
+struct SrIdx32 {
+  uint32_t blk;
+};
+__device__ __forceinline__ uint64_t sr_block(uint64_t idx0, int h) { return (idx0 >> 3) + (uint64_t)h; }
+__device__ __forceinline__ uint32_t sr_block(SrIdx32 i, int h) { return i.blk + (uint32_t)h; }
 __device__ __forceinline__ uint32_t draw16(const uint4& w, int j) {
   const uint32_t v = (j >> 1) == 0 ? w.x : (j >> 1) == 1 ? w.y : (j >> 1) == 2 ? w.z : w.w;
   return (j & 1) ? (v >> 16) : (v & 0xFFFFu);
@@ -429,8 +442,8 @@ __device__ __forceinline__ uint32_t e2m1x8_rne(const float* y) {
   return r;
 }
 
-template <bool SR, bool INT4 = false, class KEY = uint64_t>
-__device__ __forceinline__ uint2 quant16(const uint32_t* w, float r, const KEY& seed, uint64_t idx0) {
+template <bool SR, bool INT4 = false, class KEY = uint64_t, class IDX = uint64_t>
+__device__ __forceinline__ uint2 quant16(const uint32_t* w, float r, const KEY& seed, IDX idx0) {
   if constexpr (INT4) {
     uint32_t nib[16];
     if constexpr (!SR) {
@@ -442,7 +455,7 @@ __device__ __forceinline__ uint2 quant16(const uint32_t* w, float r, const KEY& 
     } else {
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        const uint4 d = sr_draws8(seed, (idx0 >> 3) + h);
+        const uint4 d = sr_draws8(seed, sr_block(idx0, h));
         const uint32_t dw[4] = {d.x, d.y, d.z, d.w};
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -469,7 +482,7 @@ __device__ __forceinline__ uint2 quant16(const uint32_t* w, float r, const KEY& 
   } else {
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
-      const uint4 d = sr_draws8(seed, (idx0 >> 3) + h);
+      const uint4 d = sr_draws8(seed, sr_block(idx0, h));
       const uint32_t dw[4] = {d.x, d.y, d.z, d.w};
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
@@ -484,8 +497,8 @@ __device__ __forceinline__ uint2 quant16(const uint32_t* w, float r, const KEY& 
 
 // quant16 of one column of a 16-row block held as 16 words, each a row's
 // pair of neighbouring columns: HI selects the high (odd) column.
-template <bool SR, bool HI, class KEY = uint64_t>
-__device__ __forceinline__ uint2 quant16_col(const uint32_t (&v)[16], float r, const KEY& seed, uint64_t idx0) {
+template <bool SR, bool HI, class KEY = uint64_t, class IDX = uint64_t>
+__device__ __forceinline__ uint2 quant16_col(const uint32_t (&v)[16], float r, const KEY& seed, IDX idx0) {
   float y[16];
   if constexpr (!SR) {
 #pragma unroll
@@ -493,7 +506,7 @@ __device__ __forceinline__ uint2 quant16_col(const uint32_t (&v)[16], float r, c
   } else {
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
-      const uint4 d = sr_draws8(seed, (idx0 >> 3) + h);
+      const uint4 d = sr_draws8(seed, sr_block(idx0, h));
       const uint32_t dw[4] = {d.x, d.y, d.z, d.w};
 #pragma unroll
       for (int i = 0; i < 4; ++i) {

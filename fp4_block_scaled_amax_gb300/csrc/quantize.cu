@@ -356,7 +356,9 @@ __global__ void __launch_bounds__(256) k_quant_tile(
 // the row scales of rows m0.. and the transposed scales of columns k0.. are
 // each two whole 512-byte atoms of the tiled layout, contiguous in memory)
 // are staged in shared memory and written by one TMA tensor store and two
-// bulk copies.  Staging is double-buffered.  Every wait is bounded.
+// bulk copies.  Staging is double-buffered.  Every wait is bounded.  The
+// Philox block indices (element index / 8) are 32-bit: a tensor of 2^35
+// elements or more takes k_quant_tile instead.
 constexpr int QD_T = 128;                    // tile rows = tile columns
 constexpr int QD_STAGES = 4;
 constexpr int QD_CONSUMERS = 16;             // warps
@@ -489,7 +491,8 @@ __global__ void __launch_bounds__(QD_THREADS, 1)
           const BlockScale bs = block_scale_tab<FMT, true>(a, s_enc, rtab);
           maxc_row = max(maxc_row, bs.code);
           const int64_t grow = m0 + rr, gcol = k0 + 16 * c;
-          const uint2 q = quant16<ROW_SR>(w, bs.r, key_row, (uint64_t)(grow * p.K + gcol));
+          const uint2 q = quant16<ROW_SR>(
+              w, bs.r, key_row, SrIdx32{(uint32_t)grow * (uint32_t)(p.K >> 3) + (uint32_t)(gcol >> 3)});
           *reinterpret_cast<uint2*>(p.codes_row + grow * (p.K / 2) + gcol / 2) = q;
           stg_sfr[qd_sf_off(rr, c)] = (uint8_t)bs.code;
         }
@@ -509,9 +512,10 @@ __global__ void __launch_bounds__(QD_THREADS, 1)
         const BlockScale b1 = block_scale_tab<FMT, true>(a_hi, s_enc, rtab);
         maxc_col = max(maxc_col, max(b0.code, b1.code));
         const int c0 = 64 * cbox + 2 * lane;  // tile column of the low half
-        const uint64_t i0 = (uint64_t)(k0 + c0) * (uint64_t)p.M + (uint64_t)(m0 + 16 * crb);
-        const uint2 q0 = quant16_col<COL_SR, false>(v, b0.r, key_col, i0);
-        const uint2 q1 = quant16_col<COL_SR, true>(v, b1.r, key_col, i0 + (uint64_t)p.M);
+        // Philox blocks of output elements (k0 + c0) M + m0 + 16 crb and the next row of the output
+        const uint32_t blk0 = (uint32_t)(k0 + c0) * (uint32_t)(p.M >> 3) + (uint32_t)((m0 + 16 * crb) >> 3);
+        const uint2 q0 = quant16_col<COL_SR, false>(v, b0.r, key_col, SrIdx32{blk0});
+        const uint2 q1 = quant16_col<COL_SR, true>(v, b1.r, key_col, SrIdx32{blk0 + (uint32_t)(p.M >> 3)});
         // staged transposed codes: output row c, bytes 8 crb .. +7 (64-byte swizzle)
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
@@ -865,6 +869,8 @@ static cudaError_t dispatch_dual_tma(const QuantArgs& a, cudaStream_t st) {
     return cudaErrorNotSupported;
   } else {
     if (!a.mma || a.M % QD_T != 0 || a.K % QD_T != 0 || a.M == 0 || a.K == 0) return cudaErrorNotSupported;
+    // the kernel's Philox block indices (element index / 8) are 32-bit
+    if ((a.M >> 3) * a.K > (int64_t)0xFFFFFFFF) return cudaErrorNotSupported;
     const bool amax = a.amax_by_product;
     if (a.mode == QuantArgs::DUAL) {
 #define DT_CASE(RS, CS, AM) \
