@@ -398,6 +398,22 @@ __device__ __forceinline__ void qd_bulk_store(void* dst, uint32_t src, uint32_t 
   asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src), "r"(bytes)
                : "memory");
 }
+// The tiles t = t0, t0 + stride, ... of a grid with m_tiles tiles per column
+// (M fastest), walked without a division per tile.
+struct TileWalk {
+  int mt, kt, dm, dk, m_tiles;
+  __device__ __forceinline__ TileWalk(int t0, int stride, int m_tiles_)
+      : mt(t0 % m_tiles_), kt(t0 / m_tiles_), dm(stride % m_tiles_), dk(stride / m_tiles_), m_tiles(m_tiles_) {}
+  __device__ __forceinline__ void next() {
+    mt += dm;
+    kt += dk;
+    if (mt >= m_tiles) {
+      mt -= m_tiles;
+      ++kt;
+    }
+  }
+};
+
 // scale (row r, block b) of a 128-row x 8-block tile inside its two atoms
 __device__ __forceinline__ int qd_sf_off(int r, int b) { return (b >> 2) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4 + (b & 3); }
 
@@ -443,13 +459,14 @@ __global__ void __launch_bounds__(QD_THREADS, 1)
     if (lane == 0) {
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_x)) : "memory");
       int it = 0;
-      for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++it) {
+      TileWalk tw(blockIdx.x, gridDim.x, m_tiles);
+      for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++it, tw.next()) {
         const int s = it % QD_STAGES;
         if (it >= QD_STAGES &&
             !wait_bounded(bar_empty + 8 * s, ((it / QD_STAGES) - 1) & 1, abort_flag, p.status))
           break;
         if (*abort_flag) break;
-        const int m0 = (t % m_tiles) * QD_T, k0 = (t / m_tiles) * QD_T;
+        const int m0 = tw.mt * QD_T, k0 = tw.kt * QD_T;
         const uint32_t fb = bar_full + 8 * s, dst = sbase + QD_SMEM_STAGES + s * QD_STAGE_BYTES;
         mbar_expect_tx(fb, QD_STAGE_BYTES);
         tma_load_2d(dst, &tm_x, fb, k0, m0);
@@ -467,9 +484,10 @@ __global__ void __launch_bounds__(QD_THREADS, 1)
     const int cbox = cw >> 3, crb = cw & 7;
     const PhiloxKey key_row(p.seed_row), key_col(p.seed_col);
     int it = 0;
-    for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++it) {
+    TileWalk tw(blockIdx.x, gridDim.x, m_tiles);
+    for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++it, tw.next()) {
       const int s = it % QD_STAGES, b = it & 1;
-      const int m0 = (t % m_tiles) * QD_T, k0 = (t / m_tiles) * QD_T;
+      const int m0 = tw.mt * QD_T, k0 = tw.kt * QD_T;
       if (!wait_lane0(bar_full + 8 * s, (it / QD_STAGES) & 1, abort_flag, p.status, lane)) break;
       if ((it >> 1) > 0 && !wait_lane0(bar_stg_free + 8 * b, ((it >> 1) - 1) & 1, abort_flag, p.status, lane))
         break;
@@ -553,10 +571,11 @@ __global__ void __launch_bounds__(QD_THREADS, 1)
     if (lane == 0) {
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_ccol)) : "memory");
       int it = 0;
-      for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++it) {
+      TileWalk tw(blockIdx.x, gridDim.x, m_tiles);
+      for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++it, tw.next()) {
         const int b = it & 1;
         if (!wait_bounded(bar_stg_full + 8 * b, (it >> 1) & 1, abort_flag, p.status)) break;
-        const int m0 = (t % m_tiles) * QD_T, k0 = (t / m_tiles) * QD_T;
+        const int m0 = tw.mt * QD_T, k0 = tw.kt * QD_T;
         const uint32_t stg = sbase + QD_SMEM_STG + b * QD_STG_BYTES;
         qd_tma_store_2d(&tm_ccol, stg, m0 / 2, k0);
         if (DO_ROW)
