@@ -15,6 +15,7 @@ N = 11008; X N(0,1) with 0.5 % outliers x100, W N(0,0.02), dY Laplace(0,1e-4)):
   wgrad    dW = dY^T X   11008 x  4096 x 16384 bf16 out
   weight-only decode GEMV with the same layer's weight (quantized once,
       batch 8): y = x W^T                                (GEMV kernel)
+      on a second stream after dgrad, beside wgrad's last round of tiles
 
 metric: FP4 GEMM TFLOP/s of the whole step (3 * 2*M*N*K / step time);
 per-kernel rooflines from CUDA events on the launching stream.
@@ -217,7 +218,7 @@ def cores():
 # the GPU step
 # ---------------------------------------------------------------------------
 
-STEP_EVENTS = 9  # start, after the amax launch, after each dual quantizer, after each GEMM, after the GEMV
+STEP_EVENTS = 9  # start, after the amax launch, after each dual quantizer, after each GEMM, after the GEMV joined
 
 
 class LinearStep:
@@ -250,6 +251,12 @@ class LinearStep:
         self.yg = torch.empty((GEMV_BATCH, N), dtype=torch.bfloat16, device=device)
         self.status = torch.zeros(1, dtype=torch.int32, device=device)
         self.launches_per_step = 8  # amax of all three, 3 dual quantizers, 3 GEMMs, 1 GEMV
+        # the decode GEMV depends on none of the GEMMs: it runs on its own
+        # stream once dgrad is done, in the SMs that the weight-gradient GEMM's
+        # last, partial round of tiles leaves idle
+        self.side = torch.cuda.Stream(device=device)
+        self.ev_dgrad = torch.cuda.Event()
+        self.ev_gemv = torch.cuda.Event()
 
     def run(self, ev=None):
         """One step; ev: optional list of STEP_EVENTS CUDA events recorded between kernels."""
@@ -282,10 +289,15 @@ class LinearStep:
         fp4.fp4_gemm(qd[0], qd[1], qW[2], qW[3], ad, aW, None, None, M, K, N, "E4M3", BF, self.dX,
                      dev_status=self.status)
         mark(6)
+        self.ev_dgrad.record(st)
         fp4.fp4_gemm(qd[2], qd[3], qX[2], qX[3], ad, aX, None, None, N, K, M, "E4M3", BF, self.dW,
                      dev_status=self.status)
         mark(7)
-        fp4.fp4_gemv_w4a16(self.Wg_codes, self.Wg_scales, self.Wg_amax, self.xg, GEMV_BATCH, N, K, BF, self.yg)
+        self.side.wait_event(self.ev_dgrad)  # launched after wgrad, so wgrad's tiles take the SMs first
+        with torch.cuda.stream(self.side):
+            fp4.fp4_gemv_w4a16(self.Wg_codes, self.Wg_scales, self.Wg_amax, self.xg, GEMV_BATCH, N, K, BF, self.yg)
+        self.ev_gemv.record(self.side)
+        st.wait_event(self.ev_gemv)
         mark(8)
 
 
@@ -991,6 +1003,24 @@ def gemv_graph_study(step, reps=5, launches=64, copies=8):
     return res
 
 
+def gemv_single_launch(step, flush, reps):
+    """The step's GEMV alone: one launch after an L2 flush, timed with CUDA
+    events on its stream (inside the step it runs beside wgrad's last round).
+    Returns the per-launch times in ms."""
+    N, K, BF = N_FFN, K_HID, step.fp4.FP4_OUT_BF16
+    st = torch.cuda.current_stream()
+    ts = []
+    for _ in range(max(reps, 3)):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(st)
+        step.fp4.fp4_gemv_w4a16(step.Wg_codes, step.Wg_scales, step.Wg_amax, step.xg, GEMV_BATCH, N, K, BF, step.yg)
+        e1.record(st)
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1))
+    return ts
+
+
 def step_graph_study(step, flush, reps=5):
     """The timed step (10 launches) replayed from one captured CUDA graph
     against the same step launched one kernel at a time, each timed with
@@ -1229,7 +1259,7 @@ def run_ours(args, rank, world, local):
     fwd_ms = [span(e, 4, 5) for e in evs]
     quant_ms = [span(e, 1 + j, 2 + j) for e in evs for j in range(3)]
     amax_ms = [span(e, 0, 1) for e in evs]
-    gemv_ms = [span(e, 7, 8) for e in evs]
+    gemv_ms = gemv_single_launch(step, flush, args.steps)
 
     hbm, bf16, src = peaks()
     fp4_peak = bf16 * FP4_PER_BF16
