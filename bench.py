@@ -13,12 +13,14 @@ N = 11008; X N(0,1) with 0.5 % outliers x100, W N(0,0.02), dY Laplace(0,1e-4)):
   forward  Y  = X W^T    16384 x 11008 x 4096  bf16 out (tcgen05 FP4 GEMM)
   dgrad    dX = dY W     16384 x  4096 x 11008 bf16 out
   wgrad    dW = dY^T X   11008 x  4096 x 16384 bf16 out
+      on a second stream after fwd, beside dgrad's last round of tiles
   weight-only decode GEMV with the same layer's weight (quantized once,
       batch 8): y = x W^T                                (GEMV kernel)
-      on a second stream after dgrad, beside wgrad's last round of tiles
+      on a third stream after dgrad, beside wgrad's last round of tiles
 
 metric: FP4 GEMM TFLOP/s of the whole step (3 * 2*M*N*K / step time);
-per-kernel rooflines from CUDA events on the launching stream.
+per-kernel rooflines from CUDA events on the launching stream (the GEMMs'
+and the GEMV's from the same step with every kernel on one stream).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 
@@ -251,15 +253,22 @@ class LinearStep:
         self.yg = torch.empty((GEMV_BATCH, N), dtype=torch.bfloat16, device=device)
         self.status = torch.zeros(1, dtype=torch.int32, device=device)
         self.launches_per_step = 8  # amax of all three, 3 dual quantizers, 3 GEMMs, 1 GEMV
-        # the decode GEMV depends on none of the GEMMs: it runs on its own
-        # stream once dgrad is done, in the SMs that the weight-gradient GEMM's
-        # last, partial round of tiles leaves idle
-        self.side = torch.cuda.Stream(device=device)
+        # wgrad depends on neither fwd nor dgrad: it runs on its own stream once
+        # fwd is done and takes the SMs that dgrad's last, partial round of
+        # tiles leaves idle; the decode GEMV depends on none of the GEMMs and
+        # fills, on a third stream, those that wgrad's last round leaves idle
+        self.s_wgrad = torch.cuda.Stream(device=device)
+        self.s_gemv = torch.cuda.Stream(device=device)
+        self.ev_fwd = torch.cuda.Event()
         self.ev_dgrad = torch.cuda.Event()
+        self.ev_wgrad = torch.cuda.Event()
         self.ev_gemv = torch.cuda.Event()
 
-    def run(self, ev=None):
-        """One step; ev: optional list of STEP_EVENTS CUDA events recorded between kernels."""
+    def run(self, ev=None, serial=False):
+        """One step; ev: optional list of STEP_EVENTS CUDA events recorded
+        between kernels.  serial: every kernel on the current stream, one after
+        another (the form in which each kernel's own time is measured);
+        otherwise wgrad and the GEMV overlap as described above."""
         fp4 = self.fp4
         RNE, SR, MMA = fp4.FP4_ROUND_RNE, fp4.FP4_ROUND_STOCHASTIC, fp4.FP4_SFLAYOUT_MMA
         M, K, N = M_TOK, K_HID, N_FFN
@@ -286,17 +295,25 @@ class LinearStep:
         fp4.fp4_gemm(qX[0], qX[1], qW[0], qW[1], aX, aW, None, None, M, N, K, "E4M3", BF, self.Y,
                      dev_status=self.status)
         mark(5)
+        s_wgrad, s_gemv = (st, st) if serial else (self.s_wgrad, self.s_gemv)
+        self.ev_fwd.record(st)
         fp4.fp4_gemm(qd[0], qd[1], qW[2], qW[3], ad, aW, None, None, M, K, N, "E4M3", BF, self.dX,
                      dev_status=self.status)
         mark(6)
         self.ev_dgrad.record(st)
-        fp4.fp4_gemm(qd[2], qd[3], qX[2], qX[3], ad, aX, None, None, N, K, M, "E4M3", BF, self.dW,
-                     dev_status=self.status)
+        # launched after dgrad, so dgrad's tiles take the SMs first
+        s_wgrad.wait_event(self.ev_fwd)
+        with torch.cuda.stream(s_wgrad):
+            fp4.fp4_gemm(qd[2], qd[3], qX[2], qX[3], ad, aX, None, None, N, K, M, "E4M3", BF, self.dW,
+                         dev_status=self.status)
+        self.ev_wgrad.record(s_wgrad)
+        st.wait_event(self.ev_wgrad)
         mark(7)
-        self.side.wait_event(self.ev_dgrad)  # launched after wgrad, so wgrad's tiles take the SMs first
-        with torch.cuda.stream(self.side):
+        # launched after wgrad, so wgrad's tiles take the SMs first
+        s_gemv.wait_event(self.ev_dgrad)
+        with torch.cuda.stream(s_gemv):
             fp4.fp4_gemv_w4a16(self.Wg_codes, self.Wg_scales, self.Wg_amax, self.xg, GEMV_BATCH, N, K, BF, self.yg)
-        self.ev_gemv.record(self.side)
+        self.ev_gemv.record(s_gemv)
         st.wait_event(self.ev_gemv)
         mark(8)
 
@@ -1003,24 +1020,6 @@ def gemv_graph_study(step, reps=5, launches=64, copies=8):
     return res
 
 
-def gemv_single_launch(step, flush, reps):
-    """The step's GEMV alone: one launch after an L2 flush, timed with CUDA
-    events on its stream (inside the step it runs beside wgrad's last round).
-    Returns the per-launch times in ms."""
-    N, K, BF = N_FFN, K_HID, step.fp4.FP4_OUT_BF16
-    st = torch.cuda.current_stream()
-    ts = []
-    for _ in range(max(reps, 3)):
-        flush.zero_()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(st)
-        step.fp4.fp4_gemv_w4a16(step.Wg_codes, step.Wg_scales, step.Wg_amax, step.xg, GEMV_BATCH, N, K, BF, step.yg)
-        e1.record(st)
-        torch.cuda.synchronize()
-        ts.append(e0.elapsed_time(e1))
-    return ts
-
-
 def step_graph_study(step, flush, reps=5):
     """The timed step (10 launches) replayed from one captured CUDA graph
     against the same step launched one kernel at a time, each timed with
@@ -1255,11 +1254,21 @@ def run_ours(args, rank, world, local):
     step_ms = [span(e, 0, 8) for e in evs]
     ms = statistics.mean(step_ms)
     ms_max = max_over_ranks(ms, world, device)
-    gemm_ms = [span(e, i, i + 1) for e in evs for i in (4, 5, 6)]
-    fwd_ms = [span(e, 4, 5) for e in evs]
     quant_ms = [span(e, 1 + j, 2 + j) for e in evs for j in range(3)]
     amax_ms = [span(e, 0, 1) for e in evs]
-    gemv_ms = gemv_single_launch(step, flush, args.steps)
+    # In the timed steps wgrad and the GEMV overlap other kernels, so each
+    # GEMM's and the GEMV's own time comes from as many more steps with every
+    # kernel launched one after another on one stream (same launches, same
+    # inputs, the same L2 flush before each step).
+    sevs = [[torch.cuda.Event(enable_timing=True) for _ in range(STEP_EVENTS)] for _ in range(args.steps)]
+    for i in range(args.steps):
+        flush.zero_()
+        step.run(sevs[i], serial=True)
+    torch.cuda.synchronize()
+    gemm_ms = [span(e, i, i + 1) for e in sevs for i in (4, 5, 6)]
+    fwd_ms = [span(e, 4, 5) for e in sevs]
+    gemv_ms = [span(e, 7, 8) for e in sevs]
+    serial_ms = statistics.mean(span(e, 0, 8) for e in sevs)
 
     hbm, bf16, src = peaks()
     fp4_peak = bf16 * FP4_PER_BF16
@@ -1337,7 +1346,9 @@ def run_ours(args, rank, world, local):
         "roofline": {"kernel": "k_gemm_fp4 (mean of fwd, dgrad, wgrad)", "bound": "tensor",
                      "achieved": round(gemm_tflops, 1), "peak": round(fp4_peak, 1), "unit": "TFLOP/s",
                      "frac": round(gemm_tflops / fp4_peak, 4), "traffic": traffic_v,
-                     "peak_source": f"{src}: bf16 burst {bf16} x {FP4_PER_BF16} (nominal FP4/bf16)"},
+                     "peak_source": f"{src}: bf16 burst {bf16} x {FP4_PER_BF16} (nominal FP4/bf16)",
+                     "measured": f"each GEMM with CUDA events in {args.steps} steps of the serial form (every kernel "
+                                 "on one stream) after the timed ones; in the timed steps wgrad runs beside dgrad"},
         "roofline_quantize": {"kernel": "k_quant_dual_tma (dual, 3.125 B/elem; X, W, dY per step)", "bound": "hbm",
                               "achieved": round(q_gbs, 1), "peak": hbm, "unit": "GB/s",
                               "frac": round(q_gbs / hbm, 4), "traffic": qtraffic_v, "peak_source": src},
@@ -1360,11 +1371,13 @@ def run_ours(args, rank, world, local):
                           "traffic": traffic_of("amax"), "peak_source": src,
                           "note": "the first launch after the L2 flush also writes back the flush's dirty lines"},
         "gemv_w4a16": {"batch": GEMV_BATCH, "N": N_FFN, "K": K_HID, "us": round(statistics.mean(gemv_ms) * 1e3, 2),
-                       "GB/s": round(gv_gbs, 1), "frac": round(gv_gbs / hbm, 4), "traffic": gvtraffic_v},
+                       "GB/s": round(gv_gbs, 1), "frac": round(gv_gbs / hbm, 4), "traffic": gvtraffic_v,
+                       "measured": "after wgrad in the serial form of the step"},
         "kernel_ms": {"fwd_gemm": round(statistics.mean(fwd_ms), 4),
                       "gemm_mean": round(statistics.mean(gemm_ms), 4),
                       "quant_dual_total": round(sum(quant_ms) / args.steps, 4),
-                      "amax_total": round(sum(amax_ms) / args.steps, 4)},
+                      "amax_total": round(sum(amax_ms) / args.steps, 4),
+                      "serial_step": round(serial_ms, 4)},
         "gpu_launches": step.launches_per_step * args.steps,
         "clocks": clk.summary(),
     }
