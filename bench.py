@@ -18,9 +18,10 @@ N = 11008; X N(0,1) with 0.5 % outliers x100, W N(0,0.02), dY Laplace(0,1e-4)):
       batch 8): y = x W^T                                (GEMV kernel)
       on a third stream after dgrad, beside wgrad's last round of tiles
 
-metric: FP4 GEMM TFLOP/s of the whole step (3 * 2*M*N*K / step time);
-per-kernel rooflines from CUDA events on the launching stream (the GEMMs'
-and the GEMV's from the same step with every kernel on one stream).
+metric: FP4 GEMM TFLOP/s of the whole step (3 * 2*M*N*K / step time), the
+step captured once as a CUDA graph and replayed once per timed step;
+per-kernel rooflines from CUDA events between the kernels of as many more
+steps launched kernel by kernel on one stream.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 
@@ -1020,13 +1021,10 @@ def gemv_graph_study(step, reps=5, launches=64, copies=8):
     return res
 
 
-def step_graph_study(step, flush, reps=5):
-    """The timed step (10 launches) replayed from one captured CUDA graph
-    against the same step launched one kernel at a time, each timed with
-    CUDA events after an L2 flush.  Outside the timed step."""
+def capture_step(step):
+    """step.run() captured as one CUDA graph (on a side stream, as capture
+    requires; its fork to the wgrad and GEMV streams joins back inside)."""
     st = torch.cuda.current_stream()
-    step.run()
-    torch.cuda.synchronize()
     side = torch.cuda.Stream()
     side.wait_stream(st)
     graph = torch.cuda.CUDAGraph()
@@ -1034,6 +1032,17 @@ def step_graph_study(step, flush, reps=5):
         with torch.cuda.graph(graph, stream=side):
             step.run()
     st.wait_stream(side)
+    return graph
+
+
+def step_graph_study(step, flush, reps=5):
+    """The timed step (10 launches) replayed from one captured CUDA graph
+    against the same step launched one kernel at a time, each timed with
+    CUDA events after an L2 flush.  Outside the timed step."""
+    st = torch.cuda.current_stream()
+    step.run()
+    torch.cuda.synchronize()
+    graph = capture_step(step)
     res = {"step": "the timed step: 3 amax, 3 dual quantizations, 3 GEMMs, GEMV", "unit": "ms"}
     for name, fn in (("eager", step.run), ("cuda_graph", graph.replay)):
         fn()
@@ -1236,35 +1245,47 @@ def run_ours(args, rank, world, local):
     if int(step.status.item()) != 0:
         raise RuntimeError(f"device status {int(step.status.item())} during warm-up")
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(STEP_EVENTS)] for _ in range(args.steps)]
+    # The timed step runs as production would run it: step.run() (its eight
+    # launches on three streams) captured once as a CUDA graph and replayed
+    # once per step, with an L2 flush between steps outside the events.
+    graph = capture_step(step)
+    graph.replay()
+    torch.cuda.synchronize()
+    st = torch.cuda.current_stream()
+    t0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    t1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     barrier(world)
     torch.cuda.synchronize()
     with ClockSampler(device) as clk:
         for i in range(args.steps):
             flush.zero_()  # L2 flush between timed steps, outside the events
-            step.run(evs[i])
+            t0[i].record(st)
+            graph.replay()
+            t1[i].record(st)
         torch.cuda.synchronize()
     barrier(world)
     if int(step.status.item()) != 0:
         raise RuntimeError(f"device status {int(step.status.item())}")
+    del graph
 
     def span(e, a, z):
         return e[a].elapsed_time(e[z])
 
-    step_ms = [span(e, 0, 8) for e in evs]
+    step_ms = [t0[i].elapsed_time(t1[i]) for i in range(args.steps)]
     ms = statistics.mean(step_ms)
     ms_max = max_over_ranks(ms, world, device)
-    quant_ms = [span(e, 1 + j, 2 + j) for e in evs for j in range(3)]
-    amax_ms = [span(e, 0, 1) for e in evs]
-    # In the timed steps wgrad and the GEMV overlap other kernels, so each
-    # GEMM's and the GEMV's own time comes from as many more steps with every
-    # kernel launched one after another on one stream (same launches, same
-    # inputs, the same L2 flush before each step).
+    # Each kernel's own time comes from as many more steps launched one kernel
+    # at a time, every kernel on one stream (the same launches and inputs, the
+    # same L2 flush before each step), with CUDA events between the kernels.
     sevs = [[torch.cuda.Event(enable_timing=True) for _ in range(STEP_EVENTS)] for _ in range(args.steps)]
     for i in range(args.steps):
         flush.zero_()
         step.run(sevs[i], serial=True)
     torch.cuda.synchronize()
+    if int(step.status.item()) != 0:
+        raise RuntimeError(f"device status {int(step.status.item())}")
+    quant_ms = [span(e, 1 + j, 2 + j) for e in sevs for j in range(3)]
+    amax_ms = [span(e, 0, 1) for e in sevs]
     gemm_ms = [span(e, i, i + 1) for e in sevs for i in (4, 5, 6)]
     fwd_ms = [span(e, 4, 5) for e in sevs]
     gemv_ms = [span(e, 7, 8) for e in sevs]
@@ -1342,16 +1363,18 @@ def run_ours(args, rank, world, local):
                    "tokens": M_TOK, "hidden": K_HID, "ffn": N_FFN, "scale_fmt": "E4M3",
                    "group": 16, "amax": "fresh per step", "gemm_out": "bf16", "gemv_batch": GEMV_BATCH,
                    "l2": "512 MB buffer written between timed steps (outside the events); X and dY also exceed L2",
+                   "launch": "step captured as one CUDA graph (8 kernels on 3 streams), replayed per step",
                    "parallelism": f"dp{world} (independent batches)"},
         "roofline": {"kernel": "k_gemm_fp4 (mean of fwd, dgrad, wgrad)", "bound": "tensor",
                      "achieved": round(gemm_tflops, 1), "peak": round(fp4_peak, 1), "unit": "TFLOP/s",
                      "frac": round(gemm_tflops / fp4_peak, 4), "traffic": traffic_v,
                      "peak_source": f"{src}: bf16 burst {bf16} x {FP4_PER_BF16} (nominal FP4/bf16)",
-                     "measured": f"each GEMM with CUDA events in {args.steps} steps of the serial form (every kernel "
-                                 "on one stream) after the timed ones; in the timed steps wgrad runs beside dgrad"},
+                     "measured": f"each GEMM with CUDA events in {args.steps} steps launched kernel by kernel on one "
+                                 "stream after the timed steps (graph replays, wgrad beside dgrad)"},
         "roofline_quantize": {"kernel": "k_quant_dual_tma (dual, 3.125 B/elem; X, W, dY per step)", "bound": "hbm",
                               "achieved": round(q_gbs, 1), "peak": hbm, "unit": "GB/s",
-                              "frac": round(q_gbs / hbm, 4), "traffic": qtraffic_v, "peak_source": src},
+                              "frac": round(q_gbs / hbm, 4), "traffic": qtraffic_v, "peak_source": src,
+                              "measured": "as the GEMMs'"},
         "quantize_modes": qmodes,
         "formats_7b_gemm": formats,
         "cublaslt_nvfp4": cublas,
@@ -1369,7 +1392,8 @@ def run_ours(args, rank, world, local):
         "roofline_amax": {"kernel": "k_amax_n (X, W, dY in one launch, 2 B/elem read)", "bound": "hbm",
                           "achieved": round(a_gbs, 1), "peak": hbm, "unit": "GB/s", "frac": round(a_gbs / hbm, 4),
                           "traffic": traffic_of("amax"), "peak_source": src,
-                          "note": "the first launch after the L2 flush also writes back the flush's dirty lines"},
+                          "note": "the first launch after the L2 flush also writes back the flush's dirty lines",
+                          "measured": "as the GEMMs'"},
         "gemv_w4a16": {"batch": GEMV_BATCH, "N": N_FFN, "K": K_HID, "us": round(statistics.mean(gemv_ms) * 1e3, 2),
                        "GB/s": round(gv_gbs, 1), "frac": round(gv_gbs / hbm, 4), "traffic": gvtraffic_v,
                        "measured": "after wgrad in the serial form of the step"},
