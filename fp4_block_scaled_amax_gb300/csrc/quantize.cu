@@ -107,7 +107,12 @@ struct AmaxN {
   int n;
 };
 
-__global__ void __launch_bounds__(256) k_amax_n(const __grid_constant__ AmaxN a, float* __restrict__ out) {
+// 128-thread CTAs (at most 64 registers a thread, 8 K a CTA): one fits on an
+// SM beside a persistent dual quantizer, whose 576 threads of 96 registers
+// leave 10 K, so that an amax pass launched on another stream runs in the
+// quantizer's spare resources.
+constexpr int AMAXN_THREADS = 128;
+__global__ void __launch_bounds__(AMAXN_THREADS, 8) k_amax_n(const __grid_constant__ AmaxN a, float* __restrict__ out) {
   int i = 0;
   while (i + 1 < a.n && (int)blockIdx.x >= a.cta_begin[i + 1]) ++i;
   const int b = (int)blockIdx.x - a.cta_begin[i], nb = a.cta_begin[i + 1] - a.cta_begin[i];
@@ -787,9 +792,9 @@ cudaError_t launch_amax_n(int n, const void* const* x, const int64_t* M, const i
   int64_t total = 0;
   for (int i = 0; i < n; ++i) total += M[i] * (K[i] / 8);
   if (total == 0) return cudaSuccess;
-  // the same cap as one fp4_amax launch, shared out by size (at least one CTA each)
-  const int64_t cap = 152 * 8;
-  int64_t blocks_total = (total + 255) / 256;
+  // as many threads as one fp4_amax launch, shared out by size (at least one CTA each)
+  const int64_t cap = 152 * 8 * (256 / AMAXN_THREADS);
+  int64_t blocks_total = (total + AMAXN_THREADS - 1) / AMAXN_THREADS;
   if (blocks_total > cap) blocks_total = cap;
   int begin = 0;
   for (int i = 0; i < n; ++i) {
@@ -804,7 +809,7 @@ cudaError_t launch_amax_n(int n, const void* const* x, const int64_t* M, const i
     begin += (int)nb;
   }
   a.cta_begin[n] = begin;
-  k_amax_n<<<(unsigned)begin, 256, 0, st>>>(a, out);
+  k_amax_n<<<(unsigned)begin, AMAXN_THREADS, 0, st>>>(a, out);
   return cudaGetLastError();
 }
 
