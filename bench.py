@@ -16,10 +16,11 @@ N = 11008; X N(0,1) with 0.5 % outliers x100, W N(0,0.02), dY Laplace(0,1e-4)):
   forward  Y  = X W^T    16384 x 11008 x 4096  bf16 out (tcgen05 FP4 GEMM)
   dgrad    dX = dY W     16384 x  4096 x 11008 bf16 out
   wgrad    dW = dY^T X   11008 x  4096 x 16384 bf16 out
-      on a second stream after fwd, beside dgrad's last round of tiles
+      dgrad and wgrad on their own streams, each launched after the previous
+      GEMM and taking the SMs that its last, partial round of tiles leaves idle
   weight-only decode GEMV with the same layer's weight (quantized once,
       batch 8): y = x W^T                                (GEMV kernel)
-      on a third stream after dgrad, beside wgrad's last round of tiles
+      on another stream after dgrad, beside wgrad's last round of tiles
 
 metric: FP4 GEMM TFLOP/s of the whole step (3 * 2*M*N*K / step time), the
 step captured once as a CUDA graph and replayed once per timed step;
@@ -259,16 +260,15 @@ class LinearStep:
         self.yg = torch.empty((GEMV_BATCH, N), dtype=torch.bfloat16, device=device)
         self.status = torch.zeros(1, dtype=torch.int32, device=device)
         self.launches_per_step = 9  # 2 amax launches (dY; X and W), 3 dual quantizers, 3 GEMMs, 1 GEMV
-        # wgrad depends on neither fwd nor dgrad: it runs on its own stream once
-        # fwd is done and takes the SMs that dgrad's last, partial round of
-        # tiles leaves idle; the decode GEMV depends on none of the GEMMs and
-        # fills, on a third stream, those that wgrad's last round leaves idle
+        # streams of the overlapped step (see run); the decode GEMV depends on
+        # none of the GEMMs and fills the SMs that wgrad's last round leaves idle
         self.s_amax = torch.cuda.Stream(device=device)
+        self.s_dgrad = torch.cuda.Stream(device=device)
         self.s_wgrad = torch.cuda.Stream(device=device)
         self.s_gemv = torch.cuda.Stream(device=device)
         self.ev_amax_dy = torch.cuda.Event()
         self.ev_amax_xw = torch.cuda.Event()
-        self.ev_fwd = torch.cuda.Event()
+        self.ev_quant = torch.cuda.Event()
         self.ev_dgrad = torch.cuda.Event()
         self.ev_wgrad = torch.cuda.Event()
         self.ev_gemv = torch.cuda.Event()
@@ -316,21 +316,27 @@ class LinearStep:
         qX, qW, qd = self.q["X"], self.q["W"], self.q["dY"]
         aX, aW, ad = self.amax[0:1], self.amax[1:2], self.amax[2:3]
         BF = fp4.FP4_OUT_BF16
+        # The three GEMMs read only the quantized operands: dgrad and wgrad wait
+        # for nothing else, each on its own stream. Launched in the order fwd,
+        # dgrad, wgrad, each takes the SMs that the previous one's last, partial
+        # round of tiles leaves idle.
+        s_dgrad, s_wgrad, s_gemv = (st, st, st) if serial else (self.s_dgrad, self.s_wgrad, self.s_gemv)
+        self.ev_quant.record(st)
         fp4.fp4_gemm(qX[0], qX[1], qW[0], qW[1], aX, aW, None, None, M, N, K, "E4M3", BF, self.Y,
                      dev_status=self.status)
         mark(6)
-        s_wgrad, s_gemv = (st, st) if serial else (self.s_wgrad, self.s_gemv)
-        self.ev_fwd.record(st)
-        fp4.fp4_gemm(qd[0], qd[1], qW[2], qW[3], ad, aW, None, None, M, K, N, "E4M3", BF, self.dX,
-                     dev_status=self.status)
+        s_dgrad.wait_event(self.ev_quant)
+        with torch.cuda.stream(s_dgrad):
+            fp4.fp4_gemm(qd[0], qd[1], qW[2], qW[3], ad, aW, None, None, M, K, N, "E4M3", BF, self.dX,
+                         dev_status=self.status)
+        self.ev_dgrad.record(s_dgrad)
         mark(7)
-        self.ev_dgrad.record(st)
-        # launched after dgrad, so dgrad's tiles take the SMs first
-        s_wgrad.wait_event(self.ev_fwd)
+        s_wgrad.wait_event(self.ev_quant)
         with torch.cuda.stream(s_wgrad):
             fp4.fp4_gemm(qd[2], qd[3], qX[2], qX[3], ad, aX, None, None, N, K, M, "E4M3", BF, self.dW,
                          dev_status=self.status)
         self.ev_wgrad.record(s_wgrad)
+        st.wait_event(self.ev_dgrad)
         st.wait_event(self.ev_wgrad)
         mark(8)
         # launched after wgrad, so wgrad's tiles take the SMs first
