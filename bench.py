@@ -69,11 +69,11 @@ FP4_PER_BF16 = 6.0  # nominal dense FP4 / bf16 tensor ratio on GB300 (13.5 / 2.2
 # held in L2 when a kernel ends do not appear in its DRAM bytes.
 NCU_TRAFFIC = {"gemm": {"bytes": 292.44e6, "src": "ff8a151e85c2daa4",
                         "files": ["gemm_sm103.cu", "async_sm103.cuh", "fp4_device.cuh", "device_cache.h"]},
-               "quant_dual": {"bytes": 803.50e6, "src": "840727fbb2b2a143",
+               "quant_dual": {"bytes": 803.50e6, "src": "c7678099edfacfa1",
                               "files": ["quantize.cu", "async_sm103.cuh", "fp4_device.cuh", "device_cache.h"]},
                "gemv": {"bytes": 25.46e6, "src": "fe1ed2b164c87513",
                         "files": ["gemv.cu", "async_sm103.cuh", "fp4_device.cuh", "device_cache.h"]},
-               "amax": {"bytes": 586.22e6, "src": "840727fbb2b2a143",
+               "amax": {"bytes": 586.87e6, "src": "c7678099edfacfa1",
                         "files": ["quantize.cu", "async_sm103.cuh", "fp4_device.cuh", "device_cache.h"]}}
 
 
